@@ -1,0 +1,256 @@
+/*
+ * pagedkv.h - C ABI of libpagedkv.so: paged KV-cache decode attention, the two
+ * kernels that keep the paged cache consistent, and the host block allocator.
+ *
+ * Method: W. Kwon et al., "Efficient Memory Management for Large Language Model
+ * Serving with PagedAttention" (SOSP 2023).  Citations below name the web page
+ * that restates it and the section on that page:
+ *   [P1]  phantomic12.github.io, paper note, method paragraph
+ *   [P3a] zeroshotmind.com, "Paging the cache"
+ *   [P3b] zeroshotmind.com, "Block tables: logical order, physical scatter"
+ *   [P3c] zeroshotmind.com, "Sharing a prefix without copying it"
+ *   [P3d] zeroshotmind.com, "The fragmentation arithmetic"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every buffer is owned by the caller.  Pointers marked "device" must
+ *   point to memory of the current CUDA device; "host" pointers to host memory.
+ *   The library never allocates device memory.
+ * - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Kernel entry points are asynchronous on that stream: they return
+ *   once the work is enqueued.
+ * - Return value: a pa_status.  Host-side argument checks fail synchronously
+ *   with PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and enqueue nothing.
+ *   PA_ERR_CUDA means a CUDA call or launch failed (cudaGetLastError()).
+ * - Device-side checks: indices read from device memory (block-table entries,
+ *   slots, copy pairs, sequence lengths) are range-checked by the kernels on
+ *   every launch.  A bad index is never dereferenced: it is clamped (decode:
+ *   block 0 is read instead) or the element is skipped (append, copy), and the
+ *   violation is recorded in the caller's device error record if one is given.
+ *   Nothing traps.  Kernels that wait on a barrier give up after about one
+ *   second, record PA_ERR_TIMEOUT and return.
+ * - Device error record: int32_t[PA_ERROR_RECORD_WORDS] in device memory,
+ *   zeroed by the caller (pa_error_clear).  Word 0: first error code (0 = none);
+ *   word 1: number of violations; word 2: index of the first violation
+ *   (sequence, token or pair number); word 3: the offending value (truncated to
+ *   32 bits).  May be NULL: checks still clamp/skip, nothing is recorded.
+ * - Cache layout (one layer): k_cache and v_cache are each
+ *   [num_blocks][num_heads][block_size][head_dim], contiguous, row-major.
+ *   Slot s is row (s % block_size) of physical block (s / block_size) [P3a].
+ * - dtypes: K/V/Q storage is PA_F16 or PA_BF16; outputs may also be PA_F32.
+ *   All attention arithmetic is fp32.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAGEDKV_VERSION 1
+#define PA_ERROR_RECORD_WORDS 4
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* bad size, pointer, alignment or combination */
+  PA_ERR_UNSUPPORTED = 2,  /* well-formed but not built (head_dim, block_size, dtype) */
+  PA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  PA_ERR_BAD_BLOCK = 4,    /* device: block number outside [0, num_blocks) */
+  PA_ERR_BAD_SLOT = 5,     /* device: slot >= num_blocks * block_size */
+  PA_ERR_BAD_SEQ_LEN = 6,  /* device: seq_len < 0 or > max_blocks_per_seq * block_size */
+  PA_ERR_TIMEOUT = 7,      /* device: a bounded wait ran out; the kernel bailed out */
+  PA_ERR_OOM = 8,          /* allocator: not enough free blocks */
+  PA_ERR_NO_SEQ = 9,       /* allocator: unknown sequence id */
+  PA_ERR_SEQ_EXISTS = 10,  /* allocator: sequence id already in use */
+  PA_ERR_REFCOUNT = 11     /* allocator: a reference count or free list is inconsistent */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+
+/* ---------------------------------------------------------------------------
+ * Library information and device error records
+ * ------------------------------------------------------------------------- */
+
+/* PAGEDKV_VERSION of the loaded library. */
+int pa_version(void);
+
+/* Static English text for a pa_status value (never NULL). */
+const char* pa_status_string(int status);
+
+/* Enqueue a zero-fill of a device error record on `stream`. */
+int pa_error_clear(int32_t* error_record, void* stream);
+
+/* Copy a device error record into host_out[PA_ERROR_RECORD_WORDS]; waits for
+ * `stream` to finish first, so it reports every kernel enqueued before it. */
+int pa_error_read(const int32_t* error_record, int32_t* host_out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decode attention through a block table  [P1], [P3b]
+ *
+ * For every sequence i and head h, with L = seq_lens[i]:
+ *   token t (0 <= t < L) is row (t % block_size) of physical block
+ *   block_tables[i * max_blocks_per_seq + t / block_size];
+ *   s_t = scale * <q[i][h], k_t>,  out[i][h] = sum_t softmax(s)_t * v_t.
+ * Attention walks the logical blocks in order; where they sit in the pool does
+ * not matter [P3b].  L = 0 gives an all-zero output row.
+ *
+ * Arguments
+ *   q             device, [num_seqs][num_heads][head_dim] in `dtype`, 16-byte aligned
+ *   k_cache, v_cache  device, [num_blocks][num_heads][block_size][head_dim] in `dtype`,
+ *                 16-byte aligned; read only
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(L / block_size) are never read
+ *   seq_lens      device int32 [num_seqs]; each in [0, max_blocks_per_seq * block_size]
+ *   head_dim      64, 128 or 256;  block_size: a multiple of 16
+ *   scale         the softmax scale, usually 1/sqrt(head_dim)
+ *   out           device [num_seqs][num_heads][head_dim] in `out_dtype`, 16-byte aligned
+ *   partition_tokens  split-K partition length: 0 = automatic (512); otherwise a
+ *                 positive multiple of 16.  When max_blocks_per_seq * block_size
+ *                 fits in one partition, a single pass writes `out` directly.
+ *                 Otherwise a first kernel computes per-partition partials and a
+ *                 second merges them by log-sum-exp.
+ *   workspace     device, 16-byte aligned, at least paged_attn_workspace_size(...)
+ *                 bytes; may be NULL when that size is 0.  Scratch only.
+ *   error_record  device error record or NULL.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of workspace paged_attn_decode needs for these sizes (0 if none). */
+size_t paged_attn_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int partition_tokens);
+
+int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                      int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                      int num_blocks, float scale, int dtype, void* out, int out_dtype,
+                      int partition_tokens, void* workspace, size_t workspace_bytes,
+                      int32_t* error_record, void* stream);
+
+/* Launch tuning and phase selection for paged_attn_decode_ex.  Zero fields take
+ * the automatic choice.
+ *   heads_per_cta  heads handled by one thread block (must divide num_heads, <= 8)
+ *   stages         shared-memory pipeline depth, 2..8
+ *   phases         0 or 3: both passes; 1: partition pass only; 2: merge pass only.
+ * With split-K, the partition pass leaves in the workspace, for partition p of
+ * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
+ * max_blocks_per_seq * block_size / partition_tokens)):
+ *   float acc[row][head_dim]  at byte 0:  sum_t 2^(u_t - m) * v_t
+ *   float2 ml[row] after all acc rows:   (m, l) with u_t = s_t * log2(e),
+ *                                        m = max_t u_t, l = sum_t 2^(u_t - m)
+ * over the tokens t of that partition.  Partitions at or past
+ * ceil(L / partition_tokens) are not written. */
+typedef struct pa_decode_opts {
+  int heads_per_cta;
+  int stages;
+  int phases;
+} pa_decode_opts;
+
+int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                         int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                         int num_blocks, float scale, int dtype, void* out, int out_dtype,
+                         int partition_tokens, void* workspace, size_t workspace_bytes,
+                         int32_t* error_record, void* stream, const pa_decode_opts* opts);
+
+/* ---------------------------------------------------------------------------
+ * KV append into slot-mapped blocks  [P3a]
+ *
+ * For each token t < num_tokens with slot = slot_mapping[t] >= 0, and every head h:
+ *   k_cache[slot / block_size][h][slot % block_size][:] = k[t][h][:]   (bit copy)
+ *   v_cache[...] likewise.
+ * A negative slot marks a padding token: nothing is written.  A slot >=
+ * num_blocks * block_size is recorded as PA_ERR_BAD_SLOT and skipped.  Two
+ * tokens with the same slot race (one of them wins).
+ *   k, v          device [num_tokens][num_heads][head_dim] in `dtype`, 16-byte aligned
+ *   slot_mapping  device int64 [num_tokens]
+ *   head_dim      a multiple of 8 (rows are moved in 16-byte pieces)
+ * ------------------------------------------------------------------------- */
+int kv_cache_append(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                    void* k_cache, void* v_cache, int num_heads, int head_dim, int block_size,
+                    int num_blocks, int dtype, int32_t* error_record, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Copy-on-write block copy  [P3c]
+ *
+ * For each pair j < num_pairs, (src, dst) = (pairs[2j], pairs[2j+1]), and each
+ * layer l < num_layers: block dst of k_caches[l] and of v_caches[l] becomes a bit
+ * copy of block src (all heads, rows and elements).  Destinations must be
+ * distinct and no destination may be a source in the same call (the allocator
+ * guarantees this: a destination is always a block just taken off the free
+ * list); otherwise the result is undefined.  A pair with a block outside
+ * [0, num_blocks) is recorded as PA_ERR_BAD_BLOCK and skipped.
+ *   k_caches, v_caches  HOST arrays of num_layers device pointers (1..128 layers),
+ *                 each cache laid out as above, 16-byte aligned
+ *   pairs         device int64 [num_pairs][2]
+ * ------------------------------------------------------------------------- */
+int block_copy(void* const* k_caches, void* const* v_caches, int num_layers,
+               const int64_t* pairs, int num_pairs, int num_heads, int head_dim, int block_size,
+               int num_blocks, int dtype, int32_t* error_record, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block allocator  [P1], [P3a], [P3c], [P3d]
+ *
+ * Host-only C++ (no device code, no CUDA calls).  Tracks, for a pool of
+ * num_blocks blocks of block_size tokens: a free list, a reference count per
+ * block, and per sequence (an int64 id) its block table and length.
+ *  - A sequence holds exactly ceil(len / block_size) blocks, so at most
+ *    block_size - 1 slots are unused, all in its last block [P3a], [P3d].
+ *  - A block's reference count is the number of sequences holding it [P3c].
+ *  - Appending into a partly filled last block that others also hold first
+ *    moves the appender onto a fresh copy of that one block (copy-on-write):
+ *    the call returns the (src, dst) pair for block_copy [P3c].
+ *  - The free list is a stack.  Blocks are first handed out in `free_order`
+ *    order (or 0, 1, 2, ... when NULL) and freed blocks go back on top.
+ * An allocator object is not thread-safe; calls on distinct objects are
+ * independent.  All pointers are host pointers.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_allocator pa_allocator;
+
+/* NULL on bad arguments (num_blocks or block_size <= 0, free_order not a
+ * permutation of 0..num_blocks-1) or when out of host memory. */
+pa_allocator* pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order);
+void pa_alloc_destroy(pa_allocator* a);
+
+/* New sequence of num_tokens tokens: takes ceil(num_tokens / block_size) blocks. */
+int pa_seq_add(pa_allocator* a, int64_t seq, int32_t num_tokens);
+/* child shares every block of parent (each count + 1); child starts at parent's length. */
+int pa_seq_fork(pa_allocator* a, int64_t parent, int64_t child);
+/* Reserve the slot of seq's next token.  *slot = block * block_size + row.  If the
+ * token goes into a shared partly filled block, *cow_src / *cow_dst receive the
+ * block pair to copy before writing; otherwise both are -1.  cow_* may be NULL. */
+int pa_seq_append(pa_allocator* a, int64_t seq, int64_t* slot, int32_t* cow_src,
+                  int32_t* cow_dst);
+/* End a sequence: every block's count - 1; blocks reaching 0 return to the free list. */
+int pa_seq_free(pa_allocator* a, int64_t seq);
+int pa_seq_len(const pa_allocator* a, int64_t seq, int32_t* len);
+/* Copy up to `capacity` table entries into out; *num_blocks = the table's length. */
+int pa_seq_block_table(const pa_allocator* a, int64_t seq, int32_t* out, int32_t capacity,
+                       int32_t* num_blocks);
+/* Slots of positions [start, start + count) of seq (all < its length). */
+int pa_seq_slots(const pa_allocator* a, int64_t seq, int32_t start, int32_t count,
+                 int64_t* slots);
+int pa_block_refcount(const pa_allocator* a, int32_t block, int32_t* refcount);
+int32_t pa_num_free_blocks(const pa_allocator* a);
+int32_t pa_num_seqs(const pa_allocator* a);
+
+/* One append per listed sequence, in order.  slots[n]; cow_pairs[2 * n] receives
+ * the copy pairs packed at the front, *num_cow their number.  All-or-nothing:
+ * if the free list cannot cover the worst case, returns PA_ERR_OOM and changes
+ * nothing. */
+int pa_batch_append(pa_allocator* a, const int64_t* seqs, int32_t n, int64_t* slots,
+                    int64_t* cow_pairs, int32_t* num_cow);
+/* Block tables of the listed sequences as rows of tables[n][max_blocks] (entries
+ * past a table's end are -1) and their lengths. PA_ERR_INVALID_ARG if a table
+ * does not fit. */
+int pa_batch_block_tables(const pa_allocator* a, const int64_t* seqs, int32_t n,
+                          int32_t max_blocks, int32_t* tables, int32_t* seq_lens);
+/* Verify every invariant above; PA_OK or PA_ERR_REFCOUNT. */
+int pa_alloc_check(const pa_allocator* a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

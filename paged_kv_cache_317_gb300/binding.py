@@ -1,0 +1,305 @@
+"""Thin ctypes binding over libpagedkv.so, with the C ABI's names.
+
+Argument marshalling only: tensors are passed by ``data_ptr()``, sizes are read
+off their shapes, and the stream is the caller's current CUDA stream.  Every
+step of the path runs in the library's kernels; there is no fallback.  If the
+library is missing, loading it raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import _build
+
+c_int, c_int32, c_int64, c_float, c_size_t, c_void_p = (
+    ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p)
+P_int32 = ctypes.POINTER(ctypes.c_int32)
+P_int64 = ctypes.POINTER(ctypes.c_int64)
+
+PA_F16, PA_BF16, PA_F32 = 0, 1, 2
+_DTYPE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+
+STATUS = {
+    0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA",
+    4: "PA_ERR_BAD_BLOCK", 5: "PA_ERR_BAD_SLOT", 6: "PA_ERR_BAD_SEQ_LEN", 7: "PA_ERR_TIMEOUT",
+    8: "PA_ERR_OOM", 9: "PA_ERR_NO_SEQ", 10: "PA_ERR_SEQ_EXISTS", 11: "PA_ERR_REFCOUNT",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+
+class pa_decode_opts(ctypes.Structure):
+    _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int)]
+
+
+# name -> (restype, argtypes); mirrors include/pagedkv.h
+SIGNATURES = {
+    "pa_version": (c_int, []),
+    "pa_status_string": (ctypes.c_char_p, [c_int]),
+    "pa_error_clear": (c_int, [c_void_p, c_void_p]),
+    "pa_error_read": (c_int, [c_void_p, P_int32, c_void_p]),
+    "paged_attn_workspace_size": (c_size_t, [c_int] * 6),
+    "paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                  c_int, c_int, c_int, c_int, c_float, c_int, c_void_p, c_int,
+                                  c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "paged_attn_decode_ex": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                     c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p,
+                                     c_int, c_int, c_void_p, c_size_t, c_void_p, c_void_p,
+                                     ctypes.POINTER(pa_decode_opts)]),
+    "kv_cache_append": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "block_copy": (c_int, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int, c_void_p,
+                           c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "pa_alloc_create": (c_void_p, [c_int32, c_int32, P_int32]),
+    "pa_alloc_destroy": (None, [c_void_p]),
+    "pa_seq_add": (c_int, [c_void_p, c_int64, c_int32]),
+    "pa_seq_fork": (c_int, [c_void_p, c_int64, c_int64]),
+    "pa_seq_append": (c_int, [c_void_p, c_int64, P_int64, P_int32, P_int32]),
+    "pa_seq_free": (c_int, [c_void_p, c_int64]),
+    "pa_seq_len": (c_int, [c_void_p, c_int64, P_int32]),
+    "pa_seq_block_table": (c_int, [c_void_p, c_int64, P_int32, c_int32, P_int32]),
+    "pa_seq_slots": (c_int, [c_void_p, c_int64, c_int32, c_int32, P_int64]),
+    "pa_block_refcount": (c_int, [c_void_p, c_int32, P_int32]),
+    "pa_num_free_blocks": (c_int32, [c_void_p]),
+    "pa_num_seqs": (c_int32, [c_void_p]),
+    "pa_batch_append": (c_int, [c_void_p, P_int64, c_int32, P_int64, P_int64, P_int32]),
+    "pa_batch_block_tables": (c_int, [c_void_p, P_int64, c_int32, c_int32, P_int32, P_int32]),
+    "pa_alloc_check": (c_int, [c_void_p]),
+}
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name} ({_status_text(status)})")
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load_library().pa_status_string(status).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return "?"
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libpagedkv.so from the package directory; raise if it was not built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"{_build.LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise PagedKVError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# --------------------------------------------------------------- error record
+def new_error_record(device="cuda") -> torch.Tensor:
+    return torch.zeros(4, dtype=torch.int32, device=device)
+
+
+def pa_error_clear(record: torch.Tensor, stream=None) -> None:
+    _check(load_library().pa_error_clear(_ptr(record), _stream(stream)), "pa_error_clear")
+
+
+def pa_error_read(record: torch.Tensor, stream=None):
+    out = (ctypes.c_int32 * 4)()
+    _check(load_library().pa_error_read(_ptr(record), out, _stream(stream)), "pa_error_read")
+    return list(out)
+
+
+# ----------------------------------------------------------------- decode
+def paged_attn_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                              partition_tokens=0) -> int:
+    return int(load_library().paged_attn_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                                        max_blocks_per_seq, partition_tokens))
+
+
+def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
+                      partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                      error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
+                      stages: int = 0, phases: int = 0, stream=None) -> torch.Tensor:
+    """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N]."""
+    N, H, D = q.shape
+    B, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if out is None:
+        out = torch.empty((N, H, D), dtype=out_dtype, device=q.device)
+    _need(out, "out")
+    need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    opts = pa_decode_opts(heads_per_cta, stages, phases)
+    st = load_library().paged_attn_decode_ex(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
+        MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
+        _ptr(workspace), ws_bytes, _ptr(error_record), _stream(stream), ctypes.byref(opts))
+    _check(st, "paged_attn_decode")
+    return out
+
+
+# ------------------------------------------------------------ cache upkeep
+def kv_cache_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    error_record: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k, v [T,H,D]; slot_mapping int64 [T]; caches [B,H,bs,D]."""
+    T, H, D = k.shape
+    B, _, bs, _ = k_cache.shape
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    st = load_library().kv_cache_append(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache),
+                                        _ptr(v_cache), H, D, bs, B, _DTYPE[k.dtype],
+                                        _ptr(error_record), _stream(stream))
+    _check(st, "kv_cache_append")
+
+
+def block_copy(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],
+               pairs: torch.Tensor, error_record: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    """Per-layer caches [B,H,bs,D]; pairs int64 [n,2] (src, dst) on the device."""
+    n_layers = len(k_caches)
+    B, H, bs, D = k_caches[0].shape
+    for t in (*k_caches, *v_caches):
+        _need(t, "cache")
+    _need(pairs, "pairs", torch.int64)
+    kp = (c_void_p * n_layers)(*[t.data_ptr() for t in k_caches])
+    vp = (c_void_p * n_layers)(*[t.data_ptr() for t in v_caches])
+    st = load_library().block_copy(kp, vp, n_layers, _ptr(pairs), int(pairs.shape[0]), H, D, bs,
+                                   B, _DTYPE[k_caches[0].dtype], _ptr(error_record),
+                                   _stream(stream))
+    _check(st, "block_copy")
+
+
+# --------------------------------------------------------------- allocator
+class BlockAllocator:
+    """Host block allocator (C++), see pa_alloc_* in include/pagedkv.h."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self._lib = load_library()
+        arr = None
+        if free_order is not None:
+            arr = (ctypes.c_int32 * num_blocks)(*[int(b) for b in free_order])
+        self._h = self._lib.pa_alloc_create(num_blocks, block_size, arr)
+        if not self._h:
+            raise PagedKVError(1, "pa_alloc_create")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_alloc_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def add(self, seq: int, num_tokens: int) -> None:
+        _check(self._lib.pa_seq_add(self._h, seq, num_tokens), "pa_seq_add")
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(self._lib.pa_seq_fork(self._h, parent, child), "pa_seq_fork")
+
+    def append(self, seq: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pa_seq_append(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                       ctypes.byref(dst)), "pa_seq_append")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def free(self, seq: int) -> None:
+        _check(self._lib.pa_seq_free(self._h, seq), "pa_seq_free")
+
+    def length(self, seq: int) -> int:
+        n = ctypes.c_int32()
+        _check(self._lib.pa_seq_len(self._h, seq, ctypes.byref(n)), "pa_seq_len")
+        return n.value
+
+    def block_table(self, seq: int):
+        n = ctypes.c_int32()
+        _check(self._lib.pa_seq_block_table(self._h, seq, None, 0, ctypes.byref(n)), "table")
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        _check(self._lib.pa_seq_block_table(self._h, seq, buf, n.value, ctypes.byref(n)), "table")
+        return list(buf[: n.value])
+
+    def slots(self, seq: int, start: int, count: int):
+        import numpy as np
+        out = np.empty(count, dtype=np.int64)
+        _check(self._lib.pa_seq_slots(self._h, seq, start, count,
+                                      out.ctypes.data_as(P_int64)), "pa_seq_slots")
+        return out
+
+    def refcount(self, block: int) -> int:
+        n = ctypes.c_int32()
+        _check(self._lib.pa_block_refcount(self._h, block, ctypes.byref(n)), "pa_block_refcount")
+        return n.value
+
+    def num_free(self) -> int:
+        return int(self._lib.pa_num_free_blocks(self._h))
+
+    def num_seqs(self) -> int:
+        return int(self._lib.pa_num_seqs(self._h))
+
+    def batch_append(self, seqs):
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = ids.shape[0]
+        slots = np.empty(n, dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+        nc = ctypes.c_int32()
+        _check(self._lib.pa_batch_append(self._h, ids.ctypes.data_as(P_int64), n,
+                                         slots.ctypes.data_as(P_int64),
+                                         pairs.ctypes.data_as(P_int64), ctypes.byref(nc)),
+               "pa_batch_append")
+        return slots, pairs[: nc.value].copy()
+
+    def batch_block_tables(self, seqs, max_blocks: int):
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = ids.shape[0]
+        tables = np.empty((n, max_blocks), dtype=np.int32)
+        lens = np.empty(n, dtype=np.int32)
+        _check(self._lib.pa_batch_block_tables(self._h, ids.ctypes.data_as(P_int64), n, max_blocks,
+                                               tables.ctypes.data_as(P_int32),
+                                               lens.ctypes.data_as(P_int32)),
+               "pa_batch_block_tables")
+        return tables, lens
+
+    def check(self) -> None:
+        _check(self._lib.pa_alloc_check(self._h), "pa_alloc_check")

@@ -1,0 +1,209 @@
+"""CPU tests of the C ABI: the library loads, exports every function the header
+declares, rejects malformed arguments on the host, and its host allocator
+matches the oracle's allocator model operation for operation."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.allocator_model import AllocatorError, BlockAllocatorModel
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(HEADER_DIR):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, re.M):
+            if m.group(1) not in ("defined",):
+                names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_functions()
+    for required in ("paged_attn_decode", "kv_cache_append", "block_copy",
+                     "paged_attn_workspace_size", "pa_alloc_create", "pa_seq_append"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    from paged_kv_cache_317_gb300.binding import STATUS
+    assert lib.pa_version() == 1
+    for code in STATUS:
+        assert lib.pa_status_string(code)
+    assert lib.pa_status_string(999) == b"unknown status"
+
+
+def test_workspace_size_arithmetic(lib):
+    # 256 seqs, 40 heads, D 128, capacity 129 blocks * 16 = 2064 tokens -> 5 partitions of 512
+    rows = 256 * 40 * 5
+    assert lib.paged_attn_workspace_size(256, 40, 128, 16, 129, 0) == rows * 128 * 4 + rows * 8
+    # the whole capacity fits one partition: no workspace
+    assert lib.paged_attn_workspace_size(4, 8, 64, 16, 32, 512) == 0
+    assert lib.paged_attn_workspace_size(4, 8, 64, 16, 33, 512) == 4 * 8 * 2 * (64 * 4 + 8)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    from paged_kv_cache_317_gb300.binding import STATUS_CODE
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    INV, UNS = STATUS_CODE["PA_ERR_INVALID_ARG"], STATUS_CODE["PA_ERR_UNSUPPORTED"]
+
+    def call(**kw):
+        a = dict(q=p, k=p, v=p, bt=p, sl=p, N=4, H=8, D=64, bs=16, MB=4, B=64, scale=0.125,
+                 dt=0, out=p, odt=2, pt=0, ws=None, wsb=0)
+        a.update(kw)
+        return lib.paged_attn_decode(a["q"], a["k"], a["v"], a["bt"], a["sl"], a["N"], a["H"],
+                                     a["D"], a["bs"], a["MB"], a["B"], a["scale"], a["dt"],
+                                     a["out"], a["odt"], a["pt"], a["ws"], a["wsb"], None, None)
+
+    assert call(D=96) == UNS
+    assert call(bs=8) == UNS
+    assert call(dt=2) == UNS
+    assert call(odt=7) == UNS
+    assert call(q=None) == INV
+    assert call(q=ctypes.c_void_p((1 << 20) + 8)) == INV      # not 16-byte aligned
+    assert call(pt=100) == INV                                # not a multiple of 16
+    assert call(MB=64) == INV                                 # needs a workspace, none given
+    assert call(H=0) == INV
+    assert call(scale=float("nan")) == INV
+    assert call(N=0) == 0                                     # nothing to do
+
+
+def test_append_and_copy_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.kv_cache_append(p, p, p, 4, p, p, 8, 60, 16, 64, 0, None, None) == 2  # D % 8
+    assert lib.kv_cache_append(p, p, p, -1, p, p, 8, 64, 16, 64, 0, None, None) == 1
+    assert lib.kv_cache_append(p, p, p, 0, p, p, 8, 64, 16, 64, 0, None, None) == 0
+    arr = (ctypes.c_void_p * 1)(1 << 20)
+    assert lib.block_copy(arr, arr, 0, p, 1, 8, 64, 16, 64, 0, None, None) == 1
+    assert lib.block_copy(arr, arr, 129, p, 1, 8, 64, 16, 64, 0, None, None) == 1
+    assert lib.block_copy(arr, arr, 1, p, 0, 8, 64, 16, 64, 0, None, None) == 0
+
+
+def test_allocator_create_rejects_non_permutations(lib):
+    bad = (ctypes.c_int32 * 3)(0, 0, 1)
+    assert not lib.pa_alloc_create(3, 4, bad)
+    assert not lib.pa_alloc_create(0, 4, None)
+    h = lib.pa_alloc_create(3, 4, (ctypes.c_int32 * 3)(2, 0, 1))
+    assert h
+    lib.pa_alloc_destroy(h)
+
+
+def _same_state(cpp, model):
+    for s in model.tables:
+        assert cpp.block_table(s) == model.tables[s]
+        assert cpp.length(s) == model.lens[s]
+    for b in range(model.num_blocks):
+        assert cpp.refcount(b) == model.refcount[b]
+    assert cpp.num_free() == len(model.free)
+    assert cpp.num_seqs() == len(model.tables)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_cpp_allocator_matches_the_model(lib, seed):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator, PagedKVError
+    rng = np.random.default_rng(100 + seed)
+    nb, bs = 120, int(rng.choice([1, 4, 16]))
+    order = rng.permutation(nb)
+    cpp, model = BlockAllocator(nb, bs, order), BlockAllocatorModel(nb, bs, order)
+    next_id = 0
+    for _ in range(600):
+        live = list(model.tables)
+        op = int(rng.integers(0, 5))
+        if op == 0 or not live:
+            n = int(rng.integers(0, 30))
+            try:
+                model.add(next_id, n)
+                ok = True
+            except AllocatorError:
+                ok = False
+            if ok:
+                cpp.add(next_id, n)
+            else:
+                with pytest.raises(PagedKVError):
+                    cpp.add(next_id, n)
+            next_id += 1
+        elif op == 1:
+            p = live[int(rng.integers(len(live)))]
+            model.fork(p, next_id)
+            cpp.fork(p, next_id)
+            next_id += 1
+        elif op in (2, 3):
+            s = live[int(rng.integers(len(live)))]
+            try:
+                expect = model.append(s)
+            except AllocatorError:
+                expect = None
+            if expect is None:
+                with pytest.raises(PagedKVError):
+                    cpp.append(s)
+            else:
+                assert cpp.append(s) == expect
+        else:
+            s = live[int(rng.integers(len(live)))]
+            model.free_seq(s)
+            cpp.free(s)
+        cpp.check()
+    _same_state(cpp, model)
+
+
+def test_batch_append_matches_sequential_appends(lib):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator
+    bs = 16
+    cpp, model = BlockAllocator(400, bs), BlockAllocatorModel(400, bs)
+    for s, n in enumerate([1029, 16, 33, 0]):
+        cpp.add(s, n)
+        model.add(s, n)
+    for child in range(4, 11):                       # 7 forks of the partly filled prompt
+        cpp.fork(0, child)
+        model.fork(0, child)
+    seqs = [0, 4, 5, 6, 7, 8, 9, 10, 1, 2, 3, 2]     # sequence 2 twice
+    slots, pairs = cpp.batch_append(seqs)
+    want = [model.append(s) for s in seqs]
+    assert slots.tolist() == [w[0] for w in want]
+    assert [tuple(p) for p in pairs.tolist()] == [w[1] for w in want if w[1] is not None]
+    assert len(pairs) == 7                           # 8 holders of one partial block
+    tables, lens = cpp.batch_block_tables(list(range(11)), 70)
+    for s in range(11):
+        assert tables[s, : len(model.tables[s])].tolist() == model.tables[s]
+        assert (tables[s, len(model.tables[s]):] == -1).all()
+        assert lens[s] == model.lens[s]
+    cpp.check()
+
+
+def test_batch_append_is_all_or_nothing_when_out_of_blocks(lib):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator, PagedKVError
+    cpp = BlockAllocator(3, 4)
+    cpp.add(0, 4)
+    cpp.add(1, 4)                                    # one block left, two appends need two
+    before = (cpp.block_table(0), cpp.block_table(1), cpp.num_free())
+    with pytest.raises(PagedKVError) as e:
+        cpp.batch_append([0, 1])
+    assert e.value.name == "PA_ERR_OOM"
+    assert (cpp.block_table(0), cpp.block_table(1), cpp.num_free()) == before
+
+
+def test_allocator_error_codes(lib):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator, PagedKVError
+    a = BlockAllocator(4, 4)
+    a.add(1, 3)
+    for fn, args, name in ((a.add, (1, 2), "PA_ERR_SEQ_EXISTS"), (a.fork, (9, 2), "PA_ERR_NO_SEQ"),
+                           (a.free, (9,), "PA_ERR_NO_SEQ"), (a.add, (2, 100), "PA_ERR_OOM")):
+        with pytest.raises(PagedKVError) as e:
+            fn(*args)
+        assert e.value.name == name
+    assert a.slots(1, 0, 3).tolist() == [a.block_table(1)[0] * 4 + i for i in range(3)]
