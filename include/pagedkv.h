@@ -154,6 +154,30 @@ int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache
                          int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* error_record, void* stream, const pa_decode_opts* opts);
 
+/* Decode without allocation.  No counterpart in the paper: this is a library
+ * convenience.  Some callers cannot allocate device memory - code running
+ * inside another runtime whose pool owns all device memory, a serving loop that
+ * must never block in cudaMalloc/cudaFree (they can synchronise the device), or
+ * a deployment whose device memory budget is fixed at start-up.  This call is
+ * paged_attn_decode with the workspace taken from a fixed array of
+ * PA_NOALLOC_SCRATCH_BYTES compiled into the library, so it allocates nothing.
+ *  - Limit: returns PA_ERR_INVALID_ARG, enqueuing nothing, when
+ *    paged_attn_workspace_size(...) for these sizes exceeds PA_NOALLOC_SCRATCH_BYTES.
+ *  - The array stays resident on every GPU that loads this code until exit.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call before
+ *    any stream capture.
+ *  - All calls share the array and it keeps the last call's contents (nothing
+ *    in it needs clearing: every partial is written before it is read).  Calls
+ *    whose kernels overlap on the GPU race on it: serialise them.
+ * Other arguments, errors and results: as paged_attn_decode. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                              int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                              int num_blocks, float scale, int dtype, void* out, int out_dtype,
+                              int partition_tokens, int32_t* error_record, void* stream);
+
 /* ---------------------------------------------------------------------------
  * KV append into slot-mapped blocks  [P3a]
  *

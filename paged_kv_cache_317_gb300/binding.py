@@ -50,6 +50,9 @@ SIGNATURES = {
                                      c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p,
                                      c_int, c_int, c_void_p, c_size_t, c_void_p, c_void_p,
                                      ctypes.POINTER(pa_decode_opts)]),
+    "paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                          c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]),
     "kv_cache_append": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                 c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "block_copy": (c_int, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int, c_void_p,
@@ -174,6 +177,30 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
         _ptr(workspace), ws_bytes, _ptr(error_record), _stream(stream), ctypes.byref(opts))
     _check(st, "paged_attn_decode")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def paged_attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                              out: torch.Tensor, partition_tokens: int = 0,
+                              error_record: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """paged_attn_decode with its scratch taken from the library's fixed array:
+    allocates nothing (``out`` must be given)."""
+    N, H, D = q.shape
+    B, _, bs, _ = k_cache.shape
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _need(t, n)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    st = load_library().paged_attn_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
+        block_tables.shape[1], B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype],
+        partition_tokens, _ptr(error_record), _stream(stream))
+    _check(st, "paged_attn_decode_noalloc")
     return out
 
 
