@@ -1,0 +1,69 @@
+"""CPU tests of bench.py's host logic: byte accounting, clock parsing, and the
+multi-rank reductions (two gloo ranks on 127.0.0.1)."""
+
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_step_bytes_by_hand():
+    # two sequences: 20 tokens (1 partition of 512) and 600 tokens (2 partitions)
+    b = bench.step_bytes([20, 600], num_heads=2, head_dim=8, block_size=16, partition_tokens=512)
+    kv = (20 + 600) * 2 * 8 * 2 * 2
+    assert b["kv"] == kv
+    partials = 2 * 2 * (8 + 2) * 4                      # 2 partitions x 2 heads of (D + m, l) fp32
+    table = (2 + 38) * 4
+    q = 2 * 2 * 8 * 2
+    assert b["decode_partition"] == kv + q + table + 2 * 4 + 1 * 2 * 8 * 2 + partials
+    assert b["decode_merge"] == partials + 1 * 2 * 8 * 2 + 2 * 4
+    assert b["append"] == 2 * (2 * 2 * 2 * 8 * 2) + 2 * 8
+    assert b["total"] == b["decode_partition"] + b["decode_merge"] + b["append"]
+
+
+def test_clock_rows_parse_reasons_and_median():
+    rows = "\n".join([
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1900, 2070, 1300.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2000, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ])
+    c = bench.parse_clock_rows(rows)
+    assert c == {"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_rank_seeds_differ():
+    assert len({bench.rank_seed(2, r) for r in range(8)}) == 8
+    assert bench.rank_seed(2, 0) == 2
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, lr = bench.dist_env()
+    bench.barrier(w)
+    mx = bench.reduce_max(1.5 + r, w)
+    sm = bench.reduce_sum(10.0 * (r + 1), w)
+    q.put((r, w, lr, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_max_and_sum():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 2, 0, 2.5, 30.0), (1, 2, 1, 2.5, 30.0)]
