@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Benchmark of the paged KV-cache decode step on the 13B-shaped workload.
 
-One step = kv_cache_append of one new token per sequence, then
-paged_attn_decode over every sequence (partition kernel + log-sum-exp merge),
+One step = one new token appended per sequence and a decode over every
+sequence, through paged_attn_decode_append (fused append + partition kernel,
+then the log-sum-exp merge kernel),
 on 256 sequences x 40 heads x head_dim 128, bf16, block size 16, lengths
 log-normal (median 350) clipped to [16, 2048], blocks scattered over a pool 1.2x
 the live tokens.  The KV pool (2.4 GB read per step) is larger than L2, so no
@@ -78,13 +79,14 @@ def barrier(world: int) -> None:
 
 
 def step_bytes(lens, num_heads, head_dim, block_size, elt=2, out_elt=2, partition_tokens=512):
-    """Algorithmic bytes of one step, split by kernel.
+    """Algorithmic bytes of one fused step (paged_attn_decode_append), by kernel.
 
-    decode partition pass: every live K and V row once, q, the table entries it
-    follows, the lengths, and what it writes (the output row of a one-partition
-    sequence, else an fp32 partial (D floats + m, l) per partition).
-    merge pass: the partials of split sequences, and their output rows.
-    append: the new k and v rows read, the same bytes written, the slots.
+    partition pass: every context K and V row once (the last one from new_k/new_v,
+    the rest from the cache), q, the table entries it follows, the lengths, the
+    appended rows written into the cache, and what it writes out (the output row
+    of a one-partition sequence, else an fp32 partial of D floats + (m, l) per
+    partition).  merge pass: the partials of split sequences, their output rows
+    and the lengths.
     """
     import numpy as np
     lens = np.asarray(lens, dtype=np.int64)
@@ -97,11 +99,11 @@ def step_bytes(lens, num_heads, head_dim, block_size, elt=2, out_elt=2, partitio
     out_merged = int(split.sum()) * H * D * out_elt
     table = int((-(-lens // block_size)).sum()) * 4
     q = N * H * D * elt
-    partition = kv + q + table + N * 4 + out_direct + partial_bytes
+    append_write = 2 * N * H * D * elt
+    partition = kv + q + table + N * 4 + out_direct + partial_bytes + append_write
     merge = partial_bytes + out_merged + N * 4
-    append = 2 * (2 * N * H * D * elt) + N * 8
-    return {"decode_partition": partition, "decode_merge": merge, "append": append,
-            "kv": kv, "total": partition + merge + append}
+    return {"decode_partition": partition, "decode_merge": merge, "append_write": append_write,
+            "kv": kv, "total": partition + merge}
 
 
 def measured_hbm_peak():
@@ -222,15 +224,16 @@ def run_ours(args, rank, world, local_rank):
     rec = B.new_error_record(dev)
 
     def step(ev=None):
-        B.kv_cache_append(b.new_k, b.new_v, slots, b.k_cache, b.v_cache, error_record=rec)
         if ev is not None:
             ev[0].record(stream)
-        B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out,
-                            partition_tokens=pt, workspace=ws, error_record=rec, phases=1)
+        B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                   out=out, partition_tokens=pt, workspace=ws, error_record=rec,
+                                   phases=1)
         if ev is not None:
             ev[1].record(stream)
-        B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out,
-                            partition_tokens=pt, workspace=ws, error_record=rec, phases=2)
+        B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                   out=out, partition_tokens=pt, workspace=ws, error_record=rec,
+                                   phases=2)
 
     K, W = args.steps, args.warmup
     for _ in range(W):
@@ -264,20 +267,18 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the public API: pinned host inputs copied in, output copied out
     pin = lambda t: t.detach().cpu().pin_memory()
     h_q, h_k, h_v = pin(b.q), pin(b.new_k), pin(b.new_v)
-    h_slots, h_bt, h_sl = pin(slots), pin(bt), pin(sl)
+    h_bt, h_sl = pin(bt), pin(sl)
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.new_k), torch.empty_like(b.new_v)
-    d_slots, d_bt, d_sl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(sl)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_sl))
+    d_bt, d_sl = torch.empty_like(bt), torch.empty_like(sl)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_sl))
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt),
-                     (d_sl, h_sl)):
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_sl, h_sl)):
             d.copy_(h, non_blocking=True)
-        B.kv_cache_append(d_k, d_v, d_slots, b.k_cache, b.v_cache, error_record=rec)
-        B.paged_attn_decode(d_q, b.k_cache, b.v_cache, d_bt, d_sl, b.scale, out=out,
-                            partition_tokens=pt, workspace=ws, error_record=rec)
+        B.paged_attn_decode_append(d_q, d_k, d_v, b.k_cache, b.v_cache, d_bt, d_sl, b.scale,
+                                   out=out, partition_tokens=pt, workspace=ws, error_record=rec)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(W):
@@ -335,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
             "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * K,
+            "gpu_launches": 2 * K,
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -154,6 +154,30 @@ int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache
                          int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* error_record, void* stream, const pa_decode_opts* opts);
 
+/* Fused KV append + decode  [P3b], [P3c]
+ *
+ * One decode step in one pass: for every sequence i with L = seq_lens[i] >= 1,
+ * the token at position L - 1 is the one being appended.  Its rows new_k[i] and
+ * new_v[i] are written into its slot (row (L-1) % block_size of physical block
+ * block_tables[i][(L-1) / block_size], every head) and the decode attends over
+ * all L tokens, taking the last one straight from new_k/new_v.  Equivalent,
+ * bit for bit, to kv_cache_append at those slots followed by paged_attn_decode,
+ * minus one launch and one re-read.  The block holding position L - 1 must be
+ * private to sequence i (the allocator's copy-on-write guarantees it).  A
+ * sequence with L = 0 appends nothing and gets a zero row.
+ *   new_k, new_v  device [num_seqs][num_heads][head_dim] in `dtype`, 16-byte aligned
+ *   k_cache, v_cache  written at one row per sequence and head, read elsewhere
+ *   opts          as for paged_attn_decode_ex (may be NULL); the append happens
+ *                 in the partition pass.
+ * Other arguments as for paged_attn_decode. */
+int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v, void* k_cache,
+                             void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                             int num_seqs, int num_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                             void* out, int out_dtype, int partition_tokens, void* workspace,
+                             size_t workspace_bytes, int32_t* error_record, void* stream,
+                             const pa_decode_opts* opts);
+
 /* Decode without allocation.  No counterpart in the paper: this is a library
  * convenience.  Some callers cannot allocate device memory - code running
  * inside another runtime whose pool owns all device memory, a serving loop that
@@ -270,6 +294,17 @@ int pa_batch_append(pa_allocator* a, const int64_t* seqs, int32_t n, int64_t* sl
  * does not fit. */
 int pa_batch_block_tables(const pa_allocator* a, const int64_t* seqs, int32_t n,
                           int32_t max_blocks, int32_t* tables, int32_t* seq_lens);
+/* Occupancy of the pool [P3a], [P3e].  All outputs optional (NULL to skip):
+ *   blocks_used      blocks held by at least one sequence
+ *   tokens_logical   sum of all sequences' lengths
+ *   slots_logical    sum over sequences of ceil(len / block_size) * block_size
+ *                    (what each sequence holds, counting shared blocks once per holder)
+ *   slots_filled     sum over used blocks of the rows written in them (the
+ *                    furthest any holder has filled that block)
+ * Paged waste = 1 - tokens_logical / slots_logical without sharing, and
+ * 1 - slots_filled / (blocks_used * block_size) physically. */
+int pa_alloc_stats(const pa_allocator* a, int32_t* blocks_used, int64_t* tokens_logical,
+                   int64_t* slots_logical, int64_t* slots_filled);
 /* Verify every invariant above; PA_OK or PA_ERR_REFCOUNT. */
 int pa_alloc_check(const pa_allocator* a);
 

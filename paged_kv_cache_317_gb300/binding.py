@@ -50,6 +50,11 @@ SIGNATURES = {
                                      c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p,
                                      c_int, c_int, c_void_p, c_size_t, c_void_p, c_void_p,
                                      ctypes.POINTER(pa_decode_opts)]),
+    "paged_attn_decode_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                         c_int, c_float, c_int, c_void_p, c_int, c_int, c_void_p,
+                                         c_size_t, c_void_p, c_void_p,
+                                         ctypes.POINTER(pa_decode_opts)]),
     "paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                           c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                           c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]),
@@ -71,6 +76,7 @@ SIGNATURES = {
     "pa_num_seqs": (c_int32, [c_void_p]),
     "pa_batch_append": (c_int, [c_void_p, P_int64, c_int32, P_int64, P_int64, P_int32]),
     "pa_batch_block_tables": (c_int, [c_void_p, P_int64, c_int32, c_int32, P_int32, P_int32]),
+    "pa_alloc_stats": (c_int, [c_void_p, P_int32, P_int64, P_int64, P_int64]),
     "pa_alloc_check": (c_int, [c_void_p]),
 }
 
@@ -177,6 +183,40 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
         _ptr(workspace), ws_bytes, _ptr(error_record), _stream(stream), ctypes.byref(opts))
     _check(st, "paged_attn_decode")
+    return out
+
+
+def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
+                             partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                             error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
+                             stages: int = 0, phases: int = 0, stream=None) -> torch.Tensor:
+    """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
+    decode over all seq_lens[i] tokens, in one pass."""
+    N, H, D = q.shape
+    B, _, bs, _ = k_cache.shape
+    MB = block_tables.shape[1]
+    for t, n in ((q, "q"), (new_k, "new_k"), (new_v, "new_v"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache")):
+        _need(t, n)
+    _need(block_tables, "block_tables", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if out is None:
+        out = torch.empty((N, H, D), dtype=out_dtype, device=q.device)
+    _need(out, "out")
+    need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    opts = pa_decode_opts(heads_per_cta, stages, phases)
+    st = load_library().paged_attn_decode_append(
+        _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),
+        _DTYPE[out.dtype], partition_tokens, _ptr(workspace), ws_bytes, _ptr(error_record),
+        _stream(stream), ctypes.byref(opts))
+    _check(st, "paged_attn_decode_append")
     return out
 
 
@@ -327,6 +367,13 @@ class BlockAllocator:
                                                lens.ctypes.data_as(P_int32)),
                "pa_batch_block_tables")
         return tables, lens
+
+    def stats(self) -> dict:
+        bu, tl, sl, sf = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.pa_alloc_stats(self._h, ctypes.byref(bu), ctypes.byref(tl),
+                                        ctypes.byref(sl), ctypes.byref(sf)), "pa_alloc_stats")
+        return {"blocks_used": bu.value, "tokens_logical": tl.value, "slots_logical": sl.value,
+                "slots_filled": sf.value}
 
     def check(self) -> None:
         _check(self._lib.pa_alloc_check(self._h), "pa_alloc_check")

@@ -284,3 +284,28 @@ extern "C" int pa_alloc_check(const pa_allocator* a) {
   if (used + static_cast<int32_t>(a->free_stack.size()) != a->num_blocks) return PA_ERR_REFCOUNT;
   return PA_OK;
 }
+
+extern "C" int pa_alloc_stats(const pa_allocator* a, int32_t* blocks_used,
+                              int64_t* tokens_logical, int64_t* slots_logical,
+                              int64_t* slots_filled) {
+  if (!a) return PA_ERR_INVALID_ARG;
+  std::vector<int32_t> fill(a->num_blocks, 0);
+  int64_t tokens = 0, slots = 0;
+  for (const auto& kv : a->seqs) {
+    const auto& s = kv.second;
+    tokens += s.len;
+    slots += static_cast<int64_t>(s.blocks.size()) * a->block_size;
+    for (size_t j = 0; j < s.blocks.size(); ++j) {
+      const int64_t rows =
+          std::min<int64_t>(a->block_size, s.len - static_cast<int64_t>(j) * a->block_size);
+      fill[s.blocks[j]] = std::max<int32_t>(fill[s.blocks[j]], static_cast<int32_t>(rows));
+    }
+  }
+  int64_t filled = 0;
+  for (int32_t f : fill) filled += f;
+  if (blocks_used) *blocks_used = a->num_blocks - static_cast<int32_t>(a->free_stack.size());
+  if (tokens_logical) *tokens_logical = tokens;
+  if (slots_logical) *slots_logical = slots;
+  if (slots_filled) *slots_filled = filled;
+  return PA_OK;
+}

@@ -19,6 +19,12 @@
 //  * One partition (the whole sequence fits): write out = acc / l directly.
 //    Several: write (m, l, acc) partials; a merge kernel combines them by
 //    log-sum-exp.
+//  * Fused append (paged_attn_decode_append): the sequence's last token is the
+//    one being appended.  Its K/V rows come straight from new_k/new_v into the
+//    stage (one extra bulk copy per head), and the consumers of the last
+//    partition write them into the token's slot, so no separate append launch
+//    and no re-read are needed.  The result is bit-identical to an append
+//    followed by a decode.
 //  * Every wait is bounded (one second), indices from device memory are range
 //    checked, and nothing traps.
 #include <cuda_runtime.h>
@@ -44,6 +50,10 @@ struct DecodeParams {
   const void* v_cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
+  const void* new_k;   // fused append: [N][H][D] rows of each sequence's last token, or null
+  const void* new_v;
+  void* k_out;         // fused append: the caches, written at each last token's slot
+  void* v_out;
   void* out;
   float* ws_acc;
   float2* ws_ml;
@@ -163,17 +173,31 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
             report_error(p.err, PA_ERR_TIMEOUT, seq, chunk);
           } else {
             const int tok = tok_begin + chunk * kChunk;
-            const uint32_t bytes = static_cast<uint32_t>(min(kChunk, tok_end - tok)) * ROW_BYTES;
+            const int rows = min(kChunk, tok_end - tok);
+            // With a fused append, the chunk that ends the sequence takes its
+            // last row from new_k/new_v instead of the cache.
+            const bool new_here = p.new_k != nullptr && tok + rows == L;
+            const int cache_rows = rows - (new_here ? 1 : 0);
+            const uint32_t bytes = static_cast<uint32_t>(cache_rows) * ROW_BYTES;
             const int row0 = tok % p.block_size;
-            mbar_arrive_expect_tx(&full[s], 2u * G * bytes);
+            mbar_arrive_expect_tx(&full[s], 2u * G * static_cast<uint32_t>(rows) * ROW_BYTES);
             uint8_t* dst = stages + s * stage_bytes;
             for (int w = 0; w < G; ++w) {
-              const size_t off =
-                  ((static_cast<size_t>(b) * p.num_heads + h0 + w) * p.block_size + row0) *
-                  ROW_BYTES;
-              bulk_g2s(dst + w * 2 * CHUNK_BYTES, kbase + off, bytes, &full[s], policy);
-              bulk_g2s(dst + w * 2 * CHUNK_BYTES + CHUNK_BYTES, vbase + off, bytes, &full[s],
-                       policy);
+              uint8_t* kd = dst + w * 2 * CHUNK_BYTES;
+              if (cache_rows > 0) {
+                const size_t off =
+                    ((static_cast<size_t>(b) * p.num_heads + h0 + w) * p.block_size + row0) *
+                    ROW_BYTES;
+                bulk_g2s(kd, kbase + off, bytes, &full[s], policy);
+                bulk_g2s(kd + CHUNK_BYTES, vbase + off, bytes, &full[s], policy);
+              }
+              if (new_here) {
+                const size_t off = (static_cast<size_t>(seq) * p.num_heads + h0 + w) * ROW_BYTES;
+                bulk_g2s(kd + bytes, static_cast<const char*>(p.new_k) + off, ROW_BYTES, &full[s],
+                         policy);
+                bulk_g2s(kd + CHUNK_BYTES + bytes, static_cast<const char*>(p.new_v) + off,
+                         ROW_BYTES, &full[s], policy);
+              }
             }
             ++issued;
           }
@@ -292,6 +316,28 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
       }
       if (lane == 0) p.ws_ml[row] = make_float2(m, l);
     }
+
+    // Fused append: the block holding the last token stores its rows into the
+    // token's slot (the table entry was range-checked by the producer; a bad
+    // one is skipped here).
+    if (p.new_k != nullptr && L > 0 && part == nparts - 1) {
+      const int pos = L - 1;
+      const int blk =
+          __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks + pos / p.block_size);
+      if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks)) {
+        const size_t dst =
+            ((static_cast<size_t>(blk) * p.num_heads + h) * p.block_size + pos % p.block_size) *
+            ROW_BYTES;
+        const size_t src = (static_cast<size_t>(seq) * p.num_heads + h) * ROW_BYTES;
+        for (int piece = lane; piece < 2 * TPR; piece += 32) {
+          const bool is_v = piece >= TPR;
+          const int x = (is_v ? piece - TPR : piece) * 16;
+          const uint4 val = *reinterpret_cast<const uint4*>(
+              static_cast<const char*>(is_v ? p.new_v : p.new_k) + src + x);
+          *reinterpret_cast<uint4*>(static_cast<char*>(is_v ? p.v_out : p.k_out) + dst + x) = val;
+        }
+      }
+    }
   }
 
   __syncthreads();
@@ -408,11 +454,11 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem, cudaStr
   return PA_OK;
 }
 
-int auto_heads_per_cta(int num_heads) {
-  for (int g : {4, 2, 1})
-    if (num_heads % g == 0) return g;
-  return 1;
-}
+// Two heads per block and two stages keep each block at ~32 KB of shared
+// memory, so six blocks (twelve consumer warps) share an SM: measured on GB300,
+// more resident consumer warps beat deeper pipelines, because each warp's
+// per-chunk work is a chain of dependent shuffles and exponentials.
+int auto_heads_per_cta(int num_heads) { return num_heads % 2 == 0 ? 2 : 1; }
 
 }  // namespace
 }  // namespace pagedkv
@@ -432,14 +478,14 @@ extern "C" size_t paged_attn_workspace_size(int num_seqs, int num_heads, int hea
   return workspace_bytes_for(num_seqs, num_heads, head_dim, P);
 }
 
-extern "C" int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
-                                    const int32_t* block_tables, const int32_t* seq_lens,
-                                    int num_seqs, int num_heads, int head_dim, int block_size,
-                                    int max_blocks_per_seq, int num_blocks, float scale,
-                                    int dtype, void* out, int out_dtype, int partition_tokens,
-                                    void* workspace, size_t workspace_bytes,
-                                    int32_t* error_record, void* stream,
-                                    const pa_decode_opts* opts) {
+namespace {
+int decode_common(const void* q, const void* new_k, const void* new_v, const void* k_cache,
+                  const void* v_cache, void* k_out, void* v_out, const int32_t* block_tables,
+                  const int32_t* seq_lens, int num_seqs, int num_heads, int head_dim,
+                  int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                  void* out, int out_dtype, int partition_tokens, void* workspace,
+                  size_t workspace_bytes, int32_t* error_record, void* stream,
+                  const pa_decode_opts* opts) {
   if (num_seqs < 0 || num_heads <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
       num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
@@ -462,12 +508,7 @@ extern "C" int paged_attn_decode_ex(const void* q, const void* k_cache, const vo
   if (G > kMaxHeadsPerCta || num_heads % G != 0) return PA_ERR_INVALID_ARG;
   const int row_bytes = head_dim * 2;
   int S = (opts && opts->stages > 0) ? opts->stages : 0;
-  if (S == 0) {
-    // Aim for about 96 KB of stages per block (two blocks per SM).
-    const int per_stage = G * 2 * kChunk * row_bytes;
-    S = (96 * 1024) / per_stage;
-    S = S < 2 ? 2 : (S > 4 ? 4 : S);
-  }
+  if (S == 0) S = 2;
   if (S < 2 || S > kMaxStages) return PA_ERR_INVALID_ARG;
   const size_t smem = kHeaderBytes + static_cast<size_t>(S) * G * 2 * kChunk * row_bytes;
   if (smem > 227 * 1024) return PA_ERR_INVALID_ARG;
@@ -483,6 +524,10 @@ extern "C" int paged_attn_decode_ex(const void* q, const void* k_cache, const vo
 
   DecodeParams p{};
   p.q = q;
+  p.new_k = new_k;
+  p.new_v = new_v;
+  p.k_out = k_out;
+  p.v_out = v_out;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.block_tables = block_tables;
@@ -518,6 +563,39 @@ extern "C" int paged_attn_decode_ex(const void* q, const void* k_cache, const vo
     case 128: return launch<F16, 128>(p, num_seqs, phases, smem, st);
     default: return launch<F16, 256>(p, num_seqs, phases, smem, st);
   }
+}
+
+}  // namespace
+
+extern "C" int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    int num_seqs, int num_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    int dtype, void* out, int out_dtype, int partition_tokens,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* error_record, void* stream,
+                                    const pa_decode_opts* opts) {
+  return decode_common(q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, block_tables,
+                       seq_lens, num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                       num_blocks, scale, dtype, out, out_dtype, partition_tokens, workspace,
+                       workspace_bytes, error_record, stream, opts);
+}
+
+extern "C" int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v,
+                                        void* k_cache, void* v_cache,
+                                        const int32_t* block_tables, const int32_t* seq_lens,
+                                        int num_seqs, int num_heads, int head_dim,
+                                        int block_size, int max_blocks_per_seq, int num_blocks,
+                                        float scale, int dtype, void* out, int out_dtype,
+                                        int partition_tokens, void* workspace,
+                                        size_t workspace_bytes, int32_t* error_record,
+                                        void* stream, const pa_decode_opts* opts) {
+  if (num_seqs > 0 && (!new_k || !new_v || !aligned16(new_k) || !aligned16(new_v)))
+    return PA_ERR_INVALID_ARG;
+  return decode_common(q, new_k, new_v, k_cache, v_cache, k_cache, v_cache, block_tables,
+                       seq_lens, num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                       num_blocks, scale, dtype, out, out_dtype, partition_tokens, workspace,
+                       workspace_bytes, error_record, stream, opts);
 }
 
 extern "C" int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -207,3 +207,12 @@ def test_allocator_error_codes(lib):
             fn(*args)
         assert e.value.name == name
     assert a.slots(1, 0, 3).tolist() == [a.block_table(1)[0] * 4 + i for i in range(3)]
+
+
+def test_fused_append_rejects_missing_rows(lib):
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.paged_attn_decode_append(p, None, p, p, p, p, p, 4, 8, 64, 16, 4, 64, 0.125, 0, p,
+                                        2, 0, None, 0, None, None, None) == 1
+    assert lib.paged_attn_decode_append(p, p, ctypes.c_void_p((1 << 20) + 4), p, p, p, p, 4, 8, 64,
+                                        16, 4, 64, 0.125, 0, p, 2, 0, None, 0, None, None,
+                                        None) == 1

@@ -18,10 +18,11 @@ def test_step_bytes_by_hand():
     partials = 2 * 2 * (8 + 2) * 4                      # 2 partitions x 2 heads of (D + m, l) fp32
     table = (2 + 38) * 4
     q = 2 * 2 * 8 * 2
-    assert b["decode_partition"] == kv + q + table + 2 * 4 + 1 * 2 * 8 * 2 + partials
+    appended = 2 * 2 * 2 * 8 * 2                        # K and V rows of 2 seqs x 2 heads written
+    assert b["append_write"] == appended
+    assert b["decode_partition"] == kv + q + table + 2 * 4 + 1 * 2 * 8 * 2 + partials + appended
     assert b["decode_merge"] == partials + 1 * 2 * 8 * 2 + 2 * 4
-    assert b["append"] == 2 * (2 * 2 * 2 * 8 * 2) + 2 * 8
-    assert b["total"] == b["decode_partition"] + b["decode_merge"] + b["append"]
+    assert b["total"] == b["decode_partition"] + b["decode_merge"]
 
 
 def test_clock_rows_parse_reasons_and_median():

@@ -1,0 +1,70 @@
+"""GPU parity of the fused append + decode call: bit-identical to append then
+decode, within tolerance of the oracle, and the cache bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_matches_oracle, bits, device_tables, oracle_decode
+from oracle import cache_ops as OC
+from workloads import decode_13b, random_decode_batch, tiny_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B(lib):
+    from paged_kv_cache_317_gb300 import binding
+    return binding
+
+
+def _both(B, b, **kw):
+    """(fused out, caches after fused) and (unfused out, caches after unfused)."""
+    bt, sl = device_tables(b)
+    k1, v1 = b.k_cache.clone(), b.v_cache.clone()
+    rec = B.new_error_record()
+    fused = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, k1, v1, bt, sl, b.scale,
+                                       error_record=rec, **kw)
+    k2, v2 = b.k_cache.clone(), b.v_cache.clone()
+    B.kv_cache_append(b.new_k, b.new_v, torch.from_numpy(b.slot_mapping).cuda(), k2, v2)
+    plain = B.paged_attn_decode(b.q, k2, v2, bt, sl, b.scale, **kw)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    return fused, (k1, v1), plain, (k2, v2)
+
+
+@pytest.mark.parametrize("pt", [0, 16, 64])
+def test_fused_tiny_matches_oracle_and_unfused(B, pt):
+    b = tiny_decode(seed=1, device="cuda")
+    ref = oracle_decode(b)
+    fused, (k1, v1), plain, (k2, v2) = _both(B, b, partition_tokens=pt)
+    assert torch.equal(fused, plain)
+    assert_matches_oracle(fused, ref, "fused tiny")
+    ek, ev = bits(b.k_cache), bits(b.v_cache)
+    OC.kv_append(ek, ev, bits(b.new_k), bits(b.new_v), b.slot_mapping, b.block_size)
+    assert np.array_equal(bits(k1), ek) and np.array_equal(bits(v1), ev)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 32), (256, 16)])
+def test_fused_ragged_lengths(B, dtype, D, bs):
+    lens = [1, 2, 16, 17, 32, 33, 511, 512, 513, 1000]
+    b = random_decode_batch(300 + D + bs, lens, 4, D, bs, dtype=dtype, device="cuda",
+                            with_append=True)
+    ref = oracle_decode(b)
+    for pt in (0, 32):
+        fused, (k1, v1), plain, (k2, v2) = _both(B, b, partition_tokens=pt)
+        assert torch.equal(fused, plain)
+        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+        assert_matches_oracle(fused, ref, f"fused {dtype} D{D} bs{bs} pt{pt}")
+
+
+def test_fused_13b_full_size(B):
+    b = decode_13b(device="cuda")
+    seqs = list(range(0, 256, 11))
+    ref = oracle_decode(b, seqs)
+    fused, _, plain, _ = _both(B, b, out_dtype=torch.bfloat16)
+    assert torch.equal(fused, plain)
+    assert_matches_oracle(fused[seqs], ref, "fused 13B")
+

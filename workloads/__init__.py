@@ -8,9 +8,11 @@ sits in, which sequences fork); it computes none of the method's arithmetic.
 
 from .gen import (  # noqa: F401
     DTYPES,
+    BeamPlan,
     DecodeBatch,
     MixedServingPlan,
     SamplingPlan,
+    beam_search,
     decode_13b,
     lognormal_lengths,
     long_context,

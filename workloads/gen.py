@@ -344,3 +344,73 @@ def mixed_serving(seed: int = 5, device="cuda", num_seqs: int = 512, steps: int 
                             init_lens=lens, init_offsets=np.concatenate([[0], np.cumsum(lens)]),
                             init_k=ik, init_v=iv, fork_pairs=pairs, free_order=free_order,
                             scale=default_scale(head_dim), device=str(device))
+
+
+# ---------------------------------------------------------------------------
+# Beam-search-style churn: survivors chosen by random scores (no model).
+# ---------------------------------------------------------------------------
+
+@dataclass
+class BeamPlan:
+    """``groups`` beam groups of ``width`` beams, run for ``steps`` steps.
+
+    Group ``g`` starts as one prompt of ``prompt_lens[g]`` tokens (rows
+    ``prompt_offsets[g]:prompt_offsets[g+1]`` of ``prompt_k``/``prompt_v``)
+    held by all ``width`` beams.  At step ``s`` new beam ``j`` of group ``g``
+    continues old beam ``parents[s, g, j]`` (the survivors of a random score
+    draw standing in for a model) and every beam appends one token;
+    ``step_tokens(s)`` gives that step's q, k, v as ``[groups * width, H, D]``.
+    """
+
+    seed: int
+    groups: int
+    width: int
+    steps: int
+    num_heads: int
+    head_dim: int
+    block_size: int
+    dtype: torch.dtype
+    num_blocks: int
+    prompt_lens: np.ndarray
+    prompt_offsets: np.ndarray
+    prompt_k: torch.Tensor
+    prompt_v: torch.Tensor
+    parents: np.ndarray           # int64 [steps, groups, width]
+    free_order: np.ndarray
+    scale: float
+    device: str = "cuda"
+
+    def step_tokens(self, step: int, device=None):
+        device = self.device if device is None else device
+        gen = _torch_gen(self.seed * 7_000_003 + 104729 * (step + 1), device)
+        shape = (self.groups * self.width, self.num_heads, self.head_dim)
+        return tuple(randn_rounded(shape, self.dtype, gen, device) for _ in range(3))
+
+
+def beam_search(seed: int = 6, device="cuda", groups: int = 16, width: int = 4,
+                steps: int = 40, prompt=(100, 400), num_heads: int = 8, head_dim: int = 128,
+                block_size: int = 16, dtype="bf16") -> BeamPlan:
+    rng = np.random.default_rng(seed)
+    gen = _torch_gen(seed, device)
+    lens = rng.integers(prompt[0], prompt[1] + 1, size=groups).astype(np.int64)
+    parents = np.zeros((steps, groups, width), dtype=np.int64)
+    for s in range(steps):
+        for g in range(groups):
+            # width x width candidate scores; the best `width` survive
+            scores = rng.random((width, width))
+            best = np.argsort(-scores, axis=None, kind="stable")[:width]
+            parents[s, g] = np.sort(best // width)
+    bs = block_size
+    # worst case: every beam private (prompt copied per beam) plus its steps
+    need = int((width * (-(-(lens + steps + 1) // bs) + 1)).sum())
+    num_blocks = int(math.ceil(1.2 * need))
+    free_order = rng.permutation(num_blocks).astype(np.int32)
+    dt = DTYPES[dtype]
+    total = int(lens.sum())
+    pk = randn_rounded((total, num_heads, head_dim), dt, gen, device)
+    pv = randn_rounded((total, num_heads, head_dim), dt, gen, device)
+    return BeamPlan(seed=seed, groups=groups, width=width, steps=steps, num_heads=num_heads,
+                    head_dim=head_dim, block_size=bs, dtype=dt, num_blocks=num_blocks,
+                    prompt_lens=lens, prompt_offsets=np.concatenate([[0], np.cumsum(lens)]),
+                    prompt_k=pk, prompt_v=pv, parents=parents, free_order=free_order,
+                    scale=default_scale(head_dim), device=str(device))
