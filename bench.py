@@ -264,35 +264,57 @@ def run_ours(args, rank, world, local_rank):
     part_ms = statistics.mean(a.elapsed_time(c) for a, c in evs)
     ms_max = reduce_max(ms, world, dev)
 
-    # end to end through the public API: pinned host inputs copied in, output copied out
+    # End to end through the public API: every step copies its inputs in from
+    # pinned host memory and its output back out.  As in a serving loop, the
+    # copies run on their own streams with two buffer sets, so step i's copies
+    # overlap step i-1's kernels; each step's bytes still cross the link.
     pin = lambda t: t.detach().cpu().pin_memory()
-    h_q, h_k, h_v = pin(b.q), pin(b.new_k), pin(b.new_v)
-    h_bt, h_sl = pin(bt), pin(sl)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.new_k), torch.empty_like(b.new_v)
-    d_bt, d_sl = torch.empty_like(bt), torch.empty_like(sl)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_sl))
-    d2h = h_out.numel() * h_out.element_size()
+    host_in = [pin(b.q), pin(b.new_k), pin(b.new_v), pin(bt), pin(sl)]
+    dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
+    h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    d_out = [torch.empty_like(out) for _ in range(2)]
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_copied = [torch.cuda.Event() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = h_out[0].numel() * h_out[0].element_size()
 
-    def e2e_step():
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_sl, h_sl)):
-            d.copy_(h, non_blocking=True)
-        B.paged_attn_decode_append(d_q, d_k, d_v, b.k_cache, b.v_cache, d_bt, d_sl, b.scale,
-                                   out=out, partition_tokens=pt, workspace=ws, error_record=rec)
-        h_out.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        j = i % 2
+        h2d_stream.wait_event(done[j])                 # buffer j's last kernels have finished
+        with torch.cuda.stream(h2d_stream):
+            for d, h in zip(dev_in[j], host_in):
+                d.copy_(h, non_blocking=True)
+        in_ready[j].record(h2d_stream)
+        stream.wait_event(in_ready[j])
+        stream.wait_event(out_copied[j])               # d_out[j] has been read back
+        q, k, v, btj, slj = dev_in[j]
+        B.paged_attn_decode_append(q, k, v, b.k_cache, b.v_cache, btj, slj, b.scale,
+                                   out=d_out[j], partition_tokens=pt, workspace=ws,
+                                   error_record=rec, stream=stream)
+        done[j].record(stream)
+        d2h_stream.wait_event(done[j])
+        with torch.cuda.stream(d2h_stream):
+            h_out[j].copy_(d_out[j], non_blocking=True)
+        out_copied[j].record(d2h_stream)
 
-    for _ in range(W):
-        e2e_step()
+    for i in range(W):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K):
-        e2e_step()
+    h2d_stream.wait_event(e0)
+    for i in range(K):
+        e2e_step(i)
+    stream.wait_event(out_copied[(K - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = reduce_max(e0.elapsed_time(e1) / K, world, dev)
+    if not torch.equal(h_out[(K - 1) % 2], out.cpu()):
+        raise RuntimeError("end-to-end output differs from the device-resident step's")
     if B.pa_error_read(rec) != [0, 0, 0, 0]:
         raise RuntimeError(f"device error record: {B.pa_error_read(rec)}")
 
@@ -335,12 +357,212 @@ def run_ours(args, rank, world, local_rank):
             },
             "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "note": "pinned H2D inputs + D2H output every step, copy streams "
+                            "double-buffered against the previous step's kernels"},
             "gpu_launches": 2 * K,
             "clocks": clk,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- other workloads
+def _time_device(fn, K, W, stream, flush=None):
+    """Mean device time of fn() over K calls (after W), in ms.  With `flush`,
+    L2 is flushed before every call and only the calls are timed."""
+    import torch
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+    times = []
+    for _ in range(K):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times)
+
+
+def run_workload(args, rank, world, local_rank):
+    """Device time of one step of the other seeded workloads (decode attention,
+    plus the allocator, copies and appends where the workload has them)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_317_gb300 import binding as B
+    from paged_kv_cache_317_gb300 import _build
+    import workloads as WL
+
+    _build.build(quiet=True)
+    B.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+    peak, peak_kind = measured_hbm_peak()
+    rec = B.new_error_record(dev)
+    line = {"metric": METRIC, "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
+            "higher_is_better": True, "vs_baseline": None, "data": "synthetic (seeded)"}
+    w = args.workload
+    if w in ("tiny", "long16", "long32"):
+        b = (WL.tiny_decode(device=dev) if w == "tiny"
+             else WL.long_context(device=dev, block_size=16 if w == "long16" else 32, poison=False))
+        bt = torch.from_numpy(b.block_tables).to(dev)
+        sl = torch.from_numpy(b.context_lens).to(dev)
+        out = torch.empty(b.q.shape, dtype=b.q.dtype, device=dev)
+        pt = 512
+        if b.has_append:
+            fn = lambda: B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt,
+                                                    sl, b.scale, out=out, partition_tokens=pt,
+                                                    error_record=rec)
+        else:
+            fn = lambda: B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out,
+                                             partition_tokens=pt, error_record=rec)
+        flush = None
+        if w == "tiny":
+            scratch = torch.empty(2 * 132 * 2 ** 20, dtype=torch.uint8, device=dev)
+            flush = lambda: scratch.fill_(1)
+        ms = _time_device(fn, K, W, stream, flush)
+        nb = step_bytes(b.context_lens, b.num_heads, b.head_dim, b.block_size,
+                        partition_tokens=pt)
+        total = nb["total"] - (0 if b.has_append else nb["append_write"])
+        line.update(config={"workload": b.name, "num_seqs": b.num_seqs, "num_heads": b.num_heads,
+                            "head_dim": b.head_dim, "block_size": b.block_size,
+                            "context_tokens": int(b.context_lens.sum()),
+                            "l2": "flushed between steps" if flush else "inputs larger than L2"},
+                    dtype="f16" if b.dtype == torch.float16 else "bf16")
+        tokens = int(b.context_lens.sum())
+        value = total / (ms * 1e-3) / 1e9
+    elif w == "sampling":
+        plan = WL.parallel_sampling(device=dev)
+        S, bs = plan.samples, plan.block_size
+        alloc = B.BlockAllocator(plan.num_blocks, bs, plan.free_order)
+        kc = torch.zeros((plan.num_blocks, plan.num_heads, bs, plan.head_dim), dtype=plan.dtype,
+                         device=dev)
+        vc = torch.zeros_like(kc)
+        for k in range(plan.num_prompts):
+            a, e = int(plan.prompt_offsets[k]), int(plan.prompt_offsets[k + 1])
+            alloc.add(k * S, e - a)
+            B.kv_cache_append(plan.prompt_k[a:e], plan.prompt_v[a:e],
+                              torch.from_numpy(alloc.slots(k * S, 0, e - a)).to(dev), kc, vc)
+            for s_ in range(1, S):
+                alloc.fork(k * S, k * S + s_)
+        ids = list(range(plan.num_seqs))
+        slots, pairs = alloc.batch_append(ids)
+        pairs_d = torch.from_numpy(pairs).to(dev)
+        copy_ms = _time_device(lambda: B.block_copy([kc], [vc], pairs_d), 20, 3, stream)
+        B.kv_cache_append(plan.tail_k[torch.from_numpy(plan.tail_offsets[:-1]).to(dev)],
+                          plan.tail_v[torch.from_numpy(plan.tail_offsets[:-1]).to(dev)],
+                          torch.from_numpy(slots).to(dev), kc, vc)
+        rows, rslots = [], []
+        for i in ids:
+            for t in range(1, int(plan.tail_lens[i])):
+                rows.append(int(plan.tail_offsets[i]) + t)
+                rslots.append(alloc.append(i)[0])
+        ri = torch.tensor(rows, device=dev)
+        B.kv_cache_append(plan.tail_k[ri], plan.tail_v[ri], torch.tensor(rslots, device=dev), kc,
+                          vc)
+        mb = max(len(alloc.block_table(i)) for i in ids)
+        tables, lens = alloc.batch_block_tables(ids, mb)
+        bt, sl = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+        out = torch.empty(plan.q.shape, dtype=plan.dtype, device=dev)
+        fn = lambda: B.paged_attn_decode(plan.q, kc, vc, bt, sl, plan.scale, out=out,
+                                         error_record=rec)
+        ms = _time_device(fn, K, W, stream)
+        nb = step_bytes(lens, plan.num_heads, plan.head_dim, bs)
+        total = nb["total"] - nb["append_write"]
+        st = alloc.stats()
+        unique_kv = st["slots_filled"] * plan.num_heads * plan.head_dim * 4
+        tokens = int(lens.sum())
+        value = total / (ms * 1e-3) / 1e9
+        line.update(config={"workload": "parallel sampling: 32 prompts x 8 samples, shared "
+                                        "1024+U[1,15]-token prefixes, tails U[1,512]",
+                            "num_seqs": plan.num_seqs, "copies": int(len(pairs)),
+                            "context_tokens": tokens, "l2": "inputs larger than L2"},
+                    dtype="bf16", block_copy_ms=round(copy_ms, 5),
+                    unique_kv_bytes=unique_kv,
+                    unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
+                    unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4))
+    elif w == "mixed":
+        plan = WL.mixed_serving(device=dev)
+        N, bs = plan.num_seqs, plan.block_size
+        alloc = B.BlockAllocator(plan.num_blocks, bs, plan.free_order)
+        kc = torch.zeros((plan.num_blocks, plan.num_heads, bs, plan.head_dim), dtype=plan.dtype,
+                         device=dev)
+        vc = torch.zeros_like(kc)
+        slots0 = []
+        for i in range(N):
+            a, e = int(plan.init_offsets[i]), int(plan.init_offsets[i + 1])
+            alloc.add(i, e - a)
+            slots0.append(alloc.slots(i, 0, e - a))
+        B.kv_cache_append(plan.init_k, plan.init_v, torch.from_numpy(np.concatenate(slots0)).to(dev),
+                          kc, vc)
+        ids, next_id = list(range(N)), N
+        max_blocks = int(-(-(plan.init_lens.max() + plan.steps) // bs))
+        tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
+        out = torch.empty((N, plan.num_heads, plan.head_dim), dtype=plan.dtype, device=dev)
+        ws = torch.empty(B.paged_attn_workspace_size(N, plan.num_heads, plan.head_dim, bs,
+                                                     max_blocks, 0), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        host_s, lens_seen = 0.0, 0
+        t0 = time.perf_counter()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for s_ in range(plan.steps):
+            h0 = time.perf_counter()
+            for a_, b_ in plan.fork_pairs[s_]:
+                alloc.free(ids[b_])
+                alloc.fork(ids[a_], next_id)
+                ids[b_] = next_id
+                next_id += 1
+            slots, pairs = alloc.batch_append(ids)
+            tables, lens = alloc.batch_block_tables(ids, max_blocks)
+            host_s += time.perf_counter() - h0
+            lens_seen += int(lens.sum())
+            if len(pairs):
+                B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
+            q, k, v = tokens_all[s_]
+            B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
+                                       torch.from_numpy(lens).to(dev), plan.scale, out=out,
+                                       workspace=ws, error_record=rec)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) / plan.steps
+        ms = ev0.elapsed_time(ev1) / plan.steps
+        tokens = lens_seen / plan.steps
+        total = tokens * plan.num_heads * plan.head_dim * 4
+        value = total / (ms * 1e-3) / 1e9
+        line.update(config={"workload": "mixed serving: 512 seqs, 70% U[32,256] / 30% "
+                                        "U[1024,4096], 26 forks/step, fused append+decode",
+                            "steps_run": plan.steps, "l2": "inputs larger than L2"},
+                    dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
+                    wall_ms_per_step=round(1e3 * wall, 4),
+                    note="value counts K/V bytes only; device time includes copies, H2D "
+                         "of tables and the decode")
+    else:
+        raise SystemExit(f"unknown workload {w}")
+    if B.pa_error_read(rec) != [0, 0, 0, 0]:
+        raise RuntimeError(f"device error record: {B.pa_error_read(rec)}")
+    line.update(value=round(value, 2), ms_per_step=round(ms, 5),
+                pct_of_hbm_peak=round(100 * value / peak, 2),
+                peak=f"{peak} GB/s ({peak_kind} hbm_gbs)",
+                seq_tokens_per_s=round(tokens / (ms * 1e-3), 1))
+    print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------- oracle arms
@@ -452,6 +674,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="13b",
+                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed"],
+                    help="13b (default, the headline line) or another seeded workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -465,6 +690,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, rank, world, local_rank)
+        elif args.workload != "13b":
+            run_workload(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:
