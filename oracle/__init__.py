@@ -23,7 +23,8 @@ Serving with PagedAttention", as restated on three web pages:
 
 Modules:
   attention      fp64 softmax attention over a sequence reassembled through its
-                 block table; per-partition partials and their log-sum-exp merge.
+                 block table; per-partition partials and their log-sum-exp merge;
+                 several causal query tokens per sequence (chunked prefill).
   cache_ops      slot-mapped append and whole-block copy, element by element.
   allocator_model  reference model of the block allocator (free list, refcounts,
                  fork, copy-on-write append, free) and its invariants.

@@ -123,3 +123,30 @@ def merge_partials(m: np.ndarray, l: np.ndarray, acc: np.ndarray) -> np.ndarray:
     M = m.max(axis=0)
     w = np.exp(m - M[None, :])
     return (w[:, :, None] * acc).sum(axis=0) / (w * l).sum(axis=0)[:, None]
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start,
+                            scale: float, block_size: int, dtype: str, seqs=None):
+    """Several query tokens per sequence, each attending causally through the block table.
+
+    Sequence i holds ``seq_lens[i]`` tokens; its last ``Q_i = query_start[i+1] -
+    query_start[i]`` are the queries, stored at rows ``query_start[i] .. query_start[i+1]``
+    of ``q`` (``[total, H, D]``).  Query j of sequence i sits at position
+    ``p = seq_lens[i] - Q_i + j`` and attends over tokens ``0 .. p`` (itself included),
+    exactly as a single-query decode of the sequence's first ``p + 1`` tokens would.
+    Returns float64 ``[total, H, D]`` (or only the rows of ``seqs``, in order).
+    """
+    idx = range(len(seq_lens)) if seqs is None else seqs
+    rows = []
+    for i in idx:
+        L = int(seq_lens[i])
+        a, b = int(query_start[i]), int(query_start[i + 1])
+        n_q = b - a
+        k = to_float64(gather_sequence(k_cache, block_tables[i], L, block_size), dtype)
+        v = to_float64(gather_sequence(v_cache, block_tables[i], L, block_size), dtype)
+        for j in range(n_q):
+            p = L - n_q + j
+            rows.append(attention(to_float64(q[a + j], dtype), k[: p + 1], v[: p + 1], scale))
+    if not rows:
+        return np.zeros((0,) + tuple(np.shape(q)[1:]), dtype=np.float64)
+    return np.stack(rows)

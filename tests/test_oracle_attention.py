@@ -183,3 +183,60 @@ def test_single_partition_partials_normalise_to_attention():
     np.testing.assert_allclose(acc[0] / l[0][:, None], A.attention(q, k, v, 1.0), rtol=0, atol=1e-13)
     s = np.einsum("hd,lhd->hl", q, k)
     np.testing.assert_array_equal(m[0], s.max(axis=1))
+
+
+def _brute_prefill(pool_k, pool_v, table, L, n_q, bs, q_rows, scale):
+    """Pure-Python causal multi-query attention: query j at position L - n_q + j."""
+    H, D = len(q_rows[0]), len(q_rows[0][0])
+    out = []
+    for j in range(n_q):
+        p = L - n_q + j
+        row = [[0.0] * D for _ in range(H)]
+        for h in range(H):
+            sc = []
+            for t in range(p + 1):
+                blk, r = table[t // bs], t % bs
+                sc.append(scale * sum(q_rows[j][h][d] * pool_k[blk][h][r][d] for d in range(D)))
+            mx = max(sc)
+            ws = [math.exp(x - mx) for x in sc]
+            tot = sum(ws)
+            for t in range(p + 1):
+                blk, r = table[t // bs], t % bs
+                for d in range(D):
+                    row[h][d] += ws[t] / tot * pool_v[blk][h][r][d]
+        out.append(row)
+    return out
+
+
+def test_prefill_matches_brute_force():
+    lens, nq = [9, 20, 5], [3, 20, 1]
+    b = random_decode_batch(31, lens, 2, 4, 4, dtype="f16", pool_factor=2.0)
+    gen = torch.Generator().manual_seed(5)
+    q = torch.randn(sum(nq), 2, 4, generator=gen).half()
+    starts = np.concatenate([[0], np.cumsum(nq)])
+    got = A.paged_prefill_attention(q.numpy(), b.k_cache.numpy(), b.v_cache.numpy(),
+                                    b.block_tables, b.context_lens, starts, 0.6, 4, "f16")
+    kc, vc = b.k_cache.double().tolist(), b.v_cache.double().tolist()
+    for i in range(3):
+        ref = _brute_prefill(kc, vc, b.block_tables[i].tolist(), lens[i], nq[i], 4,
+                             q[starts[i]:starts[i + 1]].double().tolist(), 0.6)
+        assert np.max(np.abs(got[starts[i]:starts[i + 1]] - np.array(ref))) <= 1e-12
+
+
+def test_prefill_single_query_is_decode_and_last_query_sees_everything():
+    lens = [33, 70]
+    b = random_decode_batch(32, lens, 3, 8, 16, dtype="f16")
+    dec = A.paged_decode_attention(b.q.numpy(), b.k_cache.numpy(), b.v_cache.numpy(),
+                                   b.block_tables, b.context_lens, 0.4, 16, "f16")
+    one = A.paged_prefill_attention(b.q.numpy(), b.k_cache.numpy(), b.v_cache.numpy(),
+                                    b.block_tables, b.context_lens, [0, 1, 2], 0.4, 16, "f16")
+    assert np.array_equal(one, dec)
+    # query j of a chunk = decode of the first p + 1 tokens with that query
+    q = np.repeat(b.q.numpy()[1:2], 5, axis=0)
+    many = A.paged_prefill_attention(q, b.k_cache.numpy(), b.v_cache.numpy(), b.block_tables[1:],
+                                     b.context_lens[1:], [0, 5], 0.4, 16, "f16")
+    for j in range(5):
+        p = 70 - 5 + j
+        short = A.paged_decode_attention(b.q.numpy()[1:2], b.k_cache.numpy(), b.v_cache.numpy(),
+                                         b.block_tables[1:], np.array([p + 1]), 0.4, 16, "f16")
+        assert np.array_equal(many[j], short[0])
