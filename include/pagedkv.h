@@ -178,6 +178,34 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
                              size_t workspace_bytes, int32_t* error_record, void* stream,
                              const pa_decode_opts* opts);
 
+/* Chunked prefill / multi-query attention through the block table  [P1], [P3c]
+ *
+ * Several query tokens per sequence, on the tensor cores (tcgen05).  Sequence i
+ * holds L = seq_lens[i] tokens in the cache (its new tokens already appended);
+ * its last Q_i = query_start[i+1] - query_start[i] tokens are queries, stored at
+ * rows query_start[i] .. query_start[i+1]-1 of q.  Query j sits at position
+ * p = L - Q_i + j and attends causally over tokens 0..p:
+ *   out[query_start[i] + j][h] = softmax_t<=p(scale * <q, k_t>) . v
+ * Arithmetic: Q.K^T in fp32 on the tensor cores; probabilities enter P.V as a
+ * pair of half-precision numbers (hi + lo), so P.V keeps about 16 mantissa bits;
+ * fp32 accumulation.
+ *   q             device [total_queries][num_heads][head_dim] in `dtype`, 16-byte aligned
+ *   query_start   device int32 [num_seqs + 1], nondecreasing, query_start[num_seqs]
+ *                 <= total_queries
+ *   max_query_len host: >= every Q_i (sizes the grid)
+ *   head_dim      128;  block_size: a multiple of 16
+ *   out           device [total_queries][num_heads][head_dim] in `out_dtype`
+ * Rows of out outside every sequence's query range are not written.  A sequence
+ * whose range is inconsistent (Q_i > L, range outside q, Q_i > max_query_len) is
+ * recorded as PA_ERR_BAD_SEQ_LEN and skipped.  Other arguments as for
+ * paged_attn_decode; num_blocks * num_heads * block_size must be < 2^31. */
+int paged_attn_prefill(const void* q, const int32_t* query_start, int total_queries,
+                       int max_query_len, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                       int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                       int num_blocks, float scale, int dtype, void* out, int out_dtype,
+                       int32_t* error_record, void* stream);
+
 /* Decode without allocation.  No counterpart in the paper: this is a library
  * convenience.  Some callers cannot allocate device memory - code running
  * inside another runtime whose pool owns all device memory, a serving loop that

@@ -55,6 +55,9 @@ SIGNATURES = {
                                          c_int, c_float, c_int, c_void_p, c_int, c_int, c_void_p,
                                          c_size_t, c_void_p, c_void_p,
                                          ctypes.POINTER(pa_decode_opts)]),
+    "paged_attn_prefill": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                   c_float, c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                           c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                           c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]),
@@ -217,6 +220,31 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
         _DTYPE[out.dtype], partition_tokens, _ptr(workspace), ws_bytes, _ptr(error_record),
         _stream(stream), ctypes.byref(opts))
     _check(st, "paged_attn_decode_append")
+    return out
+
+
+def paged_attn_prefill(q: torch.Tensor, query_start: torch.Tensor, max_query_len: int,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       seq_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                       out_dtype=torch.float32, error_record: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Causal multi-query attention: q [total,H,D]; query_start int32 [N+1] (device)."""
+    T, H, D = q.shape
+    B, _, bs, _ = k_cache.shape
+    N = seq_lens.shape[0]
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    for t, n in ((query_start, "query_start"), (block_tables, "block_tables"),
+                 (seq_lens, "seq_lens")):
+        _need(t, n, torch.int32)
+    if out is None:
+        out = torch.empty((T, H, D), dtype=out_dtype, device=q.device)
+    _need(out, "out")
+    st = load_library().paged_attn_prefill(
+        _ptr(q), _ptr(query_start), T, int(max_query_len), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(seq_lens), N, H, D, bs, block_tables.shape[1], B, float(scale),
+        _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(error_record), _stream(stream))
+    _check(st, "paged_attn_prefill")
     return out
 
 

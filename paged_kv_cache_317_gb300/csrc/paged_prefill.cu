@@ -1,0 +1,612 @@
+// Chunked prefill / multi-query attention through the block table on the
+// 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Several query tokens per sequence (a prefill chunk, or draft tokens to
+// verify) attend causally over the sequence's tokens, read through its block
+// table (PagedAttention, zeroshotmind.com page, "Block tables: logical order,
+// physical scatter").  With >1 query per head the work is a dense contraction,
+// so it runs on tensor cores:
+//
+//  * block = (128-query tile, head, sequence); 6 warps: 4 softmax warps (one
+//    query row per thread = one TMEM lane), 1 TMA producer warp, 1 MMA warp.
+//  * Q tile: one 3-D TMA load per 64-wide half of head_dim (128B swizzle).
+//    K/V: per 16-key chunk the producer follows the block table and issues
+//    2-D TMA loads of the rows (128B swizzle) into a 2-stage ring of 64-key tiles.
+//  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16) into one of two TMEM S
+//    buffers; the next tile's S overlaps the current tile's softmax.
+//  * Softmax warps: tcgen05.ld their S row, causal/length mask, online softmax
+//    in log2 units; P is written to shared memory as bf16/fp16 hi + lo parts
+//    (hi = round(p), lo = round(p - hi)), so P.V carries ~16 more mantissa bits
+//    than a single half-precision P and stays within the fp32-accumulation error
+//    bound; when the running max grows they rescale O in TMEM.
+//  * O += P V: 4 + 4 tcgen05.mma (M=128, N=128, K=16 keys; V as an MN-major
+//    operand) accumulating in TMEM; the last tile's P.V completion releases
+//    the epilogue: O / l, stored as rows of out.
+//  * Every mbarrier wait is bounded (one second); on a timeout the block
+//    records PA_ERR_TIMEOUT, waits (bounded) for its copies and MMAs, frees its
+//    TMEM and returns.  Nothing traps.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pagedkv {
+namespace {
+
+constexpr int kQTile = 128;                       // query rows per block (MMA M)
+constexpr int kKTile = 64;                        // keys per tile
+constexpr int kHeadDim = 128;
+constexpr int kThreads = 192;
+constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B (one 64-wide half)
+constexpr int kQBytes = kQTile * kHeadDim * 2;    // 32 KB (two 16 KB halves)
+constexpr int kKBytes = 2 * kHalfBytes;           // 16 KB
+constexpr int kStageBytes = 2 * kKBytes;          // K + V
+constexpr int kPBytes = kQTile * kKTile * 2;      // 16 KB
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + 2 * kStageBytes;
+constexpr int kOffPlo = kOffP + kPBytes;
+constexpr int kOffBar = kOffPlo + kPBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align to 1 KB
+constexpr uint32_t kTmemCols = 256;               // S buffers [0,64) [64,128), O [128,256)
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Bars {
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct PrefillParams {
+  const int32_t* query_start;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  void* out;
+  int32_t* err;
+  int num_heads, block_size, max_blocks, num_blocks, out_dtype;
+  int total_queries;  // rows of q and out
+  float qscale;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
+// offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* p, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_addr(p);
+  uint64_t d = static_cast<uint64_t>((a >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, A and B both bf16 (or
+// both fp16), A K-major, B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, bool bf16, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  uint32_t r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Two floats -> two 16-bit values (bf16 or fp16, round to nearest even), packed.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_float(uint32_t bits16) {
+  if constexpr (BF16) {
+    return __uint_as_float(bits16 << 16);
+  } else {
+    __half h;
+    *reinterpret_cast<uint16_t*>(&h) = static_cast<uint16_t>(bits16);
+    return __half2float(h);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  const int qt = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int L = p.seq_lens[seq];
+  const int q_begin = p.query_start[seq];
+  int nq = p.query_start[seq + 1] - q_begin;
+  const int cap = p.max_blocks * p.block_size;
+  // Lengths and query ranges come from device memory: a bad one is recorded and
+  // the sequence is clamped or skipped, never used to address memory.
+  const bool bad_len = L < 0 || L > cap;
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const bool bad_q = nq < 0 || nq > L || q_begin < 0 || q_begin > p.total_queries - nq ||
+                     nq > static_cast<int>(gridDim.x) * kQTile;
+  if (bad_len || bad_q) {
+    if (threadIdx.x == 0 && qt == 0 && h == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, L);
+    if (bad_q) nq = 0;
+  }
+  const int q0 = qt * kQTile;
+  if (q0 >= nq) return;
+  const int rows = min(kQTile, nq - q0);   // query rows of this tile
+  const int pos0 = L - nq + q0;            // position of the tile's first query
+  const int keys = pos0 + rows;            // keys any row of the tile may see
+  const int T = (keys + kKTile - 1) / kKTile;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* Qs = smem + kOffQ;
+  uint8_t* Ps = smem + kOffP;
+  uint8_t* Plo = smem + kOffPlo;
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort;
+  auto stage_k = [&](int s) { return smem + kOffKV + s * kStageBytes; };
+  auto stage_v = [&](int s) { return smem + kOffKV + s * kStageBytes + kKBytes; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], kQTile);
+    }
+    mbar_init(&bars->p_full, kQTile);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&bars->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  int kv_issued = 0;        // producer lane 0: tiles whose loads were issued
+  int mma_started = 0;      // MMA lane 0: whether any MMA was issued
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+      tma_load_3d(Qs, &tm_q, 0, h, q_begin + q0, &bars->q_full);
+      tma_load_3d(Qs + kQBytes / 2, &tm_q, 64, h, q_begin + q0, &bars->q_full);
+    }
+    for (int j = 0; j < T; ++j) {
+      // lanes 0..3 look up the physical block of the tile's four 16-key chunks
+      const int key0 = j * kKTile + lane * 16;
+      int blk = 0;
+      if (lane < 4 && key0 < keys) {
+        blk = __ldg(table + key0 / p.block_size);
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+          report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
+          blk = 0;
+        }
+      }
+      int ok = 1;
+      if (lane == 0) {
+        const int s = j & 1;
+        if (j >= 2) ok = mbar_wait_bounded(&bars->kv_empty[s], ((j >> 1) - 1) & 1);
+        if (!ok) {
+          *abort_flag = 1;
+          report_error(p.err, PA_ERR_TIMEOUT, seq, j);
+        } else {
+          const int n = min(4, (keys - j * kKTile + 15) / 16);
+          mbar_arrive_expect_tx(&bars->kv_full[s], static_cast<uint32_t>(n) * 4 * 2048);
+        }
+      }
+      ok = __shfl_sync(kFullMask, ok, 0);
+      if (!ok) break;
+      for (int c = 0; c < 4; ++c) {
+        const int b = __shfl_sync(kFullMask, blk, c);
+        const int k0 = j * kKTile + c * 16;
+        if (lane == 0 && k0 < keys) {
+          const int s = j & 1;
+          const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
+          tma_load_2d(stage_k(s) + c * 2048, &tm_k, 0, row, &bars->kv_full[s]);
+          tma_load_2d(stage_k(s) + kHalfBytes + c * 2048, &tm_k, 64, row, &bars->kv_full[s]);
+          tma_load_2d(stage_v(s) + c * 2048, &tm_v, 0, row, &bars->kv_full[s]);
+          tma_load_2d(stage_v(s) + kHalfBytes + c * 2048, &tm_v, 64, row, &bars->kv_full[s]);
+        }
+      }
+      kv_issued = j + 1;
+      __syncwarp();
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(kQTile, kKTile, BF16, false);
+      constexpr uint32_t idesc_o = make_idesc(kQTile, kHeadDim, BF16, true);
+      bool ok = mbar_wait_bounded(&bars->q_full, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!mbar_wait_bounded(&bars->kv_full[s], (j >> 1) & 1)) return false;
+        if (j >= 2 && !mbar_wait_bounded(&bars->s_free[s], ((j >> 1) - 1) & 1)) return false;
+        tc_fence_after();
+        const uint8_t* ks = stage_k(s);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const int half = kk >> 2, off = (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(Qs + half * (kQBytes / 2) + off, 16, 1024);
+          const uint64_t b = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
+          mma_f16(tmem + s * kKTile, a, b, idesc_s, kk > 0);
+        }
+        mma_commit(&bars->s_full[s]);
+        mma_started = 1;
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(&bars->p_full, j & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* vs = stage_v(j & 1);
+#pragma unroll
+        for (int kk = 0; kk < kKTile / 16; ++kk) {
+          const uint64_t b = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
+          mma_f16(tmem + 128, smem_desc_sw128(Ps + kk * 32, 16, 1024), b, idesc_o,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16(tmem + 128, smem_desc_sw128(Plo + kk * 32, 16, 1024), b, idesc_o, 1u);
+        }
+        mma_commit(&bars->o_done);
+        mma_commit(&bars->kv_empty[j & 1]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report_error(p.err, PA_ERR_TIMEOUT, seq, -1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;  // query row = TMEM lane
+    const bool row_valid = r < rows;
+    const int pos = row_valid ? pos0 + r : -1;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[b], (j >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float sv[kKTile];
+      {
+        float t[32];
+        tmem_ld32(tmem + lane_base + b * kKTile, t);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c] = t[c];
+        tmem_ld32(tmem + lane_base + b * kKTile + 32, t);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[b]);
+
+      const int kbase = j * kKTile;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKTile; ++c) {
+        const float u = (kbase + c <= pos) ? sv[c] * p.qscale : -INFINITY;
+        sv[c] = u;
+        mt = fmaxf(mt, u);
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool none = (m_new == -INFINITY);  // no key seen yet (or an unused row)
+      const float alpha = none ? 1.f : exp2f(m - m_new);
+      float rowsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKTile; ++c) {
+        const float e = none ? 0.f : exp2f(sv[c] - m_new);
+        sv[c] = e;
+        rowsum += e;
+      }
+      // P.V of the previous tile must be done before P and O are touched.
+      if (j > 0) {
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->o_done, (j - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(kFullMask, alpha != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + 128 + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + lane_base + 128 + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P as hi + lo halves, rows of 128 B in the 128B-swizzled K-major layout
+#pragma unroll
+      for (int ch = 0; ch < kKTile / 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = sv[ch * 8 + 2 * i], bb = sv[ch * 8 + 2 * i + 1];
+          hi[i] = pack_half2<BF16>(a, bb);
+          const float ra = half_to_float<BF16>(hi[i] & 0xffffu);
+          const float rb = half_to_float<BF16>(hi[i] >> 16);
+          lo[i] = pack_half2<BF16>(a - ra, bb - rb);
+        }
+        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(Ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(Plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      // keys past the last one any row may see: zero their V rows (they may hold
+      // stale or unused-slot data, and 0 * NaN would poison the accumulator)
+      if (j == T - 1 && keys < kbase + kKTile) {
+        uint8_t* vs = stage_v(j & 1);
+        const int first = keys - kbase;
+        const int n16 = (kKTile - first) * 2 * 8;  // rows x halves x 16-byte pieces
+        for (int idx = r; idx < n16; idx += kQTile) {
+          const int row = first + idx / 16;
+          const int rest = idx % 16;
+          *reinterpret_cast<uint4*>(vs + (rest >> 3) * kHalfBytes + row * 128 + (rest & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      l = l * alpha + rowsum;
+      m = m_new;
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      if (__shfl_sync(kFullMask, *abort_flag, 0)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok) ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->o_done, (T - 1) & 1));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row_off =
+          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + 128 + cc * 32, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= inv;
+        if (row_valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
+        }
+      }
+    } else if (lane == 0) {
+      *abort_flag = 1;
+      report_error(p.err, PA_ERR_TIMEOUT, seq, -2);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every copy and MMA this block started finish before its shared
+    // memory and TMEM are released (bounded waits).
+    if (warp == 4 && lane == 0) {
+      for (int s = 0; s < 2 && s < kv_issued; ++s) {
+        const int last = s + ((kv_issued - 1 - s) / 2) * 2;
+        mbar_wait_bounded(&bars->kv_full[s], (last >> 1) & 1);
+      }
+      mbar_wait_bounded(&bars->q_full, 0);
+    }
+    if (warp == 5 && lane == 0 && mma_started) {
+      mma_commit(&bars->drain);
+      mbar_wait_bounded(&bars->drain, 0);
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 5) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* map, bool bf16, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool BF16>
+cudaError_t ensure_prefill_smem(int device) {
+  static std::atomic<uint64_t> done{0};
+  const uint64_t bit = device < 64 ? (1ull << device) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<BF16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+}  // namespace
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int total_queries,
+                                  int max_query_len, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, const int32_t* seq_lens,
+                                  int num_seqs, int num_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                                  void* out, int out_dtype, int32_t* error_record, void* stream) {
+  if (num_seqs < 0 || total_queries < 0 || max_query_len < 0 || num_heads <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_queries == 0 || max_query_len == 0) return PA_OK;
+  if (head_dim != kHeadDim || block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32)
+    return PA_ERR_UNSUPPORTED;
+  if (!q || !query_start || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || num_seqs > 65535 || num_heads > 65535) return PA_ERR_INVALID_ARG;
+  const unsigned long long cache_rows =
+      static_cast<unsigned long long>(num_blocks) * num_heads * block_size;
+  if (cache_rows >= (1ull << 31) || static_cast<long long>(max_blocks_per_seq) * block_size >
+                                        (1ll << 30))
+    return PA_ERR_INVALID_ARG;
+
+  const bool bf16 = dtype == PA_BF16;
+  CUtensorMap tq, tk, tv;
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(head_dim),
+                               static_cast<cuuint64_t>(num_heads),
+                               static_cast<cuuint64_t>(total_queries)};
+  const cuuint64_t qstr[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                              static_cast<cuuint64_t>(head_dim) * 2 * num_heads};
+  const cuuint32_t qbox[3] = {64, 1, kQTile};
+  const cuuint64_t cdims[2] = {static_cast<cuuint64_t>(head_dim), cache_rows};
+  const cuuint64_t cstr[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t cbox[2] = {64, 16};
+  if (!encode(&tq, bf16, q, 3, qdims, qstr, qbox) ||
+      !encode(&tk, bf16, k_cache, 2, cdims, cstr, cbox) ||
+      !encode(&tv, bf16, v_cache, 2, cdims, cstr, cbox))
+    return PA_ERR_CUDA;
+
+  PrefillParams p{};
+  p.query_start = query_start;
+  p.seq_lens = seq_lens;
+  p.block_tables = block_tables;
+  p.out = out;
+  p.err = error_record;
+  p.num_heads = num_heads;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.out_dtype = out_dtype;
+  p.total_queries = total_queries;
+  p.qscale = scale * kLog2e;
+
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
+  const cudaError_t e = bf16 ? ensure_prefill_smem<true>(device) : ensure_prefill_smem<false>(device);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  dim3 grid((max_query_len + kQTile - 1) / kQTile, num_heads, num_seqs);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bf16)
+    paged_prefill_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  else
+    paged_prefill_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

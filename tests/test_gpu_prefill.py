@@ -1,0 +1,116 @@
+"""GPU parity of the tensor-core chunked prefill against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_matches_oracle, storage
+from oracle import attention as OA
+from workloads import random_decode_batch
+from workloads.gen import _torch_gen, randn_rounded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B(lib):
+    from paged_kv_cache_317_gb300 import binding
+    return binding
+
+
+def _case(seed, lens, nq, H, bs, dtype, poison=True):
+    b = random_decode_batch(seed, lens, H, 128, bs, dtype=dtype, device="cuda", poison=poison)
+    g = _torch_gen(seed + 7, "cuda")
+    q = randn_rounded((int(sum(nq)), H, 128), b.dtype, g, "cuda")
+    starts = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    return b, q, starts
+
+
+def _run(B, b, q, starts, out_dtype=torch.float32, rec=None):
+    return B.paged_attn_prefill(q, torch.from_numpy(starts).cuda(), int(np.diff(starts).max()),
+                                b.k_cache, b.v_cache, torch.from_numpy(b.block_tables).cuda(),
+                                torch.from_numpy(b.context_lens).cuda(), b.scale,
+                                out_dtype=out_dtype, error_record=rec)
+
+
+def _oracle(b, q, starts, seqs=None):
+    qs, dt = storage(q)
+    kc, _ = storage(b.k_cache)
+    vc, _ = storage(b.v_cache)
+    return OA.paged_prefill_attention(qs, kc, vc, b.block_tables, b.context_lens, starts, b.scale,
+                                      b.block_size, dt, seqs)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_prefill_small_cases(B, dtype, bs):
+    lens = [5, 300, 1000, 17, 129, 64]
+    nq = [5, 64, 200, 1, 129, 3]            # whole-sequence prefill, chunks, one query
+    b, q, starts = _case(40 + bs, lens, nq, 2, bs, dtype)
+    rec = B.new_error_record()
+    out = _run(B, b, q, starts, rec=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert_matches_oracle(out, _oracle(b, q, starts), f"prefill {dtype} bs{bs}")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_prefill_half_outputs(B, out_dtype):
+    b, q, starts = _case(50, [200, 90], [130, 90], 4, 16, "bf16")
+    assert_matches_oracle(_run(B, b, q, starts, out_dtype=out_dtype), _oracle(b, q, starts))
+
+
+def test_single_query_prefill_matches_decode(B):
+    lens = [1, 40, 513, 2000]
+    b = random_decode_batch(60, lens, 8, 128, 16, dtype="bf16", device="cuda")
+    starts = np.arange(len(lens) + 1, dtype=np.int32)
+    out = _run(B, b, b.q, starts)
+    dec = B.paged_attn_decode(b.q, b.k_cache, b.v_cache, torch.from_numpy(b.block_tables).cuda(),
+                              torch.from_numpy(b.context_lens).cuda(), b.scale)
+    torch.cuda.synchronize()
+    assert (out - dec).abs().max().item() <= 2e-3
+    assert_matches_oracle(out, _oracle(b, b.q, starts))
+
+
+def test_prefill_13b_shaped_chunks_sampled(B):
+    """16 sequences x 40 heads; each appends a 512-token chunk to a context of up to
+    2048 tokens.  The oracle checks two sequences in full and sampled rows of others."""
+    rng = np.random.default_rng(70)
+    lens = rng.integers(512, 2049, size=16)
+    nq = np.full(16, 512)
+    b, q, starts = _case(70, lens, nq, 40, 16, "bf16", poison=False)
+    out = _run(B, b, q, starts)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    qs, dt = storage(q)
+    kc, _ = storage(b.k_cache)
+    vc, _ = storage(b.v_cache)
+    for i in (0, 9):
+        a, e = starts[i], starts[i + 1]
+        ref = OA.paged_prefill_attention(qs, kc, vc, b.block_tables, b.context_lens, starts,
+                                         b.scale, 16, dt, seqs=[i])
+        assert_matches_oracle(out[a:e], ref, f"seq {i}")
+    for i in (3, 15):
+        L = int(lens[i])
+        k = OA.to_float64(OA.gather_sequence(kc, b.block_tables[i], L, 16), dt)
+        v = OA.to_float64(OA.gather_sequence(vc, b.block_tables[i], L, 16), dt)
+        for j in (0, 1, 127, 128, 255, 300, 511):
+            p = L - 512 + j
+            ref = OA.attention(OA.to_float64(qs[starts[i] + j], dt), k[: p + 1], v[: p + 1],
+                               b.scale)
+            assert_matches_oracle(out[starts[i] + j], ref, f"seq {i} row {j}")
+
+
+def test_prefill_bad_query_range_is_recorded_and_skipped(B):
+    b, q, starts = _case(80, [50, 60], [10, 20], 2, 16, "bf16", poison=False)
+    bad = starts.copy()
+    bad[1] = 45                              # sequence 0 claims 45 queries > nothing wrong yet
+    bad[2] = 30 + 60                         # sequence 1 range past the end of q
+    rec = B.new_error_record()
+    out = torch.zeros((q.shape[0], 2, 128), device="cuda")
+    B.paged_attn_prefill(q, torch.from_numpy(bad).cuda(), 60, b.k_cache, b.v_cache,
+                         torch.from_numpy(b.block_tables).cuda(),
+                         torch.from_numpy(b.context_lens).cuda(), b.scale, out=out,
+                         error_record=rec)
+    r = B.pa_error_read(rec)
+    assert r[0] == 6 and r[1] >= 1
