@@ -116,6 +116,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (burst, for a kernel timed alone) from MEASURED_PEAKS.json."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def decode_source_sha() -> str:
     h = hashlib.sha256()
     for rel in DECODE_SOURCES:
@@ -406,6 +416,7 @@ def run_workload(args, rank, world, local_rank):
     from paged_kv_cache_317_gb300 import binding as B
     from paged_kv_cache_317_gb300 import _build
     import workloads as WL
+    import workloads.gen  # noqa: F401  (randn_rounded, _torch_gen)
 
     _build.build(quiet=True)
     B.load_library()
@@ -554,6 +565,38 @@ def run_workload(args, rank, world, local_rank):
                     wall_ms_per_step=round(1e3 * wall, 4),
                     note="value counts K/V bytes only; device time includes copies, H2D "
                          "of tables and the decode")
+    elif w == "prefill":
+        # chunked prefill: 16 sequences append a 512-token chunk to contexts of 512..2048
+        rng = np.random.default_rng(70)
+        lens = rng.integers(512, 2049, size=16)
+        nq = np.full(16, 512)
+        b = WL.random_decode_batch(70, lens, 40, 128, 16, dtype="bf16", device=dev, poison=False)
+        g = WL.gen._torch_gen(77, dev)
+        q = WL.gen.randn_rounded((int(nq.sum()), 40, 128), torch.bfloat16, g, dev)
+        starts = torch.from_numpy(np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)).to(dev)
+        bt = torch.from_numpy(b.block_tables).to(dev)
+        sl = torch.from_numpy(b.context_lens).to(dev)
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        fn = lambda: B.paged_attn_prefill(q, starts, 512, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                          out=out, error_record=rec)
+        ms = _time_device(fn, K, W, stream)
+        # useful flops: 2*D per (query, visible key) for Q.K^T and again for P.V
+        visible = sum(int(((lens[i] - 512) + np.arange(1, 513)).sum()) for i in range(16))
+        flops = 4.0 * 128 * 40 * visible
+        tflops = flops / (ms * 1e-3) / 1e12
+        peak_tf, peak_tf_kind = measured_bf16_peak()
+        tokens = int(nq.sum())
+        value = (int(lens.sum()) * 40 * 128 * 4) / (ms * 1e-3) / 1e9
+        line.update(config={"workload": "chunked prefill: 16 seqs x 512-token chunk on contexts "
+                                        "U[512,2048], 40 heads x 128, bf16, block 16",
+                            "queries": tokens, "context_tokens": int(lens.sum())},
+                    dtype="bf16",
+                    roofline={"kernel": "paged_prefill_kernel", "bound": "tensor",
+                              "achieved": round(tflops, 2), "peak": peak_tf,
+                              "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
+                              "peak_source": peak_tf_kind, "flops_per_launch": flops,
+                              "note": "useful flops (causal, 4*D per visible query-key pair); "
+                                      "the kernel issues P.V twice (hi + lo parts)"})
     else:
         raise SystemExit(f"unknown workload {w}")
     if B.pa_error_read(rec) != [0, 0, 0, 0]:
@@ -675,7 +718,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="13b",
-                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed"],
+                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "prefill"],
                     help="13b (default, the headline line) or another seeded workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
