@@ -197,8 +197,9 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  *   out           device [total_queries][num_heads][head_dim] in `out_dtype`
  * Rows of out outside every sequence's query range are not written.  A sequence
  * whose range is inconsistent (Q_i > L, range outside q, Q_i > max_query_len) is
- * recorded as PA_ERR_BAD_SEQ_LEN and skipped.  Other arguments as for
- * paged_attn_decode; num_blocks * num_heads * block_size must be < 2^31. */
+ * recorded as PA_ERR_BAD_SEQ_LEN and skipped.  scale must be > 0.  Other
+ * arguments as for paged_attn_decode; num_blocks * num_heads * block_size must
+ * be < 2^31. */
 int paged_attn_prefill(const void* q, const int32_t* query_start, int total_queries,
                        int max_query_len, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,

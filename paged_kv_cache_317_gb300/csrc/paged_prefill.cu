@@ -7,18 +7,25 @@
 // physical scatter").  With >1 query per head the work is a dense contraction,
 // so it runs on tensor cores:
 //
-//  * block = (128-query tile, head, sequence); 6 warps: 4 softmax warps (one
-//    query row per thread = one TMEM lane), 1 TMA producer warp, 1 MMA warp.
+//  * block = (128-query tile, head, sequence); 7 warps: 4 softmax warps (one
+//    query row per thread = one TMEM lane), a K producer warp, an MMA warp and
+//    a V producer warp.
 //  * Q tile: one 3-D TMA load per 64-wide half of head_dim (128B swizzle).
-//    K/V: per 16-key chunk the producer follows the block table and issues
-//    2-D TMA loads of the rows (128B swizzle) into a 2-stage ring of 64-key tiles.
-//  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16) into one of two TMEM S
-//    buffers; the next tile's S overlaps the current tile's softmax.
+//    K/V: per 16-key chunk the producer follows the block table (32 entries
+//    fetched at a time) and issues 2-D TMA loads of the rows (128B swizzle) into
+//    a 4-stage K ring and a 3-stage V ring of 64-key tiles, each fed by its own
+//    warp; a K tile is released as soon as its S MMA completes, a V tile when
+//    its P.V completes.
+//  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16) into one of four TMEM S
+//    buffers, issued three tiles ahead of P.V so that a tile's S never waits in
+//    the in-order tensor pipe behind the previous tiles' P.V.
 //  * Softmax warps: tcgen05.ld their S row, causal/length mask, online softmax
 //    in log2 units; P is written to shared memory as bf16/fp16 hi + lo parts
 //    (hi = round(p), lo = round(p - hi)), so P.V carries ~16 more mantissa bits
 //    than a single half-precision P and stays within the fp32-accumulation error
-//    bound; when the running max grows they rescale O in TMEM.
+//    bound.  P is double-buffered, so softmax(j) only waits for P.V(j-2).  The
+//    exponentials use a per-row reference max that moves only when the running
+//    max passes it by 2^8; only then is O rescaled in TMEM (after P.V(j-1)).
 //  * O += P V: 4 + 4 tcgen05.mma (M=128, N=128, K=16 keys; V as an MN-major
 //    operand) accumulating in TMEM; the last tile's P.V completion releases
 //    the epilogue: O / l, stored as rows of out.
@@ -41,26 +48,36 @@ namespace {
 constexpr int kQTile = 128;                       // query rows per block (MMA M)
 constexpr int kKTile = 64;                        // keys per tile
 constexpr int kHeadDim = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
+constexpr int kKStages = 4;                       // K ring depth
+constexpr int kVStages = 3;                       // V ring depth
+constexpr int kSBufs = 4;                         // S buffers in TMEM (S issued 3 tiles ahead)
 constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B (one 64-wide half)
 constexpr int kQBytes = kQTile * kHeadDim * 2;    // 32 KB (two 16 KB halves)
-constexpr int kKBytes = 2 * kHalfBytes;           // 16 KB
-constexpr int kStageBytes = 2 * kKBytes;          // K + V
-constexpr int kPBytes = kQTile * kKTile * 2;      // 16 KB
+constexpr int kTileBytes = 2 * kHalfBytes;        // one K or V tile: 16 KB
+constexpr int kPBytes = kQTile * kKTile * 2;      // 16 KB per P part
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + 2 * kStageBytes;
-constexpr int kOffPlo = kOffP + kPBytes;
-constexpr int kOffBar = kOffPlo + kPBytes;
+constexpr int kOffP = kOffQ + kQBytes;            // 2 buffers x (hi, lo)
+constexpr int kOffK = kOffP + 4 * kPBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align to 1 KB
-constexpr uint32_t kTmemCols = 256;               // S buffers [0,64) [64,128), O [128,256)
+constexpr uint32_t kTmemCols = 512;               // S buffers [0,256), O [256,384)
+constexpr uint32_t kTmemO = kSBufs * kKTile;
 constexpr float kLog2e = 1.4426950408889634f;
+// A row's exponentials are taken against a reference max that only moves when
+// the running max exceeds it by more than this (log2 units): p <= 2^8, exact in
+// fp32, and O is rescaled only then.
+constexpr float kRescaleThreshold = 8.0f;
 
 struct Bars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, o_done, drain;
+  uint64_t q_full;
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[kSBufs], s_free[kSBufs], p_full[2], pv_done[2], drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct PrefillParams {
   const int32_t* query_start;
@@ -156,6 +173,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
                : "memory");
 }
 
+// 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32;
+// relative error ~2^-22, 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -216,23 +241,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* Qs = smem + kOffQ;
-  uint8_t* Ps = smem + kOffP;
-  uint8_t* Plo = smem + kOffPlo;
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bars->abort;
-  auto stage_k = [&](int s) { return smem + kOffKV + s * kStageBytes; };
-  auto stage_v = [&](int s) { return smem + kOffKV + s * kStageBytes + kKBytes; };
+  auto p_hi = [&](int b) { return smem + kOffP + b * 2 * kPBytes; };
+  auto p_lo = [&](int b) { return smem + kOffP + b * 2 * kPBytes + kPBytes; };
+  auto k_tile = [&](int s) { return smem + kOffK + s * kTileBytes; };
+  auto v_tile = [&](int s) { return smem + kOffV + s * kTileBytes; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], kQTile);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
     }
-    mbar_init(&bars->p_full, kQTile);
-    mbar_init(&bars->o_done, 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], kQTile);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->p_full[b], kQTile);
+      mbar_init(&bars->pv_done[b], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -249,51 +282,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  int kv_issued = 0;        // producer lane 0: tiles whose loads were issued
-  int mma_started = 0;      // MMA lane 0: whether any MMA was issued
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  int kv_issued = 0;  // producer lane 0: tiles whose loads (K for warp 4, V for warp 6) were issued
+  int mma_started = 0;             // MMA lane 0: whether any MMA was issued
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------- producers: K (warp 4), V (warp 6)
+    const bool is_v = (warp == 6);
+    const int stages = is_v ? kVStages : kKStages;
     const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-    if (lane == 0) {
+    if (!is_v && lane == 0) {
       mbar_arrive_expect_tx(&bars->q_full, kQBytes);
       tma_load_3d(Qs, &tm_q, 0, h, q_begin + q0, &bars->q_full);
       tma_load_3d(Qs + kQBytes / 2, &tm_q, 64, h, q_begin + q0, &bars->q_full);
     }
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    int blk = 0;
     for (int j = 0; j < T; ++j) {
-      // lanes 0..3 look up the physical block of the tile's four 16-key chunks
-      const int key0 = j * kKTile + lane * 16;
-      int blk = 0;
-      if (lane < 4 && key0 < keys) {
-        blk = __ldg(table + key0 / p.block_size);
-        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-          report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
-          blk = 0;
+      if ((j & 7) == 0) {
+        // lane l looks up the physical block of 16-key chunk 4*j + l (8 tiles' worth)
+        const int key0 = (j * 4 + lane) * 16;
+        blk = 0;
+        if (key0 < keys) {
+          blk = __ldg(table + key0 / p.block_size);
+          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+            if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
+            blk = 0;
+          }
         }
       }
+      const int s = j % stages, use = j / stages;
+      const int n = min(4, (keys - j * kKTile + 15) / 16);  // chunks holding visible keys
+      uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
+      uint64_t* empty = is_v ? &bars->v_empty[s] : &bars->k_empty[s];
+      uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
       int ok = 1;
       if (lane == 0) {
-        const int s = j & 1;
-        if (j >= 2) ok = mbar_wait_bounded(&bars->kv_empty[s], ((j >> 1) - 1) & 1);
-        if (!ok) {
-          *abort_flag = 1;
-          report_error(p.err, PA_ERR_TIMEOUT, seq, j);
-        } else {
-          const int n = min(4, (keys - j * kKTile + 15) / 16);
-          mbar_arrive_expect_tx(&bars->kv_full[s], static_cast<uint32_t>(n) * 4 * 2048);
-        }
+        if (use > 0) ok = mbar_wait_bounded(empty, (use - 1) & 1);
+        if (ok) mbar_arrive_expect_tx(full, static_cast<uint32_t>(n) * 2 * 2048);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
-      if (!ok) break;
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          report_error(p.err, PA_ERR_TIMEOUT, seq, j);
+        }
+        break;
+      }
       for (int c = 0; c < 4; ++c) {
-        const int b = __shfl_sync(kFullMask, blk, c);
+        const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
         const int k0 = j * kKTile + c * 16;
         if (lane == 0 && k0 < keys) {
-          const int s = j & 1;
           const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
-          tma_load_2d(stage_k(s) + c * 2048, &tm_k, 0, row, &bars->kv_full[s]);
-          tma_load_2d(stage_k(s) + kHalfBytes + c * 2048, &tm_k, 64, row, &bars->kv_full[s]);
-          tma_load_2d(stage_v(s) + c * 2048, &tm_v, 0, row, &bars->kv_full[s]);
-          tma_load_2d(stage_v(s) + kHalfBytes + c * 2048, &tm_v, 64, row, &bars->kv_full[s]);
+          tma_load_2d(dst + c * 2048, map, 0, row, full);
+          tma_load_2d(dst + kHalfBytes + c * 2048, map, 64, row, full);
         }
       }
       kv_issued = j + 1;
@@ -307,43 +347,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = make_idesc(kQTile, kHeadDim, BF16, true);
       bool ok = mbar_wait_bounded(&bars->q_full, 0);
       auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait_bounded(&bars->kv_full[s], (j >> 1) & 1)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&bars->s_free[s], ((j >> 1) - 1) & 1)) return false;
+        const int s = j % kKStages, b = j % kSBufs;
+        if (!mbar_wait_bounded(&bars->k_full[s], (j / kKStages) & 1)) return false;
+        if (j >= kSBufs && !mbar_wait_bounded(&bars->s_free[b], ((j / kSBufs) - 1) & 1))
+          return false;
         tc_fence_after();
-        const uint8_t* ks = stage_k(s);
+        const uint8_t* ks = k_tile(s);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
           const int half = kk >> 2, off = (kk & 3) * 32;
           const uint64_t a = smem_desc_sw128(Qs + half * (kQBytes / 2) + off, 16, 1024);
-          const uint64_t b = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
-          mma_f16(tmem + s * kKTile, a, b, idesc_s, kk > 0);
+          const uint64_t bd = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
+          mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
         }
-        mma_commit(&bars->s_full[s]);
+        mma_commit(&bars->s_full[b]);
+        mma_commit(&bars->k_empty[s]);
         mma_started = 1;
         return true;
       };
-      if (ok) ok = issue_s(0);
+      // S runs kSBufs - 1 tiles ahead of P.V, so the in-order tensor pipe never
+      // holds a softmax waiting behind the previous tiles' P.V.
+      for (int t = 0; ok && t < kSBufs - 1 && t < T; ++t) ok = issue_s(t);
       for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T && !issue_s(j + 1)) {
+        if (j + kSBufs - 1 < T && !issue_s(j + kSBufs - 1)) {
           ok = false;
           break;
         }
-        if (!mbar_wait_bounded(&bars->p_full, j & 1)) {
+        const int s = j % kVStages, b = j & 1;
+        if (!mbar_wait_bounded(&bars->p_full[b], (j >> 1) & 1) ||
+            !mbar_wait_bounded(&bars->v_full[s], (j / kVStages) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint8_t* vs = stage_v(j & 1);
+        const uint8_t* vs = v_tile(s);
+        const uint8_t* ph = p_hi(b);
+        const uint8_t* pl = p_lo(b);
 #pragma unroll
         for (int kk = 0; kk < kKTile / 16; ++kk) {
-          const uint64_t b = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
-          mma_f16(tmem + 128, smem_desc_sw128(Ps + kk * 32, 16, 1024), b, idesc_o,
+          const uint64_t bd = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
+          mma_f16(tmem + kTmemO, smem_desc_sw128(ph + kk * 32, 16, 1024), bd, idesc_o,
                   (j > 0 || kk > 0) ? 1u : 0u);
-          mma_f16(tmem + 128, smem_desc_sw128(Plo + kk * 32, 16, 1024), b, idesc_o, 1u);
+          mma_f16(tmem + kTmemO, smem_desc_sw128(pl + kk * 32, 16, 1024), bd, idesc_o, 1u);
         }
-        mma_commit(&bars->o_done);
-        mma_commit(&bars->kv_empty[j & 1]);
+        mma_commit(&bars->pv_done[b]);
+        mma_commit(&bars->v_empty[s]);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -357,62 +405,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = r < rows;
     const int pos = row_valid ? pos0 + r : -1;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // reference max (log2 units) and running sum
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[b], (j >> 1) & 1));
+      const int b = j & 1, sb = j % kSBufs;
+      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[sb], (j / kSBufs) & 1));
       if (!ok) break;
       tc_fence_after();
       float sv[kKTile];
       {
         float t[32];
-        tmem_ld32(tmem + lane_base + b * kKTile, t);
+        tmem_ld32(tmem + lane_base + sb * kKTile, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = t[c];
-        tmem_ld32(tmem + lane_base + b * kKTile + 32, t);
+        tmem_ld32(tmem + lane_base + sb * kKTile + 32, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
       }
       tc_fence_before();
-      mbar_arrive(&bars->s_free[b]);
+      mbar_arrive(&bars->s_free[sb]);
 
+      // Raw scores; keys a row may not see become -inf.  Only tiles that
+      // cross some row's causal limit (the diagonal and the last tile) need it.
       const int kbase = j * kKTile;
-      float mt = -INFINITY;
+      if (!__all_sync(kFullMask, kbase + kKTile - 1 <= pos)) {
 #pragma unroll
-      for (int c = 0; c < kKTile; ++c) {
-        const float u = (kbase + c <= pos) ? sv[c] * p.qscale : -INFINITY;
-        sv[c] = u;
-        mt = fmaxf(mt, u);
+        for (int c = 0; c < kKTile; ++c) sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
       }
-      const float m_new = fmaxf(m, mt);
-      const bool none = (m_new == -INFINITY);  // no key seen yet (or an unused row)
-      const float alpha = none ? 1.f : exp2f(m - m_new);
-      float rowsum = 0.f;
+      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int c = 4; c < kKTile; c += 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], sv[c + i]);
+      }
+      // scale > 0, so the max of the scaled scores is the scaled max (log2 units)
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.qscale;
+      // Move the reference only when the tile's max exceeds it by the threshold.
+      float alpha = 1.f;
+      if (mt > m_ref + kRescaleThreshold) {
+        alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+        m_ref = mt;
+      }
+      // No visible key yet (or an unused row): a -inf offset makes every p zero.
+      const float neg_ref = (m_ref == -INFINITY) ? -INFINITY : -m_ref;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kKTile; ++c) {
-        const float e = none ? 0.f : exp2f(sv[c] - m_new);
+        const float e = ex2_approx(fmaf(sv[c], p.qscale, neg_ref));
         sv[c] = e;
-        rowsum += e;
+        sum4[c & 3] += e;
       }
-      // P.V of the previous tile must be done before P and O are touched.
-      if (j > 0) {
-        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->o_done, (j - 1) & 1));
+      const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      // O must not change under a running P.V: rescaling waits for P.V(j-1).
+      const bool rescale = __any_sync(kFullMask, alpha != 1.f) && j > 0;
+      if (rescale) {
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[(j - 1) & 1],
+                                                     ((j - 1) >> 1) & 1));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tmem_ld32(tmem + lane_base + 128 + cc * 32, o);
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tmem + lane_base + 128 + cc * 32, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + lane_base + kTmemO + cc * 32, o);
         }
+        tmem_wait_st();
+      }
+      // P buffer b was last read by P.V(j-2)
+      if (j >= 2) {
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[b], ((j >> 1) - 1) & 1));
+        if (!ok) break;
       }
       // P as hi + lo halves, rows of 128 B in the 128B-swizzled K-major layout
+      uint8_t* ph = p_hi(b);
+      uint8_t* pl = p_lo(b);
 #pragma unroll
       for (int ch = 0; ch < kKTile / 8; ++ch) {
         uint32_t hi[4], lo[4];
@@ -425,13 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo[i] = pack_half2<BF16>(a - ra, bb - rb);
         }
         const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(Ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(Plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      // keys past the last one any row may see: zero their V rows (they may hold
-      // stale or unused-slot data, and 0 * NaN would poison the accumulator)
+      // keys past the last one any row may see: zero their V rows once the tile
+      // has landed (they may hold stale or unused-slot data; 0 * NaN is NaN)
       if (j == T - 1 && keys < kbase + kKTile) {
-        uint8_t* vs = stage_v(j & 1);
+        const int s = j % kVStages;
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->v_full[s], (j / kVStages) & 1));
+        if (!ok) break;
+        uint8_t* vs = v_tile(s);
         const int first = keys - kbase;
         const int n16 = (kKTile - first) * 2 * 8;  // rows x halves x 16-byte pieces
         for (int idx = r; idx < n16; idx += kQTile) {
@@ -442,16 +513,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       l = l * alpha + rowsum;
-      m = m_new;
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->p_full[b]);
       if (__shfl_sync(kFullMask, *abort_flag, 0)) {
         ok = false;
         break;
       }
     }
-    if (ok) ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->o_done, (T - 1) & 1));
+    if (ok)
+      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[(T - 1) & 1],
+                                                   ((T - 1) >> 1) & 1));
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -460,12 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         float o[32];
-        tmem_ld32(tmem + lane_base + 128 + cc * 32, o);
+        tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] *= inv;
         if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
+          for (int i = 0; i < 32; i += 8)
+            store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
         }
       }
     } else if (lane == 0) {
@@ -479,12 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag) {
     // Let every copy and MMA this block started finish before its shared
     // memory and TMEM are released (bounded waits).
-    if (warp == 4 && lane == 0) {
-      for (int s = 0; s < 2 && s < kv_issued; ++s) {
-        const int last = s + ((kv_issued - 1 - s) / 2) * 2;
-        mbar_wait_bounded(&bars->kv_full[s], (last >> 1) & 1);
+    if ((warp == 4 || warp == 6) && lane == 0) {
+      const bool is_v = (warp == 6);
+      const int stages = is_v ? kVStages : kKStages;
+      for (int s = 0; s < stages && s < kv_issued; ++s) {
+        const int last = s + ((kv_issued - 1 - s) / stages) * stages;
+        mbar_wait_bounded(is_v ? &bars->v_full[s] : &bars->k_full[s], (last / stages) & 1);
       }
-      mbar_wait_bounded(&bars->q_full, 0);
+      if (!is_v) mbar_wait_bounded(&bars->q_full, 0);
     }
     if (warp == 5 && lane == 0 && mma_started) {
       mma_commit(&bars->drain);
@@ -561,7 +636,8 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
     return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || num_seqs > 65535 || num_heads > 65535) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || num_seqs > 65535 || num_heads > 65535)
+    return PA_ERR_INVALID_ARG;
   const unsigned long long cache_rows =
       static_cast<unsigned long long>(num_blocks) * num_heads * block_size;
   if (cache_rows >= (1ull << 31) || static_cast<long long>(max_blocks_per_seq) * block_size >
