@@ -7,9 +7,9 @@
 // physical scatter").  With >1 query per head the work is a dense contraction,
 // so it runs on tensor cores:
 //
-//  * block = (128-query tile, head, sequence); 7 warps: 4 softmax warps (one
-//    query row per thread = one TMEM lane), a K producer warp, an MMA warp and
-//    a V producer warp.
+//  * block = (128-query tile, head, sequence); 11 warps: two softmax
+//    warpgroups (one query row per thread = one TMEM lane) taking alternate key
+//    tiles, a K producer warp, an MMA warp and a V producer warp.
 //  * Q tile: one 3-D TMA load per 64-wide half of head_dim (128B swizzle).
 //    K/V: per 16-key chunk the producer follows the block table (32 entries
 //    fetched at a time) and issues 2-D TMA loads of the rows (128B swizzle) into
@@ -23,12 +23,14 @@
 //    in log2 units; P is written to shared memory as bf16/fp16 hi + lo parts
 //    (hi = round(p), lo = round(p - hi)), so P.V carries ~16 more mantissa bits
 //    than a single half-precision P and stays within the fp32-accumulation error
-//    bound.  P is double-buffered, so softmax(j) only waits for P.V(j-2).  The
-//    exponentials use a per-row reference max that moves only when the running
-//    max passes it by 2^8; only then is O rescaled in TMEM (after P.V(j-1)).
+//    bound.  Each warpgroup has its own P buffer, O accumulator in TMEM and
+//    running (max, sum), so tile j only waits for P.V(j-2).  The exponentials
+//    use a per-row reference max that moves only when the running max passes it
+//    by 2^8; only then is that warpgroup's O rescaled.  The epilogue merges the
+//    two accumulators by log-sum-exp.
 //  * O += P V: 4 + 4 tcgen05.mma (M=128, N=128, K=16 keys; V as an MN-major
-//    operand) accumulating in TMEM; the last tile's P.V completion releases
-//    the epilogue: O / l, stored as rows of out.
+//    operand) accumulating in TMEM; each warpgroup's last P.V completion
+//    releases the epilogue, which writes the merged rows of out.
 //  * Every mbarrier wait is bounded (one second); on a timeout the block
 //    records PA_ERR_TIMEOUT, waits (bounded) for its copies and MMAs, frees its
 //    TMEM and returns.  Nothing traps.
@@ -48,7 +50,9 @@ namespace {
 constexpr int kQTile = 128;                       // query rows per block (MMA M)
 constexpr int kKTile = 64;                        // keys per tile
 constexpr int kHeadDim = 128;
-constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
+constexpr int kThreads = 352;                     // 8 softmax, K producer, MMA, V producer
+constexpr int kSoftmaxThreads = 256;              // two warpgroups, alternate tiles
+constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
 constexpr int kKStages = 4;                       // K ring depth
 constexpr int kVStages = 3;                       // V ring depth
 constexpr int kSBufs = 4;                         // S buffers in TMEM (S issued 3 tiles ahead)
@@ -61,8 +65,9 @@ constexpr int kOffP = kOffQ + kQBytes;            // 2 buffers x (hi, lo)
 constexpr int kOffK = kOffP + 4 * kPBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align to 1 KB
-constexpr uint32_t kTmemCols = 512;               // S buffers [0,256), O [256,384)
+constexpr int kOffXch = kOffBar + 256;            // per-row (max, sum) of each warpgroup
+constexpr int kSmemBytes = kOffXch + 2 * kQTile * 8 + 1024;  // + slack to align to 1 KB
+constexpr uint32_t kTmemCols = 512;               // S buffers [0,256), O0 [256,384), O1 [384,512)
 constexpr uint32_t kTmemO = kSBufs * kKTile;
 constexpr float kLog2e = 1.4426950408889634f;
 // A row's exponentials are taken against a reference max that only moves when
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&bars->tmem_base)),
                  "r"(kTmemCols)
@@ -284,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int kv_issued = 0;  // producer lane 0: tiles whose loads (K for warp 4, V for warp 6) were issued
   int mma_started = 0;             // MMA lane 0: whether any MMA was issued
-  if (warp == 4 || warp == 6) {
-    // ------------------------------------------------- producers: K (warp 4), V (warp 6)
-    const bool is_v = (warp == 6);
+  if (warp == kWarpK || warp == kWarpV) {
+    // ------------------------------------------------- producers: K and V
+    const bool is_v = (warp == kWarpV);
     const int stages = is_v ? kVStages : kKStages;
     const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
     if (!is_v && lane == 0) {
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(kQTile, kKTile, BF16, false);
@@ -386,9 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kKTile / 16; ++kk) {
           const uint64_t bd = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
-          mma_f16(tmem + kTmemO, smem_desc_sw128(ph + kk * 32, 16, 1024), bd, idesc_o,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-          mma_f16(tmem + kTmemO, smem_desc_sw128(pl + kk * 32, 16, 1024), bd, idesc_o, 1u);
+          // tile j accumulates into its warpgroup's O (the first tile of each
+          // warpgroup overwrites)
+          const uint32_t o_tmem = tmem + kTmemO + b * kHeadDim;
+          mma_f16(o_tmem, smem_desc_sw128(ph + kk * 32, 16, 1024), bd, idesc_o,
+                  (j > 1 || kk > 0) ? 1u : 0u);
+          mma_f16(o_tmem, smem_desc_sw128(pl + kk * 32, 16, 1024), bd, idesc_o, 1u);
         }
         mma_commit(&bars->pv_done[b]);
         mma_commit(&bars->v_empty[s]);
@@ -401,14 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x;  // query row = TMEM lane
+    // Warpgroup wg takes tiles wg, wg + 2, ... with its own O accumulator,
+    // reference max and sum; the epilogue merges the two by log-sum-exp.
+    const int wg = threadIdx.x / kQTile;
+    const int r = threadIdx.x % kQTile;  // query row = TMEM lane
+    const int wq = warp & 3;             // TMEM lane quarter of this warp
     const bool row_valid = r < rows;
     const int pos = row_valid ? pos0 + r : -1;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t o_tmem = tmem + lane_base + kTmemO + wg * kHeadDim;
     float m_ref = -INFINITY, l = 0.f;  // reference max (log2 units) and running sum
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j & 1, sb = j % kSBufs;
+    int last = -1;                     // this warpgroup's last tile
+    for (int j = wg; j < T; j += 2) {
+      const int b = wg, sb = j % kSBufs;
       ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[sb], (j / kSBufs) & 1));
       if (!ok) break;
       tc_fence_after();
@@ -456,27 +470,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         sum4[c & 3] += e;
       }
       const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // O must not change under a running P.V: rescaling waits for P.V(j-1).
-      const bool rescale = __any_sync(kFullMask, alpha != 1.f) && j > 0;
-      if (rescale) {
-        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[(j - 1) & 1],
-                                                     ((j - 1) >> 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + lane_base + kTmemO + cc * 32, o);
-        }
-        tmem_wait_st();
-      }
-      // P buffer b was last read by P.V(j-2)
+      // This warpgroup's previous tile (P buffer b, O accumulator wg) must be
+      // through P.V before P is rewritten or O rescaled.
       if (j >= 2) {
         ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[b], ((j >> 1) - 1) & 1));
         if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(kFullMask, alpha != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(o_tmem + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(o_tmem + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
       }
       // P as hi + lo halves, rows of 128 B in the 128B-swizzled K-major layout
       uint8_t* ph = p_hi(b);
@@ -516,34 +526,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[b]);
+      last = j;
       if (__shfl_sync(kFullMask, *abort_flag, 0)) {
         ok = false;
         break;
       }
     }
-    if (ok)
-      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[(T - 1) & 1],
-                                                   ((T - 1) >> 1) & 1));
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t row_off =
-          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= inv;
-        if (row_valid) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 8)
-            store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
-        }
-      }
-    } else if (lane == 0) {
+    // publish (max, sum) per row; both warpgroups always reach the barrier once
+    float2* xch = reinterpret_cast<float2*>(smem + kOffXch);
+    xch[wg * kQTile + r] = make_float2(m_ref, last >= 0 ? l : 0.f);
+    if (!ok && lane == 0) {
       *abort_flag = 1;
       report_error(p.err, PA_ERR_TIMEOUT, seq, -2);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+    if (!__shfl_sync(kFullMask, *abort_flag, 0)) {
+      // the epilogue reads both accumulators: wait for each one's last P.V
+      bool ready = true;
+      for (int w = 0; w < 2; ++w) {
+        if (T > w) {
+          const int last_w = w + 2 * ((T - 1 - w) / 2);
+          ready = ready && mbar_wait_bounded(&bars->pv_done[w], (last_w >> 1) & 1);
+        }
+      }
+      ready = __all_sync(kFullMask, ready);
+      if (!ready && lane == 0) {
+        *abort_flag = 1;
+        report_error(p.err, PA_ERR_TIMEOUT, seq, -3);
+      }
+      if (ready) {
+        tc_fence_after();
+        const float2 a = xch[r], c = xch[kQTile + r];
+        const float M = fmaxf(a.x, c.x);
+        const float w0 = a.y > 0.f ? exp2f(a.x - M) : 0.f;
+        const float w1 = c.y > 0.f ? exp2f(c.x - M) : 0.f;
+        const float den = w0 * a.y + w1 * c.y;
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const uint32_t o0 = tmem + lane_base + kTmemO, o1 = o0 + kHeadDim;
+        const size_t row_off =
+            (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
+        // warpgroup wg writes columns [64 wg, 64 wg + 64)
+  #pragma unroll 1
+        for (int cc = 2 * wg; cc < 2 * wg + 2; ++cc) {
+          float x[32], y[32];
+          tmem_ld32(o0 + cc * 32, x);
+          tmem_ld32(o1 + cc * 32, y);
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float u = w0 > 0.f ? x[i] : 0.f;  // an unused accumulator holds garbage
+            const float v = w1 > 0.f ? y[i] : 0.f;
+            x[i] = (w0 * u + w1 * v) * inv;
+          }
+          if (row_valid) {
+  #pragma unroll
+            for (int i = 0; i < 32; i += 8)
+              store_out<8>(p.out, row_off + cc * 32 + i, x + i, p.out_dtype);
+          }
+        }
+      }
     }
   }
 
@@ -552,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort_flag) {
     // Let every copy and MMA this block started finish before its shared
     // memory and TMEM are released (bounded waits).
-    if ((warp == 4 || warp == 6) && lane == 0) {
-      const bool is_v = (warp == 6);
+    if ((warp == kWarpK || warp == kWarpV) && lane == 0) {
+      const bool is_v = (warp == kWarpV);
       const int stages = is_v ? kVStages : kKStages;
       for (int s = 0; s < stages && s < kv_issued; ++s) {
         const int last = s + ((kv_issued - 1 - s) / stages) * stages;
@@ -561,14 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!is_v) mbar_wait_bounded(&bars->q_full, 0);
     }
-    if (warp == 5 && lane == 0 && mma_started) {
+    if (warp == kWarpMma && lane == 0 && mma_started) {
       mma_commit(&bars->drain);
       mbar_wait_bounded(&bars->drain, 0);
     }
     __syncthreads();
   }
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
