@@ -50,25 +50,22 @@ namespace {
 constexpr int kQTile = 128;                       // query rows per block (MMA M)
 constexpr int kKTile = 64;                        // keys per tile
 constexpr int kHeadDim = 128;
-constexpr int kThreads = 352;                     // 8 softmax, K producer, MMA, V producer
-constexpr int kSoftmaxThreads = 256;              // two warpgroups, alternate tiles
-constexpr int kWarpK = 8, kWarpMma = 9, kWarpV = 10;
-constexpr int kKStages = 4;                       // K ring depth
-constexpr int kVStages = 3;                       // V ring depth
-constexpr int kSBufs = 4;                         // S buffers in TMEM (S issued 3 tiles ahead)
+constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
+constexpr int kWarpK = 4, kWarpMma = 5, kWarpV = 6;
+constexpr int kKStages = 2;                       // K ring depth
+constexpr int kVStages = 2;                       // V ring depth
 constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B (one 64-wide half)
 constexpr int kQBytes = kQTile * kHeadDim * 2;    // 32 KB (two 16 KB halves)
 constexpr int kTileBytes = 2 * kHalfBytes;        // one K or V tile: 16 KB
-constexpr int kPBytes = kQTile * kKTile * 2;      // 16 KB per P part
 constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;            // 2 buffers x (hi, lo)
-constexpr int kOffK = kOffP + 4 * kPBytes;
+constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kOffXch = kOffBar + 256;            // per-row (max, sum) of each warpgroup
-constexpr int kSmemBytes = kOffXch + 2 * kQTile * 8 + 1024;  // + slack to align to 1 KB
-constexpr uint32_t kTmemCols = 512;               // S buffers [0,256), O0 [256,384), O1 [384,512)
-constexpr uint32_t kTmemO = kSBufs * kKTile;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align to 1 KB
+// TMEM: two S/P buffers of 64 columns (S in fp32; after the softmax, P hi in the
+// first 32 columns and P lo in the next 32, two 16-bit values per column) and O.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemO = 2 * kKTile;
 constexpr float kLog2e = 1.4426950408889634f;
 // A row's exponentials are taken against a reference max that only moves when
 // the running max exceeds it by more than this (log2 units): p <= 2^8, exact in
@@ -78,7 +75,9 @@ constexpr float kRescaleThreshold = 8.0f;
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[kSBufs], s_free[kSBufs], p_full[2], pv_done[2], drain;
+  // s_free[b] completes when the P.V of buffer b's tile finishes (one phase
+  // per two tiles), so it doubles as that P.V's completion signal.
+  uint64_t s_full[2], s_free[2], p_full[2], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -153,6 +152,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
       : "memory");
 }
 
+// Same, with A read from tensor memory (M rows = lanes, K values packed two per
+// 32-bit column).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -214,7 +224,7 @@ __device__ __forceinline__ float half_to_float(uint32_t bits16) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -248,8 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* Qs = smem + kOffQ;
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bars->abort;
-  auto p_hi = [&](int b) { return smem + kOffP + b * 2 * kPBytes; };
-  auto p_lo = [&](int b) { return smem + kOffP + b * 2 * kPBytes + kPBytes; };
   auto k_tile = [&](int s) { return smem + kOffK + s * kTileBytes; };
   auto v_tile = [&](int s) { return smem + kOffV + s * kTileBytes; };
 
@@ -263,13 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < kSBufs; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], kQTile);
-    }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 1);
       mbar_init(&bars->p_full[b], kQTile);
-      mbar_init(&bars->pv_done[b], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -287,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  int kv_issued = 0;  // producer lane 0: tiles whose loads (K for warp 4, V for warp 6) were issued
-  int mma_started = 0;             // MMA lane 0: whether any MMA was issued
+  int kv_issued = 0;   // producer lane 0: tiles whose loads (K or V) were issued
+  int mma_started = 0; // MMA lane 0: whether any MMA was issued
   if (warp == kWarpK || warp == kWarpV) {
     // ------------------------------------------------- producers: K and V
     const bool is_v = (warp == kWarpV);
@@ -351,11 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = make_idesc(kQTile, kKTile, BF16, false);
       constexpr uint32_t idesc_o = make_idesc(kQTile, kHeadDim, BF16, true);
       bool ok = mbar_wait_bounded(&bars->q_full, 0);
+      // S_j goes to TMEM buffer j & 1, whose previous contents (P of tile j-2)
+      // must have been consumed by P.V(j-2).
       auto issue_s = [&](int j) -> bool {
-        const int s = j % kKStages, b = j % kSBufs;
+        const int s = j % kKStages, b = j & 1;
         if (!mbar_wait_bounded(&bars->k_full[s], (j / kKStages) & 1)) return false;
-        if (j >= kSBufs && !mbar_wait_bounded(&bars->s_free[b], ((j / kSBufs) - 1) & 1))
-          return false;
+        if (j >= 2 && !mbar_wait_bounded(&bars->s_free[b], ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
         const uint8_t* ks = k_tile(s);
 #pragma unroll
@@ -370,11 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_started = 1;
         return true;
       };
-      // S runs kSBufs - 1 tiles ahead of P.V, so the in-order tensor pipe never
-      // holds a softmax waiting behind the previous tiles' P.V.
-      for (int t = 0; ok && t < kSBufs - 1 && t < T; ++t) ok = issue_s(t);
+      if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < T; ++j) {
-        if (j + kSBufs - 1 < T && !issue_s(j + kSBufs - 1)) {
+        if (j + 1 < T && !issue_s(j + 1)) {
           ok = false;
           break;
         }
@@ -386,19 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint8_t* vs = v_tile(s);
-        const uint8_t* ph = p_hi(b);
-        const uint8_t* pl = p_lo(b);
+        const uint32_t ph = tmem + b * kKTile, pl = ph + kKTile / 2;
 #pragma unroll
         for (int kk = 0; kk < kKTile / 16; ++kk) {
           const uint64_t bd = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
-          // tile j accumulates into its warpgroup's O (the first tile of each
-          // warpgroup overwrites)
-          const uint32_t o_tmem = tmem + kTmemO + b * kHeadDim;
-          mma_f16(o_tmem, smem_desc_sw128(ph + kk * 32, 16, 1024), bd, idesc_o,
-                  (j > 1 || kk > 0) ? 1u : 0u);
-          mma_f16(o_tmem, smem_desc_sw128(pl + kk * 32, 16, 1024), bd, idesc_o, 1u);
+          mma_f16_ts(tmem + kTmemO, ph + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + kTmemO, pl + kk * 8, bd, idesc_o, 1u);
         }
-        mma_commit(&bars->pv_done[b]);
+        mma_commit(&bars->s_free[b]);
         mma_commit(&bars->v_empty[s]);
       }
       if (!ok) {
@@ -409,36 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Warpgroup wg takes tiles wg, wg + 2, ... with its own O accumulator,
-    // reference max and sum; the epilogue merges the two by log-sum-exp.
-    const int wg = threadIdx.x / kQTile;
-    const int r = threadIdx.x % kQTile;  // query row = TMEM lane
-    const int wq = warp & 3;             // TMEM lane quarter of this warp
+    const int r = threadIdx.x;  // query row = TMEM lane
     const bool row_valid = r < rows;
     const int pos = row_valid ? pos0 + r : -1;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t o_tmem = tmem + lane_base + kTmemO + wg * kHeadDim;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;  // reference max (log2 units) and running sum
     bool ok = true;
-    int last = -1;                     // this warpgroup's last tile
-    for (int j = wg; j < T; j += 2) {
-      const int b = wg, sb = j % kSBufs;
-      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[sb], (j / kSBufs) & 1));
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[b], (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
       float sv[kKTile];
       {
         float t[32];
-        tmem_ld32(tmem + lane_base + sb * kKTile, t);
+        tmem_ld32(tmem + lane_base + b * kKTile, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[c] = t[c];
-        tmem_ld32(tmem + lane_base + sb * kKTile + 32, t);
+        tmem_ld32(tmem + lane_base + b * kKTile + 32, t);
 #pragma unroll
         for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
       }
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[sb]);
-
       // Raw scores; keys a row may not see become -inf.  Only tiles that
       // cross some row's causal limit (the diagonal and the last tile) need it.
       const int kbase = j * kKTile;
@@ -463,49 +453,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       // No visible key yet (or an unused row): a -inf offset makes every p zero.
       const float neg_ref = (m_ref == -INFINITY) ? -INFINITY : -m_ref;
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P as hi + lo halves, two 16-bit values per 32-bit TMEM column
+      float hi_f[32], lo_f[32];
 #pragma unroll
-      for (int c = 0; c < kKTile; ++c) {
-        const float e = ex2_approx(fmaf(sv[c], p.qscale, neg_ref));
-        sv[c] = e;
-        sum4[c & 3] += e;
+      for (int c = 0; c < kKTile; c += 2) {
+        const float e0 = ex2_approx(fmaf(sv[c], p.qscale, neg_ref));
+        const float e1 = ex2_approx(fmaf(sv[c + 1], p.qscale, neg_ref));
+        sum4[c & 3] += e0;
+        sum4[(c + 1) & 3] += e1;
+        const uint32_t hi = pack_half2<BF16>(e0, e1);
+        const float r0 = half_to_float<BF16>(hi & 0xffffu);
+        const float r1 = half_to_float<BF16>(hi >> 16);
+        hi_f[c / 2] = __uint_as_float(hi);
+        lo_f[c / 2] = __uint_as_float(pack_half2<BF16>(e0 - r0, e1 - r1));
       }
       const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // This warpgroup's previous tile (P buffer b, O accumulator wg) must be
-      // through P.V before P is rewritten or O rescaled.
-      if (j >= 2) {
-        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->pv_done[b], ((j >> 1) - 1) & 1));
+      // O must not change under a running P.V: rescaling waits for P.V(j-1).
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        ok = __all_sync(kFullMask,
+                        mbar_wait_bounded(&bars->s_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tmem_ld32(o_tmem + cc * 32, o);
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(o_tmem + cc * 32, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + lane_base + kTmemO + cc * 32, o);
         }
       }
-      // P as hi + lo halves, rows of 128 B in the 128B-swizzled K-major layout
-      uint8_t* ph = p_hi(b);
-      uint8_t* pl = p_lo(b);
-#pragma unroll
-      for (int ch = 0; ch < kKTile / 8; ++ch) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a = sv[ch * 8 + 2 * i], bb = sv[ch * 8 + 2 * i + 1];
-          hi[i] = pack_half2<BF16>(a, bb);
-          const float ra = half_to_float<BF16>(hi[i] & 0xffffu);
-          const float rb = half_to_float<BF16>(hi[i] >> 16);
-          lo[i] = pack_half2<BF16>(a - ra, bb - rb);
-        }
-        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
+      // P replaces S in this tile's buffer (S has been read into registers)
+      tmem_st32(tmem + lane_base + b * kKTile, hi_f);
+      tmem_st32(tmem + lane_base + b * kKTile + kKTile / 2, lo_f);
+      tmem_wait_st();
       // keys past the last one any row may see: zero their V rows once the tile
       // has landed (they may hold stale or unused-slot data; 0 * NaN is NaN)
       if (j == T - 1 && keys < kbase + kKTile) {
@@ -521,69 +502,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(vs + (rest >> 3) * kHalfBytes + row * 128 + (rest & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_async_smem();
       }
       l = l * alpha + rowsum;
-      fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->p_full[b]);
-      last = j;
       if (__shfl_sync(kFullMask, *abort_flag, 0)) {
         ok = false;
         break;
       }
     }
-    // publish (max, sum) per row; both warpgroups always reach the barrier once
-    float2* xch = reinterpret_cast<float2*>(smem + kOffXch);
-    xch[wg * kQTile + r] = make_float2(m_ref, last >= 0 ? l : 0.f);
-    if (!ok && lane == 0) {
+    // the last P.V (earlier ones finish first: the tensor pipe runs in order)
+    if (ok)
+      ok = __all_sync(kFullMask,
+                      mbar_wait_bounded(&bars->s_free[(T - 1) & 1], ((T - 1) >> 1) & 1));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row_off =
+          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= inv;
+        if (row_valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8)
+            store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
+        }
+      }
+    } else if (lane == 0) {
       *abort_flag = 1;
       report_error(p.err, PA_ERR_TIMEOUT, seq, -2);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-    if (!__shfl_sync(kFullMask, *abort_flag, 0)) {
-      // the epilogue reads both accumulators: wait for each one's last P.V
-      bool ready = true;
-      for (int w = 0; w < 2; ++w) {
-        if (T > w) {
-          const int last_w = w + 2 * ((T - 1 - w) / 2);
-          ready = ready && mbar_wait_bounded(&bars->pv_done[w], (last_w >> 1) & 1);
-        }
-      }
-      ready = __all_sync(kFullMask, ready);
-      if (!ready && lane == 0) {
-        *abort_flag = 1;
-        report_error(p.err, PA_ERR_TIMEOUT, seq, -3);
-      }
-      if (ready) {
-        tc_fence_after();
-        const float2 a = xch[r], c = xch[kQTile + r];
-        const float M = fmaxf(a.x, c.x);
-        const float w0 = a.y > 0.f ? exp2f(a.x - M) : 0.f;
-        const float w1 = c.y > 0.f ? exp2f(c.x - M) : 0.f;
-        const float den = w0 * a.y + w1 * c.y;
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        const uint32_t o0 = tmem + lane_base + kTmemO, o1 = o0 + kHeadDim;
-        const size_t row_off =
-            (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
-        // warpgroup wg writes columns [64 wg, 64 wg + 64)
-  #pragma unroll 1
-        for (int cc = 2 * wg; cc < 2 * wg + 2; ++cc) {
-          float x[32], y[32];
-          tmem_ld32(o0 + cc * 32, x);
-          tmem_ld32(o1 + cc * 32, y);
-  #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float u = w0 > 0.f ? x[i] : 0.f;  // an unused accumulator holds garbage
-            const float v = w1 > 0.f ? y[i] : 0.f;
-            x[i] = (w0 * u + w1 * v) * inv;
-          }
-          if (row_valid) {
-  #pragma unroll
-            for (int i = 0; i < 32; i += 8)
-              store_out<8>(p.out, row_off + cc * 32 + i, x + i, p.out_dtype);
-          }
-        }
-      }
     }
   }
 

@@ -114,3 +114,18 @@ def test_prefill_bad_query_range_is_recorded_and_skipped(B):
                          error_record=rec)
     r = B.pa_error_read(rec)
     assert r[0] == 6 and r[1] >= 1
+
+
+def test_prefill_is_deterministic_across_launches(B):
+    """Repeated launches give bit-identical outputs (a race on a TMEM or shared
+    buffer would show up as run-to-run differences)."""
+    rng = np.random.default_rng(90)
+    lens = rng.integers(200, 1500, size=24)
+    nq = np.minimum(lens, rng.integers(1, 400, size=24))
+    b, q, starts = _case(90, lens, nq, 8, 16, "bf16", poison=False)
+    first = _run(B, b, q, starts)
+    for _ in range(4):
+        again = _run(B, b, q, starts)
+        torch.cuda.synchronize()
+        assert torch.equal(first, again)
+    assert_matches_oracle(first[: starts[3]], _oracle(b, q, starts, seqs=[0, 1, 2]), "determinism")
