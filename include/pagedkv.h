@@ -87,6 +87,15 @@ int pa_error_clear(int32_t* error_record, void* stream);
  * `stream` to finish first, so it reports every kernel enqueued before it. */
 int pa_error_read(const int32_t* error_record, int32_t* host_out, void* stream);
 
+/* Self-test of the bounded wait that every kernel uses on its mbarriers (no
+ * counterpart in the method: a failure-detection check).  One warp waits on a
+ * barrier phase that completes only when `arrive` is nonzero.  Without the
+ * arrival the wait gives up after limit_ns (1 .. 10^9 ns) and records
+ * PA_ERR_TIMEOUT in error_record (device, as above); the kernel then exits
+ * normally and the context stays usable.  Asynchronous on `stream`. */
+int pa_selftest_bounded_wait(int32_t* error_record, int arrive, unsigned long long limit_ns,
+                             void* stream);
+
 /* ---------------------------------------------------------------------------
  * Decode attention through a block table  [P1], [P3b]
  *

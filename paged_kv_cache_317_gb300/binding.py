@@ -42,6 +42,7 @@ SIGNATURES = {
     "pa_status_string": (ctypes.c_char_p, [c_int]),
     "pa_error_clear": (c_int, [c_void_p, c_void_p]),
     "pa_error_read": (c_int, [c_void_p, P_int32, c_void_p]),
+    "pa_selftest_bounded_wait": (c_int, [c_void_p, c_int, ctypes.c_ulonglong, c_void_p]),
     "paged_attn_workspace_size": (c_size_t, [c_int] * 6),
     "paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_float, c_int, c_void_p, c_int,
@@ -150,6 +151,12 @@ def pa_error_read(record: torch.Tensor, stream=None):
     out = (ctypes.c_int32 * 4)()
     _check(load_library().pa_error_read(_ptr(record), out, _stream(stream)), "pa_error_read")
     return list(out)
+
+
+def pa_selftest_bounded_wait(record: torch.Tensor, arrive: bool, limit_ns: int,
+                             stream=None) -> None:
+    _check(load_library().pa_selftest_bounded_wait(_ptr(record), int(arrive), int(limit_ns),
+                                                   _stream(stream)), "pa_selftest_bounded_wait")
 
 
 # ----------------------------------------------------------------- decode

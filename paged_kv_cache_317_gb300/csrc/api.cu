@@ -39,3 +39,32 @@ extern "C" int pa_error_read(const int32_t* error_record, int32_t* host_out, voi
     return PA_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
+
+// Self-test of the bounded wait every kernel uses: one warp waits on an
+// mbarrier phase that completes only if `arrive` is set.  Without the arrival
+// the wait gives up after `limit_ns` and records PA_ERR_TIMEOUT, exactly as a
+// stalled pipeline inside a real kernel would; the kernel then returns normally.
+namespace {
+__global__ void bounded_wait_selftest_kernel(int32_t* err, unsigned long long limit_ns,
+                                             int arrive) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    pagedkv::mbar_init(&bar, 1);
+    pagedkv::fence_mbar_init();
+  }
+  __syncthreads();
+  if (arrive && threadIdx.x == 0) pagedkv::mbar_arrive(&bar);
+  const bool ok = pagedkv::mbar_wait_bounded(&bar, 0, limit_ns);
+  if (!__all_sync(pagedkv::kFullMask, ok) && threadIdx.x == 0)
+    pagedkv::report_error(err, PA_ERR_TIMEOUT, 0, 0);
+}
+}  // namespace
+
+extern "C" int pa_selftest_bounded_wait(int32_t* error_record, int arrive,
+                                        unsigned long long limit_ns, void* stream) {
+  if (!error_record || limit_ns == 0 || limit_ns > pagedkv::kWaitLimitNs)
+    return PA_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      error_record, limit_ns, arrive);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
