@@ -225,7 +225,8 @@ def run_ours(args, rank, world, local_rank):
     pt = 512
     bt = torch.from_numpy(b.block_tables).to(dev)
     sl = torch.from_numpy(b.context_lens).to(dev)
-    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    # longest sequences scheduled first: the host knows the lengths it built the tables from
+    order = torch.from_numpy(np.argsort(-b.context_lens, kind="stable").astype(np.int32)).to(dev)
     out = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, MB, pt), dtype=torch.uint8,
                      device=dev)
@@ -238,7 +239,7 @@ def run_ours(args, rank, world, local_rank):
             ev[0].record(stream)
         B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
                                    out=out, partition_tokens=pt, workspace=ws, error_record=rec,
-                                   phases=1)
+                                   phases=1, seq_order=order)
         if ev is not None:
             ev[1].record(stream)
         B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
@@ -279,7 +280,7 @@ def run_ours(args, rank, world, local_rank):
     # copies run on their own streams with two buffer sets, so step i's copies
     # overlap step i-1's kernels; each step's bytes still cross the link.
     pin = lambda t: t.detach().cpu().pin_memory()
-    host_in = [pin(b.q), pin(b.new_k), pin(b.new_v), pin(bt), pin(sl)]
+    host_in = [pin(b.q), pin(b.new_k), pin(b.new_v), pin(bt), pin(sl), pin(order)]
     dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
     h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     d_out = [torch.empty_like(out) for _ in range(2)]
@@ -299,10 +300,10 @@ def run_ours(args, rank, world, local_rank):
         in_ready[j].record(h2d_stream)
         stream.wait_event(in_ready[j])
         stream.wait_event(out_copied[j])               # d_out[j] has been read back
-        q, k, v, btj, slj = dev_in[j]
+        q, k, v, btj, slj, oj = dev_in[j]
         B.paged_attn_decode_append(q, k, v, b.k_cache, b.v_cache, btj, slj, b.scale,
                                    out=d_out[j], partition_tokens=pt, workspace=ws,
-                                   error_record=rec, stream=stream)
+                                   error_record=rec, seq_order=oj, stream=stream)
         done[j].record(stream)
         d2h_stream.wait_event(done[j])
         with torch.cuda.stream(d2h_stream):
@@ -353,6 +354,7 @@ def run_ours(args, rank, world, local_rank):
                 "context_tokens_per_gpu": int(b.context_lens.sum()),
                 "lengths": "lognormal(median 350, sigma 0.75) clipped to [16, 2048]",
                 "pool_blocks": b.num_blocks, "partition_tokens": pt, "out_dtype": "bf16",
+                "schedule": "sequences longest first (seq_order)",
                 "l2": "inputs larger than L2 (2.4 GB of K/V read per step); no flush",
                 "parallelism": f"replicas x{world} (independent batches, no collective)",
             },

@@ -142,6 +142,13 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *   heads_per_cta  heads handled by one thread block (must divide num_heads, <= 8)
  *   stages         shared-memory pipeline depth, 2..8
  *   phases         0 or 3: both passes; 1: partition pass only; 2: merge pass only.
+ *   seq_order      NULL, or device int32 [num_seqs]: a permutation of 0..num_seqs-1
+ *                  giving the order in which sequences are scheduled (results are
+ *                  identical, bit for bit).  Longest first shortens the ragged tail
+ *                  of the launch; the host knows the lengths when it builds the
+ *                  tables.  An entry outside [0, num_seqs) is recorded as
+ *                  PA_ERR_BAD_SEQ_LEN (index = position, value = entry) and skipped;
+ *                  a repeated entry leaves some sequence's output unwritten.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -154,6 +161,7 @@ typedef struct pa_decode_opts {
   int heads_per_cta;
   int stages;
   int phases;
+  const int32_t* seq_order;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,

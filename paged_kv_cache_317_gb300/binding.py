@@ -33,7 +33,8 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 
 class pa_decode_opts(ctypes.Structure):
-    _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int)]
+    _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
+                ("seq_order", c_void_p)]
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
@@ -171,8 +172,10 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
                       partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                       error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
-                      stages: int = 0, phases: int = 0, stream=None) -> torch.Tensor:
-    """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N]."""
+                      stages: int = 0, phases: int = 0, seq_order: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
+    seq_order: optional int32 [N] scheduling permutation on the device."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -187,7 +190,10 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    opts = pa_decode_opts(heads_per_cta, stages, phases)
+    if seq_order is not None:
+        _need(seq_order, "seq_order", torch.int32)
+    opts = pa_decode_opts(heads_per_cta, stages, phases,
+                          None if seq_order is None else seq_order.data_ptr())
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -202,7 +208,9 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
                              partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                              error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
-                             stages: int = 0, phases: int = 0, stream=None) -> torch.Tensor:
+                             stages: int = 0, phases: int = 0,
+                             seq_order: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
     N, H, D = q.shape
@@ -220,7 +228,10 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    opts = pa_decode_opts(heads_per_cta, stages, phases)
+    if seq_order is not None:
+        _need(seq_order, "seq_order", torch.int32)
+    opts = pa_decode_opts(heads_per_cta, stages, phases,
+                          None if seq_order is None else seq_order.data_ptr())
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),

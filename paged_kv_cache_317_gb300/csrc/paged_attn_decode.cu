@@ -50,6 +50,8 @@ struct DecodeParams {
   const void* v_cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
+  const int32_t* seq_order;  // optional scheduling permutation of the sequences
+  int num_seqs;
   const void* new_k;   // fused append: [N][H][D] rows of each sequence's last token, or null
   const void* new_v;
   void* k_out;         // fused append: the caches, written at each last token's slot
@@ -114,8 +116,17 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
   const int S = p.stages;
-  const int hg = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
+  const int hg = blockIdx.x, part = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int seq = blockIdx.z;
+  if (p.seq_order != nullptr) {
+    seq = __ldg(p.seq_order + blockIdx.z);
+    if (static_cast<unsigned>(seq) >= static_cast<unsigned>(p.num_seqs)) {
+      if (threadIdx.x == 0 && hg == 0 && part == 0)
+        report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.z, seq);
+      return;
+    }
+  }
 
   const int L = clamp_len(p, seq, threadIdx.x == 0 && hg == 0 && part == 0);
   const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
@@ -524,6 +535,8 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
 
   DecodeParams p{};
   p.q = q;
+  p.seq_order = opts ? opts->seq_order : nullptr;
+  p.num_seqs = num_seqs;
   p.new_k = new_k;
   p.new_v = new_v;
   p.k_out = k_out;

@@ -172,3 +172,32 @@ def test_bad_seq_len_is_recorded_and_clamped(B):
     r = B.pa_error_read(rec)
     assert r[0] == 6 and r[1] == 2
     assert not out[0].any()
+
+
+def test_seq_order_changes_nothing_but_the_schedule(B):
+    b = random_decode_batch(16, [5, 900, 33, 1500, 64, 700, 2, 1100], 8, 128, 16, dtype="bf16",
+                            device="cuda", with_append=True)
+    bt, sl = device_tables(b)
+    order = torch.from_numpy(np.argsort(-b.context_lens, kind="stable").astype(np.int32)).cuda()
+    k1, v1, k2, v2 = b.k_cache.clone(), b.v_cache.clone(), b.k_cache.clone(), b.v_cache.clone()
+    plain = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, k1, v1, bt, sl, b.scale)
+    ordered = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, k2, v2, bt, sl, b.scale,
+                                         seq_order=order)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, ordered)
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert_matches_oracle(ordered, oracle_decode(b), "ordered")
+
+
+def test_bad_seq_order_entry_is_recorded_and_skipped(B):
+    b = random_decode_batch(17, [40, 20, 60], 4, 64, 16, dtype="f16", device="cuda", poison=False)
+    bt, sl = device_tables(b)
+    order = torch.tensor([2, 7, 0], dtype=torch.int32, device="cuda")
+    rec = B.new_error_record()
+    out = torch.zeros(3, 4, 64, device="cuda")
+    B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out, seq_order=order,
+                        error_record=rec)
+    assert B.pa_error_read(rec) == [6, 1, 1, 7]
+    ref = oracle_decode(b, [0, 2])
+    assert_matches_oracle(out[[0, 2]], ref, "valid entries")
+    assert not out[1].any()                 # sequence 1 was not scheduled
