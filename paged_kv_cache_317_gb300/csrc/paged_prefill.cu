@@ -53,7 +53,7 @@ constexpr int kHeadDim = 128;
 constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
 constexpr int kWarpK = 4, kWarpMma = 5, kWarpV = 6;
 constexpr int kKStages = 2;                       // K ring depth
-constexpr int kVStages = 2;                       // V ring depth
+constexpr int kVStages = 3;                       // V ring depth: V(j+3) loads while P.V(j+1..j+2) run
 constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B (one 64-wide half)
 constexpr int kQBytes = kQTile * kHeadDim * 2;    // 32 KB (two 16 KB halves)
 constexpr int kTileBytes = 2 * kHalfBytes;        // one K or V tile: 16 KB
@@ -61,7 +61,11 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, then slack to align to 1 KB
+// Two blocks must fit an SM (228 KB, less 1 KB reserved per block): 768 bytes are
+// left for aligning the dynamic shared-memory base to 1 KB; the kernel checks it.
+constexpr int kAlignSlack = 768;
+constexpr int kSmemBytes = kOffBar + 256 + kAlignSlack;
+static_assert(kSmemBytes <= 116 * 1024 - 1024, "two blocks per SM");
 // TMEM: two S/P buffers of 64 columns (S in fp32; after the softmax, P hi in the
 // first 32 columns and P lo in the next 32, two 16-bit values per column) and O.
 constexpr uint32_t kTmemCols = 256;
@@ -253,8 +257,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int T = (keys + kKTile - 1) / kKTile;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  if (pad > kAlignSlack) {  // never seen: the base is 1 KB aligned in practice
+    if (threadIdx.x == 0) report_error(p.err, PA_ERR_UNSUPPORTED, seq, static_cast<int>(pad));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   uint8_t* Qs = smem + kOffQ;
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bars->abort;
