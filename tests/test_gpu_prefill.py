@@ -129,3 +129,15 @@ def test_prefill_is_deterministic_across_launches(B):
         torch.cuda.synchronize()
         assert torch.equal(first, again)
     assert_matches_oracle(first[: starts[3]], _oracle(b, q, starts, seqs=[0, 1, 2]), "determinism")
+
+
+def test_prefill_long_context_many_tiles(B):
+    """16K-token contexts: every ring and barrier phase wraps around many times."""
+    lens = [16384, 12001]
+    nq = [200, 77]
+    b, q, starts = _case(95, lens, nq, 4, 32, "bf16", poison=True)
+    rec = B.new_error_record()
+    out = _run(B, b, q, starts, rec=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert_matches_oracle(out, _oracle(b, q, starts), "long prefill")
