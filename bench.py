@@ -549,9 +549,10 @@ def run_workload(args, rank, world, local_rank):
             if len(pairs):
                 B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
             q, k, v = tokens_all[s_]
+            order = torch.from_numpy(np.argsort(-lens, kind="stable").astype(np.int32)).to(dev)
             B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
                                        torch.from_numpy(lens).to(dev), plan.scale, out=out,
-                                       workspace=ws, error_record=rec)
+                                       workspace=ws, error_record=rec, seq_order=order)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
