@@ -61,6 +61,7 @@ extern "C" int block_copy(void* const* k_caches, void* const* v_caches, int num_
                           const int64_t* pairs, int num_pairs, int num_heads, int head_dim,
                           int block_size, int num_blocks, int dtype, int32_t* error_record,
                           void* stream) {
+  NvtxRange range("block_copy");
   if (num_layers <= 0 || num_layers > kMaxLayers || num_pairs < 0 || num_heads <= 0 ||
       head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;

@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 
 #include "pagedkv.h"
@@ -177,5 +179,14 @@ __device__ __forceinline__ void store_out(void* out, size_t elem, const float* v
 
 // Host-side helpers -------------------------------------------------------
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Named NVTX range over a C-ABI call, so the library's calls show up in
+// Nsight timelines; a push/pop costs a few ns when no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 }  // namespace pagedkv

@@ -51,6 +51,7 @@ extern "C" int kv_cache_append(const void* k, const void* v, const int64_t* slot
                                int num_tokens, void* k_cache, void* v_cache, int num_heads,
                                int head_dim, int block_size, int num_blocks, int dtype,
                                int32_t* error_record, void* stream) {
+  NvtxRange range("kv_cache_append");
   if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;

@@ -497,6 +497,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
                   void* out, int out_dtype, int partition_tokens, void* workspace,
                   size_t workspace_bytes, int32_t* error_record, void* stream,
                   const pa_decode_opts* opts) {
+  NvtxRange range(new_k ? "paged_attn_decode_append" : "paged_attn_decode");
   if (num_seqs < 0 || num_heads <= 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
       num_blocks <= 0)
     return PA_ERR_INVALID_ARG;

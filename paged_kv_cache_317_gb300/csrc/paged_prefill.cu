@@ -624,6 +624,7 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
                                   int num_seqs, int num_heads, int head_dim, int block_size,
                                   int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                   void* out, int out_dtype, int32_t* error_record, void* stream) {
+  NvtxRange range("paged_attn_prefill");
   if (num_seqs < 0 || total_queries < 0 || max_query_len < 0 || num_heads <= 0 ||
       block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
