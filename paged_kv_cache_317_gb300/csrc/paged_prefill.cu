@@ -7,30 +7,30 @@
 // physical scatter").  With >1 query per head the work is a dense contraction,
 // so it runs on tensor cores:
 //
-//  * block = (128-query tile, head, sequence); 11 warps: two softmax
-//    warpgroups (one query row per thread = one TMEM lane) taking alternate key
-//    tiles, a K producer warp, an MMA warp and a V producer warp.
-//  * Q tile: one 3-D TMA load per 64-wide half of head_dim (128B swizzle).
-//    K/V: per 16-key chunk the producer follows the block table (32 entries
-//    fetched at a time) and issues 2-D TMA loads of the rows (128B swizzle) into
-//    a 4-stage K ring and a 3-stage V ring of 64-key tiles, each fed by its own
-//    warp; a K tile is released as soon as its S MMA completes, a V tile when
-//    its P.V completes.
-//  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16) into one of four TMEM S
-//    buffers, issued three tiles ahead of P.V so that a tile's S never waits in
-//    the in-order tensor pipe behind the previous tiles' P.V.
-//  * Softmax warps: tcgen05.ld their S row, causal/length mask, online softmax
-//    in log2 units; P is written to shared memory as bf16/fp16 hi + lo parts
-//    (hi = round(p), lo = round(p - hi)), so P.V carries ~16 more mantissa bits
-//    than a single half-precision P and stays within the fp32-accumulation error
-//    bound.  Each warpgroup has its own P buffer, O accumulator in TMEM and
-//    running (max, sum), so tile j only waits for P.V(j-2).  The exponentials
-//    use a per-row reference max that moves only when the running max passes it
-//    by 2^8; only then is that warpgroup's O rescaled.  The epilogue merges the
-//    two accumulators by log-sum-exp.
-//  * O += P V: 4 + 4 tcgen05.mma (M=128, N=128, K=16 keys; V as an MN-major
-//    operand) accumulating in TMEM; each warpgroup's last P.V completion
-//    releases the epilogue, which writes the merged rows of out.
+//  * block = (128-query tile, head, sequence); 7 warps: one softmax warpgroup
+//    (one query row per thread = one TMEM lane), a K producer, an MMA issuer
+//    and a V producer.  ~113 KB of shared memory and 256 TMEM columns, so two
+//    blocks share an SM and cover each other's start-up and tail.
+//  * Q tile: two 3-D TMA loads (one per 64-wide half of head_dim, 128B
+//    swizzle), issued before the block-wide set-up barrier.  K/V: per 16-key
+//    chunk the producers follow the block table (32 entries at a time) and
+//    issue 2-D TMA loads of the rows (128B swizzle) into a 2-stage K ring and a
+//    3-stage V ring of 64-key tiles; a K tile is released when its S MMA
+//    completes, a V tile when its P.V completes.
+//  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16, fp32 accumulate) into one of
+//    two 64-column TMEM buffers.  Buffer j & 1 is reused for S(j+2) only after
+//    P.V(j), which reads the P stored there, has completed.
+//  * Softmax: tcgen05.ld of the S row, causal/length mask only on tiles that
+//    cross a row's limit, exponentials by ex2.approx against a per-row
+//    reference max that moves only when the running max passes it by 2^8 (O is
+//    rescaled in TMEM only then).  P is stored back over its S as two 16-bit
+//    parts per key, hi = round(p) and lo = round(p - hi): a single bf16 P would
+//    carry up to 2^-8 relative error per weight, more than the 2e-3 bound
+//    allows on rows dominated by a few keys.
+//  * O += P V: 4 + 4 tcgen05.mma (hi and lo; M=128, N=128, K=16 keys) with A
+//    read from TMEM and V as an MN-major shared-memory operand, accumulating
+//    in TMEM.  The commit of buffer b's P.V is also the completion signal the
+//    softmax waits on before rescaling O or reading it in the epilogue.
 //  * Every mbarrier wait is bounded (one second); on a timeout the block
 //    records PA_ERR_TIMEOUT, waits (bounded) for its copies and MMAs, frees its
 //    TMEM and returns.  Nothing traps.
@@ -65,7 +65,7 @@ constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 // left for aligning the dynamic shared-memory base to 1 KB; the kernel checks it.
 constexpr int kAlignSlack = 768;
 constexpr int kSmemBytes = kOffBar + 256 + kAlignSlack;
-static_assert(kSmemBytes <= 116 * 1024 - 1024, "two blocks per SM");
+static_assert(kSmemBytes <= 228 * 1024 / 2 - 1024, "two blocks per SM");
 // TMEM: two S/P buffers of 64 columns (S in fp32; after the softmax, P hi in the
 // first 32 columns and P lo in the next 32, two 16-bit values per column) and O.
 constexpr uint32_t kTmemCols = 256;
@@ -192,6 +192,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
                : "memory");
 }
 
+// Two fp32 lanes at once (sm_100+ packed f32x2 arithmetic, round to nearest:
+// the same results as two scalar operations).
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float s, float c) {
+  asm("{\n\t.reg .b64 x, s, c, d;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %5};\n\tfma.rn.f32x2 d, x, s, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+__device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 x, {%2, %3};\n\t"
+      "add.rn.f32x2 d, a, x;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+
 // 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32;
 // relative error ~2^-22, 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -269,8 +285,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto k_tile = [&](int s) { return smem + kOffK + s * kTileBytes; };
   auto v_tile = [&](int s) { return smem + kOffV + s * kTileBytes; };
 
+  // Started before the block-wide barrier so that their latency overlaps the
+  // set-up: the Q tile load (its barrier initialised by the issuing thread)
+  // and the producers' first block-table entries.
+  int blk_first = 0;  // producers: physical block of 16-key chunk `lane`
+  if (warp == kWarpK || warp == kWarpV) {
+    if (lane * 16 < keys)
+      blk_first = __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks +
+                        lane * 16 / p.block_size);
+    if (warp == kWarpK && lane == 0) {
+      mbar_init(&bars->q_full, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
+      tma_load_3d(Qs, &tm_q, 0, h, q_begin + q0, &bars->q_full);
+      tma_load_3d(Qs + kQBytes / 2, &tm_q, 64, h, q_begin + q0, &bars->q_full);
+    }
+  }
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -307,11 +338,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool is_v = (warp == kWarpV);
     const int stages = is_v ? kVStages : kKStages;
     const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
-    if (!is_v && lane == 0) {
-      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-      tma_load_3d(Qs, &tm_q, 0, h, q_begin + q0, &bars->q_full);
-      tma_load_3d(Qs + kQBytes / 2, &tm_q, 64, h, q_begin + q0, &bars->q_full);
-    }
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     int blk = 0;
     for (int j = 0; j < T; ++j) {
@@ -320,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int key0 = (j * 4 + lane) * 16;
         blk = 0;
         if (key0 < keys) {
-          blk = __ldg(table + key0 / p.block_size);
+          blk = j == 0 ? blk_first : __ldg(table + key0 / p.block_size);
           if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
             if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
             blk = 0;
@@ -465,10 +491,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       float hi_f[32], lo_f[32];
 #pragma unroll
       for (int c = 0; c < kKTile; c += 2) {
-        const float e0 = ex2_approx(fmaf(sv[c], p.qscale, neg_ref));
-        const float e1 = ex2_approx(fmaf(sv[c + 1], p.qscale, neg_ref));
-        sum4[c & 3] += e0;
-        sum4[(c + 1) & 3] += e1;
+        float x0, x1;
+        fma2(x0, x1, sv[c], sv[c + 1], p.qscale, neg_ref);
+        const float e0 = ex2_approx(x0);
+        const float e1 = ex2_approx(x1);
+        add2(sum4[c & 2], sum4[(c & 2) + 1], e0, e1);
         const uint32_t hi = pack_half2<BF16>(e0, e1);
         const float r0 = half_to_float<BF16>(hi & 0xffffu);
         const float r1 = half_to_float<BF16>(hi >> 16);
