@@ -201,3 +201,41 @@ def test_bad_seq_order_entry_is_recorded_and_skipped(B):
     ref = oracle_decode(b, [0, 2])
     assert_matches_oracle(out[[0, 2]], ref, "valid entries")
     assert not out[1].any()                 # sequence 1 was not scheduled
+
+
+def test_shared_prefix_equals_private_copy_bit_exact(B):
+    """A sequence whose leading blocks are shared with another sequence decodes
+    bit-identically to the same sequence holding private copies of those blocks
+    (PagedAttention, "Sharing a prefix without copying it": sharing changes only
+    the table, never what attention reads)."""
+    lens = [700, 900, 40]
+    bs = 16
+    b = random_decode_batch(18, lens, 8, 128, bs, dtype="bf16", device="cuda", pool_factor=3.0,
+                            poison=False)
+    bt = b.block_tables.copy()
+    n = lens[0] // bs                          # full blocks of sequence 0
+    shared = bt.copy()
+    shared[1, :n] = bt[0, :n]
+    used = {int(x) for x in bt[bt >= 0]}
+    free = [x for x in range(b.num_blocks) if x not in used][:n]
+    assert len(free) == n
+    pairs = torch.tensor([[int(bt[0, j]), free[j]] for j in range(n)], dtype=torch.int64,
+                         device="cuda")
+    B.block_copy([b.k_cache], [b.v_cache], pairs)
+    private = bt.copy()
+    private[1, :n] = free
+    sl = torch.from_numpy(b.context_lens).cuda()
+    for pt in (0, 64):
+        out_s = B.paged_attn_decode(b.q, b.k_cache, b.v_cache, torch.from_numpy(shared).cuda(), sl,
+                                    b.scale, partition_tokens=pt)
+        out_p = B.paged_attn_decode(b.q, b.k_cache, b.v_cache, torch.from_numpy(private).cuda(),
+                                    sl, b.scale, partition_tokens=pt)
+        torch.cuda.synchronize()
+        assert torch.equal(out_s, out_p)
+    kc, dt = storage(b.k_cache)
+    vc, _ = storage(b.v_cache)
+    qs, _ = storage(b.q)
+    k = OA.to_float64(OA.gather_sequence(kc, shared[1], lens[1], bs), dt)
+    v = OA.to_float64(OA.gather_sequence(vc, shared[1], lens[1], bs), dt)
+    ref = OA.attention(OA.to_float64(qs[1], dt), k, v, b.scale)
+    assert_matches_oracle(out_s[1], ref, "shared prefix")

@@ -141,3 +141,31 @@ def test_prefill_long_context_many_tiles(B):
     torch.cuda.synchronize()
     assert B.pa_error_read(rec) == [0, 0, 0, 0]
     assert_matches_oracle(out, _oracle(b, q, starts), "long prefill")
+
+
+def test_prefill_sequences_without_queries_are_skipped(B):
+    """Sequences with no queries in the launch (query_start[i] == query_start[i+1])
+    write nothing; the others are unaffected."""
+    lens = [300, 120, 0, 900]
+    nq = [40, 0, 0, 130]
+    b, q, starts = _case(97, lens, nq, 4, 16, "bf16")
+    rec = B.new_error_record()
+    out = _run(B, b, q, starts, rec=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert_matches_oracle(out, _oracle(b, q, starts, seqs=[0, 3]), "skipped sequences")
+
+
+def test_prefill_bad_block_entry_is_recorded_and_clamped(B):
+    b, q, starts = _case(98, [200, 150], [64, 50], 2, 16, "bf16", poison=False)
+    bt = torch.from_numpy(b.block_tables).cuda()
+    bt[1, 2] = b.num_blocks + 9
+    rec = B.new_error_record()
+    out = B.paged_attn_prefill(q, torch.from_numpy(starts).cuda(), 64, b.k_cache, b.v_cache, bt,
+                               torch.from_numpy(b.context_lens).cuda(), b.scale,
+                               error_record=rec)
+    torch.cuda.synchronize()
+    r = B.pa_error_read(rec)
+    assert r[0] == 4 and r[1] >= 1 and r[2] == 1 and r[3] == b.num_blocks + 9
+    assert torch.isfinite(out).all()
+    assert_matches_oracle(out[: starts[1]], _oracle(b, q, starts, seqs=[0]), "unaffected sequence")
