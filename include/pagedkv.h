@@ -274,7 +274,9 @@ int kv_cache_append(const void* k, const void* v, const int64_t* slot_mapping, i
  * distinct and no destination may be a source in the same call (the allocator
  * guarantees this: a destination is always a block just taken off the free
  * list); otherwise the result is undefined.  A pair with a block outside
- * [0, num_blocks) is recorded as PA_ERR_BAD_BLOCK and skipped.
+ * [0, num_blocks) is recorded as PA_ERR_BAD_BLOCK and skipped, except the
+ * padding pair (-1, -1), which is skipped silently: a launch captured in a CUDA
+ * graph with room for num_pairs copies can then replay steps that need fewer.
  *   k_caches, v_caches  HOST arrays of num_layers device pointers (1..128 layers),
  *                 each cache laid out as above, 16-byte aligned
  *   pairs         device int64 [num_pairs][2]

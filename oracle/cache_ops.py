@@ -34,8 +34,11 @@ def kv_append(k_cache: np.ndarray, v_cache: np.ndarray, k: np.ndarray, v: np.nda
 
 def block_copy(k_caches, v_caches, pairs) -> None:
     """In place, over every layer's pair of caches.  ``pairs`` is ``[n, 2]`` of
-    (source block, destination block), applied in order."""
+    (source block, destination block), applied in order; the pair (-1, -1) is
+    padding and copies nothing (a library convention, not from the sources)."""
     for src, dst in np.asarray(pairs).reshape(-1, 2):
+        if src == -1 and dst == -1:
+            continue
         for kc, vc in zip(k_caches, v_caches):
             kc[int(dst)] = kc[int(src)].copy()
             vc[int(dst)] = vc[int(src)].copy()

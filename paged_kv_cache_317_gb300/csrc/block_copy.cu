@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kThreads)
   const int layer = blockIdx.z >> 1;
   const long long src = __ldg(pairs + 2 * pair);
   const long long dst = __ldg(pairs + 2 * pair + 1);
+  if (src == -1 && dst == -1) return;  // padding
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
     if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
       report_error(err, PA_ERR_BAD_BLOCK, pair, (src < 0 || src >= num_blocks) ? src : dst);

@@ -83,3 +83,14 @@ def test_block_copy_bad_pair_is_recorded_and_skipped(B):
     assert B.pa_error_read(rec) == [4, 1, 1, 99]
     OC.block_copy([ek], [ev], [[1, 2], [4, 5]])
     assert np.array_equal(bits(kc), ek) and np.array_equal(bits(vc), ev)
+
+
+def test_block_copy_padding_pairs_are_skipped_silently(B):
+    kc, vc = _pool(21, 8, 4, 16, 64, torch.bfloat16)
+    pairs = np.array([[-1, -1], [1, 2], [-1, -1], [4, 5], [-1, -1]], dtype=np.int64)
+    ek, ev = bits(kc), bits(vc)
+    rec = B.new_error_record()
+    B.block_copy([kc], [vc], torch.from_numpy(pairs).cuda(), error_record=rec)
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    OC.block_copy([ek], [ev], pairs)
+    assert np.array_equal(bits(kc), ek) and np.array_equal(bits(vc), ev)

@@ -54,3 +54,15 @@ def test_block_copy_duplicates_exactly_the_listed_blocks():
             assert np.array_equal(vlayers[L][dst], before_v[L][src])
         for untouched in (1, 2, 4):
             assert np.array_equal(layers[L][untouched], before_k[L][untouched])
+
+
+def test_block_copy_padding_pairs_copy_nothing():
+    rng = np.random.default_rng(2)
+    kc = rng.integers(0, 1000, size=(4, 2, 4, 3)).astype(np.uint16)
+    vc = kc + 1
+    before_k, before_v = kc.copy(), vc.copy()
+    C.block_copy([kc], [vc], np.array([[-1, -1], [2, 0], [-1, -1]]))
+    assert np.array_equal(kc[0], before_k[2]) and np.array_equal(vc[0], before_v[2])
+    for untouched in (1, 2, 3):
+        assert np.array_equal(kc[untouched], before_k[untouched])
+        assert np.array_equal(vc[untouched], before_v[untouched])
