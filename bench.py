@@ -225,8 +225,10 @@ def run_ours(args, rank, world, local_rank):
     pt = 512
     bt = torch.from_numpy(b.block_tables).to(dev)
     sl = torch.from_numpy(b.context_lens).to(dev)
-    # longest sequences scheduled first: the host knows the lengths it built the tables from
-    order = torch.from_numpy(np.argsort(-b.context_lens, kind="stable").astype(np.int32)).to(dev)
+    # The host knows the lengths it built the tables from: it lists the (sequence,
+    # partition) pairs that hold tokens, longest sequences first.
+    order = torch.from_numpy(B.partition_work_items(
+        b.context_lens, pt, MB, bs, order=np.argsort(-b.context_lens, kind="stable"))).to(dev)
     out = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, MB, pt), dtype=torch.uint8,
                      device=dev)
@@ -239,7 +241,7 @@ def run_ours(args, rank, world, local_rank):
             ev[0].record(stream)
         B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
                                    out=out, partition_tokens=pt, workspace=ws, error_record=rec,
-                                   phases=1, seq_order=order)
+                                   phases=1, work_items=order)
         if ev is not None:
             ev[1].record(stream)
         B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
@@ -303,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
         q, k, v, btj, slj, oj = dev_in[j]
         B.paged_attn_decode_append(q, k, v, b.k_cache, b.v_cache, btj, slj, b.scale,
                                    out=d_out[j], partition_tokens=pt, workspace=ws,
-                                   error_record=rec, seq_order=oj, stream=stream)
+                                   error_record=rec, work_items=oj, stream=stream)
         done[j].record(stream)
         d2h_stream.wait_event(done[j])
         with torch.cuda.stream(d2h_stream):
@@ -354,7 +356,8 @@ def run_ours(args, rank, world, local_rank):
                 "context_tokens_per_gpu": int(b.context_lens.sum()),
                 "lengths": "lognormal(median 350, sigma 0.75) clipped to [16, 2048]",
                 "pool_blocks": b.num_blocks, "partition_tokens": pt, "out_dtype": "bf16",
-                "schedule": "sequences longest first (seq_order)",
+                "schedule": "(sequence, partition) work items holding tokens, longest "
+                            "sequences first (work_items)",
                 "l2": "inputs larger than L2 (2.4 GB of K/V read per step); no flush",
                 "parallelism": f"replicas x{world} (independent batches, no collective)",
             },
@@ -549,10 +552,11 @@ def run_workload(args, rank, world, local_rank):
             if len(pairs):
                 B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
             q, k, v = tokens_all[s_]
-            order = torch.from_numpy(np.argsort(-lens, kind="stable").astype(np.int32)).to(dev)
+            items = torch.from_numpy(B.partition_work_items(lens, 0, max_blocks, plan.block_size))
             B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
                                        torch.from_numpy(lens).to(dev), plan.scale, out=out,
-                                       workspace=ws, error_record=rec, seq_order=order)
+                                       workspace=ws, error_record=rec,
+                                       work_items=items.to(dev))
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()

@@ -149,6 +149,14 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  tables.  An entry outside [0, num_seqs) is recorded as
  *                  PA_ERR_BAD_SEQ_LEN (index = position, value = entry) and skipped;
  *                  a repeated entry leaves some sequence's output unwritten.
+ *   work_items     NULL, or device int32 [num_work_items]: the (sequence, partition)
+ *                  pairs to run, item = i * P + p (P as below), in the order they
+ *                  should be scheduled; seq_order is then ignored.  Listing only the
+ *                  partitions that hold tokens (p < ceil(L_i / partition_tokens))
+ *                  avoids launching blocks that would exit at once; every such
+ *                  pair must appear exactly once for `out` to be complete.  An
+ *                  item outside [0, num_seqs * P) is recorded as PA_ERR_BAD_SEQ_LEN
+ *                  (index = position, value = item) and skipped.  At most 65535.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -162,6 +170,8 @@ typedef struct pa_decode_opts {
   int stages;
   int phases;
   const int32_t* seq_order;
+  const int32_t* work_items;
+  int num_work_items;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,

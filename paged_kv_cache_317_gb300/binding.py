@@ -34,7 +34,32 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
-                ("seq_order", c_void_p)]
+                ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int)]
+
+
+def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items):
+    if seq_order is not None:
+        _need(seq_order, "seq_order", torch.int32)
+    if work_items is not None:
+        _need(work_items, "work_items", torch.int32)
+    return pa_decode_opts(heads_per_cta, stages, phases,
+                          None if seq_order is None else seq_order.data_ptr(),
+                          None if work_items is None else work_items.data_ptr(),
+                          0 if work_items is None else int(work_items.numel()))
+
+
+def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: int,
+                         block_size: int, order=None) -> "np.ndarray":
+    """Host helper: the (sequence, partition) items that hold tokens, item =
+    i * P + p, in the given sequence order (default: longest first)."""
+    import numpy as np
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    pt = partition_tokens if partition_tokens > 0 else 512
+    P = max(1, -(-max_blocks_per_seq * block_size // pt))
+    if order is None:
+        order = np.argsort(-lens, kind="stable")
+    items = [i * P + p for i in order for p in range(max(1, -(-int(lens[i]) // pt)))]
+    return np.asarray(items, dtype=np.int32)
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
@@ -173,9 +198,10 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                       error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
                       stages: int = 0, phases: int = 0, seq_order: Optional[torch.Tensor] = None,
-                      stream=None) -> torch.Tensor:
+                      work_items: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
-    seq_order: optional int32 [N] scheduling permutation on the device."""
+    seq_order: optional int32 [N] scheduling permutation on the device; work_items:
+    optional int32 list of (sequence * P + partition) on the device."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -190,10 +216,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if seq_order is not None:
-        _need(seq_order, "seq_order", torch.int32)
-    opts = pa_decode_opts(heads_per_cta, stages, phases,
-                          None if seq_order is None else seq_order.data_ptr())
+    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items)
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -210,6 +233,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
                              stages: int = 0, phases: int = 0,
                              seq_order: Optional[torch.Tensor] = None,
+                             work_items: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
@@ -228,10 +252,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if seq_order is not None:
-        _need(seq_order, "seq_order", torch.int32)
-    opts = pa_decode_opts(heads_per_cta, stages, phases,
-                          None if seq_order is None else seq_order.data_ptr())
+    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items)
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),

@@ -51,7 +51,9 @@ struct DecodeParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* seq_order;  // optional scheduling permutation of the sequences
+  const int32_t* work_items; // optional (sequence * P + partition) list, one per block row
   int num_seqs;
+  int num_work_items;
   const void* new_k;   // fused append: [N][H][D] rows of each sequence's last token, or null
   const void* new_v;
   void* k_out;         // fused append: the caches, written at each last token's slot
@@ -116,10 +118,18 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
   const int S = p.stages;
-  const int hg = blockIdx.x, part = blockIdx.y;
+  const int hg = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int seq = blockIdx.z;
-  if (p.seq_order != nullptr) {
+  int part = blockIdx.y, seq = blockIdx.z;
+  if (p.work_items != nullptr) {
+    const int item = __ldg(p.work_items + blockIdx.y);
+    if (item < 0 || item / p.num_partitions >= p.num_seqs) {
+      if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, item);
+      return;
+    }
+    seq = item / p.num_partitions;
+    part = item % p.num_partitions;
+  } else if (p.seq_order != nullptr) {
     seq = __ldg(p.seq_order + blockIdx.z);
     if (static_cast<unsigned>(seq) >= static_cast<unsigned>(p.num_seqs)) {
       if (threadIdx.x == 0 && hg == 0 && part == 0)
@@ -449,9 +459,12 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem, cudaStr
   if (phases & 1) {
     if (ensure_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(p.num_heads / p.heads_per_cta, p.num_partitions, num_seqs);
+    if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
     dim3 block((p.heads_per_cta + 1) * 32);
-    paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (grid.y > 0) {
+      paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
+      if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
   }
   if ((phases & 2) && p.num_partitions > 1) {
     MergeParams mp{p.seq_lens, p.ws_acc, p.ws_ml, p.out, num_seqs, p.num_heads,
@@ -537,6 +550,10 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   DecodeParams p{};
   p.q = q;
   p.seq_order = opts ? opts->seq_order : nullptr;
+  p.work_items = opts ? opts->work_items : nullptr;
+  p.num_work_items = p.work_items ? opts->num_work_items : 0;
+  if (p.work_items && (p.num_work_items < 0 || p.num_work_items > 65535))
+    return PA_ERR_INVALID_ARG;
   p.num_seqs = num_seqs;
   p.new_k = new_k;
   p.new_v = new_v;

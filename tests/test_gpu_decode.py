@@ -239,3 +239,44 @@ def test_shared_prefix_equals_private_copy_bit_exact(B):
     v = OA.to_float64(OA.gather_sequence(vc, shared[1], lens[1], bs), dt)
     ref = OA.attention(OA.to_float64(qs[1], dt), k, v, b.scale)
     assert_matches_oracle(out_s[1], ref, "shared prefix")
+
+
+def test_work_items_change_nothing_but_the_schedule(B):
+    """Running only the (sequence, partition) items that hold tokens, in any order,
+    gives the same bits as the full grid; fused append included."""
+    from paged_kv_cache_317_gb300.binding import partition_work_items
+    lens = [5, 900, 2048, 1500, 64, 513, 2, 1100, 1, 512]
+    b = random_decode_batch(22, lens, 8, 128, 16, dtype="bf16", device="cuda", with_append=True)
+    bt, sl = device_tables(b)
+    MB = b.max_blocks_per_seq
+    for pt in (0, 256):
+        k1, v1 = b.k_cache.clone(), b.v_cache.clone()
+        plain = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, k1, v1, bt, sl, b.scale,
+                                           partition_tokens=pt)
+        items = partition_work_items(b.context_lens, pt, MB, 16)
+        for perm in (None, np.random.default_rng(pt).permutation(len(items))):
+            it = items if perm is None else items[perm]
+            k2, v2 = b.k_cache.clone(), b.v_cache.clone()
+            got = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, k2, v2, bt, sl, b.scale,
+                                             partition_tokens=pt,
+                                             work_items=torch.from_numpy(it).cuda())
+            torch.cuda.synchronize()
+            assert torch.equal(plain, got)
+            assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert_matches_oracle(plain, oracle_decode(b), "work items")
+
+
+def test_bad_work_item_is_recorded_and_skipped(B):
+    from paged_kv_cache_317_gb300.binding import partition_work_items
+    b = random_decode_batch(23, [40, 20, 60], 4, 64, 16, dtype="f16", device="cuda", poison=False)
+    bt, sl = device_tables(b)
+    items = partition_work_items(b.context_lens, 0, b.max_blocks_per_seq, 16, order=[0, 1, 2])
+    P = 1
+    bad = np.array([items[0], 3 * P + 5, items[2]], dtype=np.int32)   # sequence 1 replaced
+    rec = B.new_error_record()
+    out = torch.zeros(3, 4, 64, device="cuda")
+    B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out,
+                        work_items=torch.from_numpy(bad).cuda(), error_record=rec)
+    assert B.pa_error_read(rec) == [6, 1, 1, 3 * P + 5]
+    assert_matches_oracle(out[[0, 2]], oracle_decode(b, [0, 2]), "valid items")
+    assert not out[1].any()
