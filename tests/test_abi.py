@@ -216,3 +216,34 @@ def test_fused_append_rejects_missing_rows(lib):
     assert lib.paged_attn_decode_append(p, p, ctypes.c_void_p((1 << 20) + 4), p, p, p, p, 4, 8, 64,
                                         16, 4, 64, 0.125, 0, p, 2, 0, None, 0, None, None,
                                         None) == 1
+
+
+def test_partition_work_items_cover_each_partition_once():
+    from paged_kv_cache_317_gb300.binding import partition_work_items
+    lens = np.array([5, 0, 1024, 1025, 512, 3000, 513])
+    MB, bs, pt = 200, 16, 512
+    P = -(-MB * bs // pt)
+    items = partition_work_items(lens, pt, MB, bs)
+    assert items.dtype == np.int32
+    seen = sorted((int(i) // P, int(i) % P) for i in items)
+    want = sorted((i, p) for i, L in enumerate(lens) for p in range(max(1, -(-int(L) // pt))))
+    assert seen == want
+    # longest sequences first, partitions of a sequence in order
+    seqs = [int(i) // P for i in items]
+    order = list(dict.fromkeys(seqs))
+    assert order == sorted(range(len(lens)), key=lambda i: (-lens[i], i))
+    # automatic partition length (0) means 512; an explicit order is followed
+    assert np.array_equal(partition_work_items(lens, 0, MB, bs), items)
+    mine = partition_work_items(lens, 256, MB, bs, order=[6, 0, 1, 2, 3, 4, 5])
+    assert int(mine[0]) // (-(-MB * bs // 256)) == 6
+
+
+def test_decode_opts_layout_matches_the_header():
+    """The ctypes mirror of pa_decode_opts has the header's field order and size."""
+    from paged_kv_cache_317_gb300.binding import pa_decode_opts
+    hdr = open(os.path.join(HEADER_DIR, "pagedkv.h")).read()
+    body = hdr[hdr.index("typedef struct pa_decode_opts {"):hdr.index("} pa_decode_opts;")]
+    names = [ln.strip().rstrip(";").split()[-1].lstrip("*") for ln in body.splitlines()[1:]
+             if ln.strip()]
+    assert names == [f[0] for f in pa_decode_opts._fields_]
+    assert ctypes.sizeof(pa_decode_opts) == 40
