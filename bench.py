@@ -106,6 +106,26 @@ def step_bytes(lens, num_heads, head_dim, block_size, elt=2, out_elt=2, partitio
             "kv": kv, "total": partition + merge}
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, then /proc/cpuinfo), or 'unknown'."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine() or "unknown"
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -534,7 +554,19 @@ def run_workload(args, rank, world, local_rank):
         ws = torch.empty(B.paged_attn_workspace_size(N, plan.num_heads, plan.head_dim, bs,
                                                      max_blocks, 0), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
-        host_s, lens_seen = 0.0, 0
+        # per-step host inputs staged in pinned memory (two sets, reused once the
+        # copy that read them two steps back has finished)
+        n_items_max = N * int(-(-max_blocks * bs // 512))
+        pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
+                     "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
+                     "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
+                     "done": torch.cuda.Event()} for _ in range(2)]
+        dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
+                     "sl": torch.empty(N, dtype=torch.int32, device=dev),
+                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev)}
+                    for _ in range(2)]
+        host_s, stage_s, lens_seen = 0.0, 0.0, 0
+        split = []   # per step: events before copies, before table uploads, before decode, after
         t0 = time.perf_counter()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
@@ -549,19 +581,36 @@ def run_workload(args, rank, world, local_rank):
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs[0].record(stream)
             if len(pairs):
                 B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
+            evs[1].record(stream)
             q, k, v = tokens_all[s_]
-            items = torch.from_numpy(B.partition_work_items(lens, 0, max_blocks, plan.block_size))
-            B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
-                                       torch.from_numpy(lens).to(dev), plan.scale, out=out,
-                                       workspace=ws, error_record=rec,
-                                       work_items=items.to(dev))
+            hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
+            items = B.partition_work_items(lens, 0, max_blocks, plan.block_size)
+            h1 = time.perf_counter()
+            hs["done"].synchronize()
+            hs["bt"].numpy()[:] = tables
+            hs["sl"].numpy()[:] = lens
+            hs["it"].numpy()[: len(items)] = items
+            stage_s += time.perf_counter() - h1
+            ds["bt"].copy_(hs["bt"], non_blocking=True)
+            ds["sl"].copy_(hs["sl"], non_blocking=True)
+            ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
+            hs["done"].record(stream)
+            bt_d, sl_d, it_d = ds["bt"], ds["sl"], ds["it"][: len(items)]
+            evs[2].record(stream)
+            B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
+                                       workspace=ws, error_record=rec, work_items=it_d)
+            evs[3].record(stream)
+            split.append(evs)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) / plan.steps
         ms = ev0.elapsed_time(ev1) / plan.steps
+        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
         tokens = lens_seen / plan.steps
         total = tokens * plan.num_heads * plan.head_dim * 4
         value = total / (ms * 1e-3) / 1e9
@@ -569,9 +618,14 @@ def run_workload(args, rank, world, local_rank):
                                         "U[1024,4096], 26 forks/step, fused append+decode",
                             "steps_run": plan.steps, "l2": "inputs larger than L2"},
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
+                    host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
+                    device_ms_per_step_split={
+                        "block_copy": seg(0, 1), "table_uploads": seg(1, 2),
+                        "append_and_decode": seg(2, 3),
+                        "note": "the append is fused into the decode launch"},
                     note="value counts K/V bytes only; device time includes copies, H2D "
-                         "of tables and the decode")
+                         "of tables (staged in pinned memory, two buffer sets) and the decode")
     elif w == "prefill":
         # chunked prefill: 16 sequences append a 512-token chunk to contexts of 512..2048
         rng = np.random.default_rng(70)
@@ -661,6 +715,7 @@ def cpu_baseline(b, budget_s=15.0):
     dt = time.perf_counter() - t
     nb = step_bytes(b.context_lens[seqs], b.num_heads, b.head_dim, b.block_size)
     return {"value": round(nb["total"] / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "host_cpus": os.cpu_count(), "cpu_model": host_cpu_model(),
             "sample": f"{n} of {b.num_seqs} sequences (all heads), append + decode, "
                       f"{int(b.context_lens[seqs].sum())} context tokens, {dt:.2f} s",
             "seconds": round(dt, 3)}
@@ -709,6 +764,7 @@ def run_reference(args, rank, world, local_rank):
         "config": {"workload": "13B-shaped paged decode step: append 1 token/seq + decode",
                    "sample_seqs_per_step": n, "of_seqs": b.num_seqs},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "host_cpus": os.cpu_count(), "cpu_model": host_cpu_model(),
                          "sample": f"{n} of {b.num_seqs} sequences per step, all heads"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

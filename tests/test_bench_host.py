@@ -68,3 +68,8 @@ def test_two_gloo_ranks_reduce_max_and_sum():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert got == [(0, 2, 0, 2.5, 30.0), (1, 2, 1, 2.5, 30.0)]
+
+
+def test_host_cpu_model_is_a_nonempty_string():
+    m = bench.host_cpu_model()
+    assert isinstance(m, str) and m
