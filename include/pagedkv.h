@@ -220,7 +220,7 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  *   query_start   device int32 [num_seqs + 1], nondecreasing, query_start[num_seqs]
  *                 <= total_queries
  *   max_query_len host: >= every Q_i (sizes the grid)
- *   head_dim      128;  block_size: a multiple of 16
+ *   head_dim      64, 128 or 256;  block_size: a multiple of 16
  *   out           device [total_queries][num_heads][head_dim] in `out_dtype`
  * Rows of out outside every sequence's query range are not written.  A sequence
  * whose range is inconsistent (Q_i > L, range outside q, Q_i > max_query_len) is

@@ -9,8 +9,10 @@
 //
 //  * block = (128-query tile, head, sequence); 7 warps: one softmax warpgroup
 //    (one query row per thread = one TMEM lane), a K producer, an MMA issuer
-//    and a V producer.  ~113 KB of shared memory and 256 TMEM columns, so two
-//    blocks share an SM and cover each other's start-up and tail.
+//    and a V producer.  head_dim 64, 128 or 256: tiles are stored as head_dim /
+//    64 column groups of 64 elements.  At 64 and 128, <= 113 KB of shared memory
+//    and 256 TMEM columns, so two blocks share an SM and cover each other's
+//    start-up and tail; at 256, ~225 KB and 512 columns, one block per SM.
 //  * Q tile: two 3-D TMA loads (one per 64-wide half of head_dim, 128B
 //    swizzle), issued before the block-wide set-up barrier.  K/V: per 16-key
 //    chunk the producers follow the block table (32 entries at a time) and
@@ -49,27 +51,42 @@ namespace {
 
 constexpr int kQTile = 128;                       // query rows per block (MMA M)
 constexpr int kKTile = 64;                        // keys per tile
-constexpr int kHeadDim = 128;
 constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
 constexpr int kWarpK = 4, kWarpMma = 5, kWarpV = 6;
 constexpr int kKStages = 2;                       // K ring depth
 constexpr int kVStages = 3;                       // V ring depth: V(j+3) loads while P.V(j+1..j+2) run
-constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B (one 64-wide half)
-constexpr int kQBytes = kQTile * kHeadDim * 2;    // 32 KB (two 16 KB halves)
-constexpr int kTileBytes = 2 * kHalfBytes;        // one K or V tile: 16 KB
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-// Two blocks must fit an SM (228 KB, less 1 KB reserved per block): 768 bytes are
-// left for aligning the dynamic shared-memory base to 1 KB; the kernel checks it.
-constexpr int kAlignSlack = 768;
-constexpr int kSmemBytes = kOffBar + 256 + kAlignSlack;
-static_assert(kSmemBytes <= 228 * 1024 / 2 - 1024, "two blocks per SM");
+constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B: one 64-wide column group of a K/V tile
+constexpr int kQHalfBytes = kQTile * 128;         // 128 rows x 128 B: one 64-wide column group of Q
 // TMEM: two S/P buffers of 64 columns (S in fp32; after the softmax, P hi in the
-// first 32 columns and P lo in the next 32, two 16-bit values per column) and O.
-constexpr uint32_t kTmemCols = 256;
+// first 32 columns and P lo in the next 32, two 16-bit values per column), then O.
 constexpr uint32_t kTmemO = 2 * kKTile;
+
+// Sizes that follow from head_dim D (64, 128 or 256): the tiles are stored as
+// D / 64 column groups of 64 elements (128 bytes, the 128-byte swizzle atom).
+template <int D>
+struct Cfg {
+  static constexpr int kGroups = D / 64;
+  static constexpr int kQBytes = kGroups * kQHalfBytes;       // 16 / 32 / 64 KB
+  static constexpr int kTileBytes = kGroups * kHalfBytes;     // one K or V tile: 8 / 16 / 32 KB
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  // At D = 128 two blocks must fit an SM (228 KB, less 1 KB reserved per block):
+  // 768 bytes are left for aligning the dynamic shared-memory base to 1 KB; the
+  // kernel checks it.  Otherwise a full 1 KB is left.
+  static constexpr int kAlignSlack = D == 128 ? 768 : 1024;
+  static constexpr int kSmemUsed = kOffBar + 256 + kAlignSlack;
+  // Requested per block: at least 80 KB, so that no more than two blocks (two
+  // 256-column TMEM allocations) ever share an SM, whatever the register count.
+  static constexpr int kSmemBytes = kSmemUsed > 80 * 1024 ? kSmemUsed : 80 * 1024;
+  // D = 256 needs 384 TMEM columns (allocated as 512) and ~225 KB: one block per SM.
+  static constexpr int kMinBlocks = D <= 128 ? 2 : 1;
+  static constexpr uint32_t kTmemCols = kTmemO + D <= 256 ? 256 : 512;
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+  static_assert(kMinBlocks == 1 || kSmemBytes <= 228 * 1024 / 2 - 1024, "two blocks per SM");
+  static_assert(kSmemBytes <= 227 * 1024, "one block per SM");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 // A row's exponentials are taken against a reference max that only moves when
 // the running max exceeds it by more than this (log2 units): p <= 2^8, exact in
@@ -243,11 +260,12 @@ __device__ __forceinline__ float half_to_float(uint32_t bits16) {
   }
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using C = Cfg<D>;
   const int qt = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -274,16 +292,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
-  if (pad > kAlignSlack) {  // never seen: the base is 1 KB aligned in practice
+  if (pad > C::kAlignSlack) {  // never seen: the base is 1 KB aligned in practice
     if (threadIdx.x == 0) report_error(p.err, PA_ERR_UNSUPPORTED, seq, static_cast<int>(pad));
     return;
   }
   uint8_t* smem = smem_raw + pad;
-  uint8_t* Qs = smem + kOffQ;
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  uint8_t* Qs = smem + C::kOffQ;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   volatile int* abort_flag = &bars->abort;
-  auto k_tile = [&](int s) { return smem + kOffK + s * kTileBytes; };
-  auto v_tile = [&](int s) { return smem + kOffV + s * kTileBytes; };
+  auto k_tile = [&](int s) { return smem + C::kOffK + s * C::kTileBytes; };
+  auto v_tile = [&](int s) { return smem + C::kOffV + s * C::kTileBytes; };
 
   // Started before the block-wide barrier so that their latency overlaps the
   // set-up: the Q tile load (its barrier initialised by the issuing thread)
@@ -296,9 +314,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kWarpK && lane == 0) {
       mbar_init(&bars->q_full, 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-      tma_load_3d(Qs, &tm_q, 0, h, q_begin + q0, &bars->q_full);
-      tma_load_3d(Qs + kQBytes / 2, &tm_q, 64, h, q_begin + q0, &bars->q_full);
+      mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
+#pragma unroll
+      for (int g = 0; g < C::kGroups; ++g)
+        tma_load_3d(Qs + g * kQHalfBytes, &tm_q, 64 * g, h, q_begin + q0, &bars->q_full);
     }
   }
   if (threadIdx.x == 0) {
@@ -322,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kWarpMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&bars->tmem_base)),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       int ok = 1;
       if (lane == 0) {
         if (use > 0) ok = mbar_wait_bounded(empty, (use - 1) & 1);
-        if (ok) mbar_arrive_expect_tx(full, static_cast<uint32_t>(n) * 2 * 2048);
+        if (ok) mbar_arrive_expect_tx(full, static_cast<uint32_t>(n) * C::kGroups * 2048);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
       if (!ok) {
@@ -376,8 +395,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int k0 = j * kKTile + c * 16;
         if (lane == 0 && k0 < keys) {
           const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
-          tma_load_2d(dst + c * 2048, map, 0, row, full);
-          tma_load_2d(dst + kHalfBytes + c * 2048, map, 64, row, full);
+#pragma unroll
+          for (int g = 0; g < C::kGroups; ++g)
+            tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
         }
       }
       kv_issued = j + 1;
@@ -388,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(kQTile, kKTile, BF16, false);
-      constexpr uint32_t idesc_o = make_idesc(kQTile, kHeadDim, BF16, true);
+      constexpr uint32_t idesc_o = make_idesc(kQTile, D, BF16, true);
       bool ok = mbar_wait_bounded(&bars->q_full, 0);
       // S_j goes to TMEM buffer j & 1, whose previous contents (P of tile j-2)
       // must have been consumed by P.V(j-2).
@@ -399,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         const uint8_t* ks = k_tile(s);
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const int half = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(Qs + half * (kQBytes / 2) + off, 16, 1024);
+          const uint64_t a = smem_desc_sw128(Qs + half * kQHalfBytes + off, 16, 1024);
           const uint64_t bd = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
           mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
         }
@@ -510,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           float o[32];
           tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
 #pragma unroll
@@ -530,10 +550,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!ok) break;
         uint8_t* vs = v_tile(s);
         const int first = keys - kbase;
-        const int n16 = (kKTile - first) * 2 * 8;  // rows x halves x 16-byte pieces
+        constexpr int kPieces = C::kGroups * 8;     // 16-byte pieces per row
+        const int n16 = (kKTile - first) * kPieces;
         for (int idx = r; idx < n16; idx += kQTile) {
-          const int row = first + idx / 16;
-          const int rest = idx % 16;
+          const int row = first + idx / kPieces;
+          const int rest = idx % kPieces;
           *reinterpret_cast<uint4*>(vs + (rest >> 3) * kHalfBytes + row * 128 + (rest & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
@@ -555,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t row_off =
-          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * kHeadDim;
+          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
         tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
 #pragma unroll
@@ -597,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_after();
   if (warp == kWarpMma) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
   }
 }
@@ -628,16 +649,24 @@ bool encode(CUtensorMap* map, bool bf16, const void* base, int rank, const cuuin
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool BF16>
+template <bool BF16, int D>
 cudaError_t ensure_prefill_smem(int device) {
   static std::atomic<uint64_t> done{0};
   const uint64_t bit = device < 64 ? (1ull << device) : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<BF16>,
+  const cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<BF16, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+                                             Cfg<D>::kSmemBytes);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
+}
+
+template <bool BF16, int D>
+int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const PrefillParams& p, dim3 grid, int device, cudaStream_t st) {
+  if (ensure_prefill_smem<BF16, D>(device) != cudaSuccess) return PA_ERR_CUDA;
+  paged_prefill_kernel<BF16, D><<<grid, kThreads, Cfg<D>::kSmemBytes, st>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -656,7 +685,8 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
       block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || total_queries == 0 || max_query_len == 0) return PA_OK;
-  if (head_dim != kHeadDim || block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if ((head_dim != 64 && head_dim != 128 && head_dim != 256) || block_size % 16 != 0)
+    return PA_ERR_UNSUPPORTED;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32)
     return PA_ERR_UNSUPPORTED;
@@ -704,13 +734,14 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
 
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
-  const cudaError_t e = bf16 ? ensure_prefill_smem<true>(device) : ensure_prefill_smem<false>(device);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  dim3 grid((max_query_len + kQTile - 1) / kQTile, num_heads, num_seqs);
+  const dim3 grid((max_query_len + kQTile - 1) / kQTile, num_heads, num_seqs);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (bf16)
-    paged_prefill_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
-  else
-    paged_prefill_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  switch ((bf16 ? 1 : 0) | (head_dim == 64 ? 0 : head_dim == 128 ? 2 : 4)) {
+    case 0: return launch_prefill<false, 64>(tq, tk, tv, p, grid, device, st);
+    case 1: return launch_prefill<true, 64>(tq, tk, tv, p, grid, device, st);
+    case 2: return launch_prefill<false, 128>(tq, tk, tv, p, grid, device, st);
+    case 3: return launch_prefill<true, 128>(tq, tk, tv, p, grid, device, st);
+    case 4: return launch_prefill<false, 256>(tq, tk, tv, p, grid, device, st);
+    default: return launch_prefill<true, 256>(tq, tk, tv, p, grid, device, st);
+  }
 }

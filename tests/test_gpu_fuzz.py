@@ -67,14 +67,15 @@ def test_decode_random_configuration(B, seed):
 @pytest.mark.parametrize("seed", range(32))
 def test_prefill_random_configuration(B, seed):
     rng = np.random.default_rng(3000 + seed)
+    D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32]))
     H = int(rng.integers(1, 5))
     N = int(rng.integers(1, 5))
     dtype = str(rng.choice(["f16", "bf16"]))
     lens = [int(x) for x in rng.integers(1, 900, size=N)]
     nq = [min(L, int(rng.integers(0, 257))) if rng.random() < 0.8 else min(L, 300) for L in lens]
-    b = random_decode_batch(4000 + seed, lens, H, 128, bs, dtype=dtype, device="cuda")
-    q = randn_rounded((max(1, sum(nq)), H, 128), b.dtype, _torch_gen(5000 + seed, "cuda"),
+    b = random_decode_batch(4000 + seed, lens, H, D, bs, dtype=dtype, device="cuda")
+    q = randn_rounded((max(1, sum(nq)), H, D), b.dtype, _torch_gen(5000 + seed, "cuda"),
                       "cuda")
     starts = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
     out_dtype = [torch.float32, torch.float16, torch.bfloat16][int(rng.integers(0, 3))]
@@ -91,4 +92,4 @@ def test_prefill_random_configuration(B, seed):
     ref = OA.paged_prefill_attention(qs, kc, vc, b.block_tables, b.context_lens, starts, b.scale,
                                      bs, dt)
     assert_matches_oracle(out[: starts[-1]], ref,
-                          f"seed {seed}: bs{bs} H{H} N{N} {dtype} nq={nq} lens={lens}")
+                          f"seed {seed}: D{D} bs{bs} H{H} N{N} {dtype} nq={nq} lens={lens}")

@@ -18,10 +18,10 @@ def B(lib):
     return binding
 
 
-def _case(seed, lens, nq, H, bs, dtype, poison=True):
-    b = random_decode_batch(seed, lens, H, 128, bs, dtype=dtype, device="cuda", poison=poison)
+def _case(seed, lens, nq, H, bs, dtype, poison=True, D=128):
+    b = random_decode_batch(seed, lens, H, D, bs, dtype=dtype, device="cuda", poison=poison)
     g = _torch_gen(seed + 7, "cuda")
-    q = randn_rounded((int(sum(nq)), H, 128), b.dtype, g, "cuda")
+    q = randn_rounded((int(sum(nq)), H, D), b.dtype, g, "cuda")
     starts = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
     return b, q, starts
 
@@ -169,3 +169,20 @@ def test_prefill_bad_block_entry_is_recorded_and_clamped(B):
     assert r[0] == 4 and r[1] >= 1 and r[2] == 1 and r[3] == b.num_blocks + 9
     assert torch.isfinite(out).all()
     assert_matches_oracle(out[: starts[1]], _oracle(b, q, starts, seqs=[0]), "unaffected sequence")
+
+
+@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_other_head_dims(B, D, dtype):
+    """head_dim 64 (two blocks per SM) and 256 (512 TMEM columns, one block per SM)."""
+    lens = [5, 300, 1000, 17, 129, 700]
+    nq = [5, 64, 200, 1, 129, 256]
+    b, q, starts = _case(60 + D, lens, nq, 3, 16, dtype, D=D)
+    rec = B.new_error_record()
+    out = _run(B, b, q, starts, rec=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert_matches_oracle(out, _oracle(b, q, starts), f"prefill D{D} {dtype}")
+    again = _run(B, b, q, starts)
+    torch.cuda.synchronize()
+    assert torch.equal(out, again)
