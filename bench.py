@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 METRIC = "paged-attn decode KV GB/s (% of HBM peak), seq-tokens/s at 13B shape"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+PREFILL_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_prefill.cu",
+                   "paged_kv_cache_317_gb300/csrc/common.cuh")
 DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_attn_decode.cu",
                   "paged_kv_cache_317_gb300/csrc/common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -146,22 +148,26 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
-def decode_source_sha() -> str:
+def source_sha(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in DECODE_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
+def decode_source_sha() -> str:
+    return source_sha(DECODE_SOURCES)
+
+
+def recorded_traffic(kernel: str, sources=DECODE_SOURCES):
     """dram bytes per launch from the last ncu capture, if the kernel is unchanged since."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)[kernel]
     except Exception:
         return None
-    if rec.get("source_sha") != decode_source_sha():
+    if rec.get("source_sha") != source_sha(sources):
         return None
     return rec.get("dram_bytes_per_launch_full_size")
 
@@ -653,6 +659,8 @@ def run_workload(args, rank, world, local_rank):
                             "queries": tokens, "context_tokens": int(lens.sum())},
                     dtype="bf16",
                     roofline={"kernel": "paged_prefill_kernel", "bound": "tensor",
+                              "traffic": recorded_traffic("paged_prefill_kernel",
+                                                          PREFILL_SOURCES),
                               "achieved": round(tflops, 2), "peak": peak_tf,
                               "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4),
                               "peak_source": peak_tf_kind, "flops_per_launch": flops,
