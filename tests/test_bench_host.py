@@ -4,7 +4,6 @@ multi-rank reductions (two gloo ranks on 127.0.0.1)."""
 import os
 import socket
 
-import numpy as np
 import torch.multiprocessing as mp
 
 import bench

@@ -5,7 +5,6 @@ max-length reservation wastes 60-80 % (PagedAttention, zeroshotmind.com page,
 "The memory you allocate but never use" and "The fragmentation arithmetic")."""
 
 import json
-import math
 import os
 
 import numpy as np

@@ -6,7 +6,6 @@ in logical order and recomputes every output (PagedAttention, zeroshotmind.com
 page, "Sharing a prefix without copying it": candidates share everything up to
 where they differ)."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import (assert_matches_oracle, bits, device_tables, oracle_decode, storage)
+from gpu_util import (assert_matches_oracle, device_tables, oracle_decode, storage)
 from oracle import attention as OA
 from workloads import random_decode_batch, tiny_decode
 

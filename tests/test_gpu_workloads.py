@@ -14,10 +14,10 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import assert_matches_oracle, bits, device_tables, oracle_decode, storage
+from gpu_util import assert_matches_oracle, device_tables, oracle_decode, storage
 from oracle import attention as OA
 from oracle.content import LogicalSequences
-from workloads import decode_13b, long_context, mixed_serving, parallel_sampling, tiny_decode
+from workloads import decode_13b, long_context, mixed_serving, parallel_sampling
 
 pytestmark = pytest.mark.gpu
 
