@@ -72,3 +72,14 @@ def test_two_gloo_ranks_reduce_max_and_sum():
 def test_host_cpu_model_is_a_nonempty_string():
     m = bench.host_cpu_model()
     assert isinstance(m, str) and m
+
+
+def test_clock_records_that_are_rejected():
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(dict(ok, reasons=["sw_power_cap"], sm_mhz=1800.0))
+    assert bench.clocks_rejected(dict(ok, reasons=["hw_slowdown"]))
+    assert bench.clocks_rejected(dict(ok, reasons=["sw_thermal_slowdown", "sw_power_cap"]))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))          # locked low, no reason
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None,
+                                      "reasons": ["nvidia-smi unavailable"]})
