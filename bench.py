@@ -599,11 +599,13 @@ def run_workload(args, rank, world, local_rank):
         ev0.record(stream)
         for s_ in range(plan.steps):
             h0 = time.perf_counter()
-            for a_, b_ in plan.fork_pairs[s_]:
-                alloc.free(ids[b_])
-                alloc.fork(ids[a_], next_id)
-                ids[b_] = next_id
-                next_id += 1
+            fp = plan.fork_pairs[s_]
+            if len(fp):
+                alloc.batch_free([ids[b_] for _, b_ in fp])
+                alloc.batch_fork([ids[a_] for a_, _ in fp], range(next_id, next_id + len(fp)))
+                for a_, b_ in fp:
+                    ids[b_] = next_id
+                    next_id += 1
             slots, pairs = alloc.batch_append(ids)
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
@@ -616,8 +618,8 @@ def run_workload(args, rank, world, local_rank):
             q, k, v = tokens_all[s_]
             hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
             items = B.partition_work_items(lens, 0, max_blocks, plan.block_size)
+            hs["done"].synchronize()            # the copy that read this buffer set
             h1 = time.perf_counter()
-            hs["done"].synchronize()
             hs["bt"].numpy()[:] = tables
             hs["sl"].numpy()[:] = lens
             hs["it"].numpy()[: len(items)] = items
@@ -653,6 +655,118 @@ def run_workload(args, rank, world, local_rank):
                         "note": "the append is fused into the decode launch"},
                     note="value counts K/V bytes only; device time includes copies, H2D "
                          "of tables (staged in pinned memory, two buffer sets) and the decode")
+    elif w == "beam":
+        # beam-search churn: each step every group keeps the survivors of a random
+        # score draw (forks of their parents, the old beams end), every beam
+        # appends a token (copy-on-write of shared tails) and all beams decode
+        plan = WL.beam_search(device=dev, groups=64, width=4, steps=40, prompt=(500, 1500),
+                              num_heads=40, head_dim=128)
+        G_, Wd, H, D, bs = plan.groups, plan.width, plan.num_heads, plan.head_dim, plan.block_size
+        N = G_ * Wd
+        alloc = B.BlockAllocator(plan.num_blocks, bs, plan.free_order)
+        kc = torch.zeros((plan.num_blocks, H, bs, D), dtype=plan.dtype, device=dev)
+        vc = torch.zeros_like(kc)
+        next_id, beams = 0, []
+        for g in range(G_):
+            a, e = int(plan.prompt_offsets[g]), int(plan.prompt_offsets[g + 1])
+            root = next_id
+            next_id += 1
+            alloc.add(root, e - a)
+            B.kv_cache_append(plan.prompt_k[a:e], plan.prompt_v[a:e],
+                              torch.from_numpy(alloc.slots(root, 0, e - a)).to(dev), kc, vc)
+            grp = []
+            for _ in range(Wd):
+                alloc.fork(root, next_id)
+                grp.append(next_id)
+                next_id += 1
+            alloc.free(root)
+            beams.append(grp)
+        max_blocks = int(-(-(plan.prompt_lens.max() + plan.steps + 1) // bs))
+        tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
+        out = torch.empty((N, H, D), dtype=plan.dtype, device=dev)
+        ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, max_blocks, 0),
+                         dtype=torch.uint8, device=dev)
+        n_items_max = N * int(-(-max_blocks * bs // 512))
+        pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
+                     "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
+                     "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
+                     "done": torch.cuda.Event()} for _ in range(2)]
+        dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
+                     "sl": torch.empty(N, dtype=torch.int32, device=dev),
+                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev)}
+                    for _ in range(2)]
+        torch.cuda.synchronize()
+        host_s, stage_s, lens_seen, copies = 0.0, 0.0, 0, 0
+        split = []
+        t0 = time.perf_counter()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for s_ in range(plan.steps):
+            h0 = time.perf_counter()
+            old = np.asarray(beams, dtype=np.int64)                    # [groups, width]
+            parents = np.take_along_axis(old, plan.parents[s_], axis=1).ravel()
+            children = np.arange(next_id, next_id + N, dtype=np.int64)
+            next_id += N
+            alloc.batch_fork(parents, children)
+            alloc.batch_free(old.ravel())
+            beams = children.reshape(G_, Wd).tolist()
+            ids = [i for grp in beams for i in grp]
+            slots, pairs = alloc.batch_append(ids)
+            tables, lens = alloc.batch_block_tables(ids, max_blocks)
+            host_s += time.perf_counter() - h0
+            lens_seen += int(lens.sum())
+            copies += len(pairs)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs[0].record(stream)
+            if len(pairs):
+                B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
+            evs[1].record(stream)
+            q, k, v = tokens_all[s_]
+            hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
+            items = B.partition_work_items(lens, 0, max_blocks, bs)
+            hs["done"].synchronize()            # the copy that read this buffer set
+            h1 = time.perf_counter()
+            hs["bt"].numpy()[:] = tables
+            hs["sl"].numpy()[:] = lens
+            hs["it"].numpy()[: len(items)] = items
+            stage_s += time.perf_counter() - h1
+            ds["bt"].copy_(hs["bt"], non_blocking=True)
+            ds["sl"].copy_(hs["sl"], non_blocking=True)
+            ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
+            hs["done"].record(stream)
+            evs[2].record(stream)
+            B.paged_attn_decode_append(q, k, v, kc, vc, ds["bt"], ds["sl"], plan.scale, out=out,
+                                       workspace=ws, error_record=rec,
+                                       work_items=ds["it"][: len(items)])
+            evs[3].record(stream)
+            split.append(evs)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) / plan.steps
+        ms = ev0.elapsed_time(ev1) / plan.steps
+        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
+        tokens = lens_seen / plan.steps
+        total = tokens * H * D * 4
+        value = total / (ms * 1e-3) / 1e9
+        for grp in beams:
+            for i in grp:
+                alloc.free(i)
+        if alloc.num_free() != plan.num_blocks:
+            raise RuntimeError("beam workload leaked blocks")
+        line.update(config={"workload": "beam-search churn: 64 groups x 4 beams, prompts "
+                                        "U[500,1500], 40 heads x 128, bf16, block 16",
+                            "steps_run": plan.steps, "l2": "inputs larger than L2"},
+                    dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
+                    host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
+                    wall_ms_per_step=round(1e3 * wall, 4),
+                    copies_per_step=round(copies / plan.steps, 2),
+                    device_ms_per_step_split={
+                        "block_copy": seg(0, 1), "table_uploads": seg(1, 2),
+                        "append_and_decode": seg(2, 3),
+                        "note": "the append is fused into the decode launch"},
+                    note="value counts logical K/V bytes (beams share prefix blocks, so part "
+                         "of them is served from L2)")
     elif w == "prefill":
         # chunked prefill: 16 sequences append a 512-token chunk to contexts of 512..2048
         rng = np.random.default_rng(70)
@@ -810,7 +924,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="13b",
-                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "prefill"],
+                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "beam",
+                             "prefill"],
                     help="13b (default, the headline line) or another seeded workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -347,6 +347,14 @@ int32_t pa_num_seqs(const pa_allocator* a);
  * nothing. */
 int pa_batch_append(pa_allocator* a, const int64_t* seqs, int32_t n, int64_t* slots,
                     int64_t* cow_pairs, int32_t* num_cow);
+/* n forks, children[i] sharing every block of parents[i], applied in order (a
+ * child forked earlier in the call may be a later parent).  All-or-nothing: a
+ * missing parent (PA_ERR_NO_SEQ) or a child that exists or repeats
+ * (PA_ERR_SEQ_EXISTS) is reported before anything changes. */
+int pa_batch_fork(pa_allocator* a, const int64_t* parents, const int64_t* children, int32_t n);
+/* n frees (see pa_seq_free).  All-or-nothing: an id that is missing or listed
+ * twice returns PA_ERR_NO_SEQ before anything changes. */
+int pa_batch_free(pa_allocator* a, const int64_t* seqs, int32_t n);
 /* Block tables of the listed sequences as rows of tables[n][max_blocks] (entries
  * past a table's end are -1) and their lengths. PA_ERR_INVALID_ARG if a table
  * does not fit. */

@@ -56,10 +56,11 @@ def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: in
     lens = np.asarray(seq_lens, dtype=np.int64)
     pt = partition_tokens if partition_tokens > 0 else 512
     P = max(1, -(-max_blocks_per_seq * block_size // pt))
-    if order is None:
-        order = np.argsort(-lens, kind="stable")
-    items = [i * P + p for i in order for p in range(max(1, -(-int(lens[i]) // pt)))]
-    return np.asarray(items, dtype=np.int32)
+    order = np.argsort(-lens, kind="stable") if order is None else np.asarray(order, np.int64)
+    nparts = np.maximum(1, -(-lens[order] // pt))
+    first = np.repeat(np.cumsum(nparts) - nparts, nparts)
+    part = np.arange(int(nparts.sum()), dtype=np.int64) - first
+    return (np.repeat(order, nparts) * P + part).astype(np.int32)
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
@@ -105,6 +106,8 @@ SIGNATURES = {
     "pa_num_free_blocks": (c_int32, [c_void_p]),
     "pa_num_seqs": (c_int32, [c_void_p]),
     "pa_batch_append": (c_int, [c_void_p, P_int64, c_int32, P_int64, P_int64, P_int32]),
+    "pa_batch_fork": (c_int, [c_void_p, P_int64, P_int64, c_int32]),
+    "pa_batch_free": (c_int, [c_void_p, P_int64, c_int32]),
     "pa_batch_block_tables": (c_int, [c_void_p, P_int64, c_int32, c_int32, P_int32, P_int32]),
     "pa_alloc_stats": (c_int, [c_void_p, P_int32, P_int64, P_int64, P_int64]),
     "pa_alloc_check": (c_int, [c_void_p]),
@@ -422,6 +425,24 @@ class BlockAllocator:
                                          pairs.ctypes.data_as(P_int64), ctypes.byref(nc)),
                "pa_batch_append")
         return slots, pairs[: nc.value].copy()
+
+    def batch_fork(self, parents, children) -> None:
+        """children[i] shares every block of parents[i]; all-or-nothing."""
+        import numpy as np
+        par = np.ascontiguousarray(parents, dtype=np.int64)
+        chi = np.ascontiguousarray(children, dtype=np.int64)
+        if par.shape != chi.shape:
+            raise ValueError("parents and children differ in length")
+        _check(self._lib.pa_batch_fork(self._h, par.ctypes.data_as(P_int64),
+                                       chi.ctypes.data_as(P_int64), par.shape[0]),
+               "pa_batch_fork")
+
+    def batch_free(self, seqs) -> None:
+        """End every listed sequence; all-or-nothing."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        _check(self._lib.pa_batch_free(self._h, ids.ctypes.data_as(P_int64), ids.shape[0]),
+               "pa_batch_free")
 
     def batch_block_tables(self, seqs, max_blocks: int):
         import numpy as np

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <new>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "pagedkv.h"
@@ -242,6 +243,51 @@ extern "C" int pa_batch_append(pa_allocator* a, const int64_t* seqs, int32_t n, 
   }
   *num_cow = nc;
   return PA_OK;
+}
+
+extern "C" int pa_batch_fork(pa_allocator* a, const int64_t* parents, const int64_t* children,
+                             int32_t n) {
+  if (!a || n < 0 || (n > 0 && (!parents || !children))) return PA_ERR_INVALID_ARG;
+  try {
+    // Check every pair in order (a child forked earlier in the batch may be a
+    // later parent) before changing anything.
+    std::unordered_set<int64_t> added;
+    for (int32_t i = 0; i < n; ++i) {
+      if (!a->seqs.count(parents[i]) && !added.count(parents[i])) return PA_ERR_NO_SEQ;
+      if (a->seqs.count(children[i]) || !added.insert(children[i]).second)
+        return PA_ERR_SEQ_EXISTS;
+    }
+    a->seqs.reserve(a->seqs.size() + static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i) {
+      pa_allocator::Seq copy = a->seqs.at(parents[i]);
+      for (int32_t b : copy.blocks) ++a->refcount[b];
+      a->seqs.emplace(children[i], std::move(copy));
+    }
+  } catch (...) {
+    return PA_ERR_OOM;
+  }
+  return PA_OK;
+}
+
+extern "C" int pa_batch_free(pa_allocator* a, const int64_t* seqs, int32_t n) {
+  if (!a || n < 0 || (n > 0 && !seqs)) return PA_ERR_INVALID_ARG;
+  try {
+    std::unordered_set<int64_t> seen;
+    for (int32_t i = 0; i < n; ++i) {
+      if (!a->seqs.count(seqs[i])) return PA_ERR_NO_SEQ;
+      if (!seen.insert(seqs[i]).second) return PA_ERR_NO_SEQ;  // listed twice
+    }
+  } catch (...) {
+    return PA_ERR_OOM;
+  }
+  int status = PA_OK;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = a->seqs.find(seqs[i]);
+    for (int32_t b : it->second.blocks)
+      if (!a->release(b)) status = PA_ERR_REFCOUNT;
+    a->seqs.erase(it);
+  }
+  return status;
 }
 
 extern "C" int pa_batch_block_tables(const pa_allocator* a, const int64_t* seqs, int32_t n,

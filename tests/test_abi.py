@@ -247,3 +247,62 @@ def test_decode_opts_layout_matches_the_header():
              if ln.strip()]
     assert names == [f[0] for f in pa_decode_opts._fields_]
     assert ctypes.sizeof(pa_decode_opts) == 40
+
+
+def test_batch_fork_and_free_match_single_calls(lib):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator
+    rng = np.random.default_rng(11)
+    order = rng.permutation(600).astype(np.int32)
+    one, many = BlockAllocator(600, 16, order), BlockAllocator(600, 16, order)
+    model = BlockAllocatorModel(600, 16, order)
+    for s in range(6):
+        n = int(rng.integers(1, 300))
+        for a in (one, many, model):
+            a.add(s, n)
+    next_id = 6
+    live = list(range(6))
+    for step in range(30):
+        parents = [int(rng.choice(live)) for _ in range(5)]
+        children = list(range(next_id, next_id + 5))
+        next_id += 5
+        parents[3] = children[1]                     # a child forked earlier in the batch
+        for p, c in zip(parents, children):
+            one.fork(p, c)
+            model.fork(p, c)
+        many.batch_fork(parents, children)
+        live += children
+        gone = [int(x) for x in rng.choice(live, size=4, replace=False)]
+        for g in gone:
+            one.free(g)
+            model.free_seq(g)
+        many.batch_free(gone)
+        live = [x for x in live if x not in gone]
+        for a in (one, many, model):
+            a.append(live[0])
+        for s in live:
+            assert many.block_table(s) == one.block_table(s) == model.tables[s]
+        assert many.num_free() == one.num_free()
+    many.check()
+    _same_state(many, model)
+
+
+def test_batch_fork_and_free_are_all_or_nothing(lib):
+    from paged_kv_cache_317_gb300.binding import BlockAllocator, PagedKVError
+    cpp = BlockAllocator(50, 16)
+    cpp.add(0, 40)
+    cpp.add(1, 20)
+    before = (cpp.num_seqs(), cpp.num_free(), cpp.refcount(cpp.block_table(0)[0]))
+    for parents, children, code in (([0, 7], [2, 3], "PA_ERR_NO_SEQ"),       # missing parent
+                                    ([0, 1], [2, 2], "PA_ERR_SEQ_EXISTS"),   # repeated child
+                                    ([0, 1], [2, 1], "PA_ERR_SEQ_EXISTS")):  # existing child
+        with pytest.raises(PagedKVError) as e:
+            cpp.batch_fork(parents, children)
+        assert e.value.name == code
+        assert (cpp.num_seqs(), cpp.num_free(), cpp.refcount(cpp.block_table(0)[0])) == before
+    for seqs in ([0, 9], [1, 1]):                                            # missing / twice
+        with pytest.raises(PagedKVError) as e:
+            cpp.batch_free(seqs)
+        assert e.value.name == "PA_ERR_NO_SEQ"
+        assert (cpp.num_seqs(), cpp.num_free()) == before[:2]
+    cpp.batch_free([0, 1])
+    assert cpp.num_seqs() == 0 and cpp.num_free() == 50
