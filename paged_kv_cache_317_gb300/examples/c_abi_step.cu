@@ -1,0 +1,178 @@
+// A decode step driven through the C ABI alone (include/pagedkv.h and
+// libpagedkv.so; no Python): host allocator, KV append, copy-on-write block
+// copy and paged decode attention.  It checks two exact properties:
+//  * a sequence forked from another and given the same next token decodes to
+//    the same bits as its parent, although its last block is a private copy;
+//  * a one-token sequence returns its value row exactly (one weight of 1).
+// Build: nvcc -std=c++17 -I include c_abi_step.cu -L<dir> -lpagedkv -o c_abi_step
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace {
+
+constexpr int kHeads = 4, kDim = 128, kBlock = 16, kBlocks = 64, kMaxBlocks = 8;
+
+#define CHECK(call)                                                                 \
+  do {                                                                              \
+    const int st_ = (call);                                                         \
+    if (st_ != 0) {                                                                 \
+      std::fprintf(stderr, "%s failed: %d (%s)\n", #call, st_, pa_status_string(st_)); \
+      return 1;                                                                     \
+    }                                                                               \
+  } while (0)
+#define CUDA(call)                                                                  \
+  do {                                                                              \
+    const cudaError_t e_ = (call);                                                  \
+    if (e_ != cudaSuccess) {                                                        \
+      std::fprintf(stderr, "%s: %s\n", #call, cudaGetErrorString(e_));            \
+      return 1;                                                                     \
+    }                                                                               \
+  } while (0)
+
+// Deterministic values in [-1, 1) (a 32-bit linear congruential sequence).
+struct Lcg {
+  uint32_t s;
+  float next() {
+    s = s * 1664525u + 1013904223u;
+    return static_cast<float>(s >> 8) / 8388608.0f - 1.0f;
+  }
+};
+
+std::vector<__half> random_rows(Lcg& g, int rows) {
+  std::vector<__half> v(static_cast<size_t>(rows) * kHeads * kDim);
+  for (auto& x : v) x = __float2half(g.next());
+  return v;
+}
+
+}  // namespace
+
+int main() {
+  std::printf("libpagedkv version %d\n", pa_version());
+  pa_allocator* alloc = pa_alloc_create(kBlocks, kBlock, nullptr);
+  if (!alloc) return 1;
+
+  // sequence 0: a 37-token prompt; sequence 2: one token; sequence 1 = fork of 0
+  const int prompt = 37;
+  CHECK(pa_seq_add(alloc, 0, prompt));
+  CHECK(pa_seq_add(alloc, 2, 1));
+  CHECK(pa_seq_fork(alloc, 0, 1));
+  std::vector<int64_t> slots(prompt + 1);
+  CHECK(pa_seq_slots(alloc, 0, 0, prompt, slots.data()));
+  CHECK(pa_seq_slots(alloc, 2, 0, 1, slots.data() + prompt));
+
+  Lcg g{12345u};
+  const std::vector<__half> k0 = random_rows(g, prompt + 1), v0 = random_rows(g, prompt + 1);
+  const size_t row = static_cast<size_t>(kHeads) * kDim;
+  const size_t cache_elems = static_cast<size_t>(kBlocks) * kHeads * kBlock * kDim;
+
+  __half *kc, *vc, *k, *v, *q;
+  int64_t* slot_d;
+  int64_t* pair_d;
+  int32_t *tables_d, *lens_d, *rec;
+  float* out;
+  CUDA(cudaMalloc(&kc, cache_elems * sizeof(__half)));
+  CUDA(cudaMalloc(&vc, cache_elems * sizeof(__half)));
+  CUDA(cudaMemset(kc, 0, cache_elems * sizeof(__half)));
+  CUDA(cudaMemset(vc, 0, cache_elems * sizeof(__half)));
+  CUDA(cudaMalloc(&k, (prompt + 1) * row * sizeof(__half)));
+  CUDA(cudaMalloc(&v, (prompt + 1) * row * sizeof(__half)));
+  CUDA(cudaMalloc(&slot_d, (prompt + 1) * sizeof(int64_t)));
+  CUDA(cudaMalloc(&pair_d, 2 * sizeof(int64_t)));
+  CUDA(cudaMalloc(&q, 3 * row * sizeof(__half)));
+  CUDA(cudaMalloc(&tables_d, 3 * kMaxBlocks * sizeof(int32_t)));
+  CUDA(cudaMalloc(&lens_d, 3 * sizeof(int32_t)));
+  CUDA(cudaMalloc(&out, 3 * row * sizeof(float)));
+  CUDA(cudaMalloc(&rec, 4 * sizeof(int32_t)));
+  CHECK(pa_error_clear(rec, nullptr));
+
+  CUDA(cudaMemcpy(k, k0.data(), k0.size() * sizeof(__half), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(v, v0.data(), v0.size() * sizeof(__half), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(slot_d, slots.data(), slots.size() * sizeof(int64_t), cudaMemcpyHostToDevice));
+  CHECK(kv_cache_append(k, v, slot_d, prompt + 1, kc, vc, kHeads, kDim, kBlock, kBlocks, PA_F16,
+                        rec, nullptr));
+
+  // Both holders of the shared partial block append the same new token: the
+  // fork first (it gets a private copy of that block), then the parent (now the
+  // sole holder, it writes in place).
+  int64_t slot1, slot0;
+  int32_t src, dst, src0, dst0;
+  CHECK(pa_seq_append(alloc, 1, &slot1, &src, &dst));
+  CHECK(pa_seq_append(alloc, 0, &slot0, &src0, &dst0));
+  if (src < 0 || src0 >= 0) {
+    std::fprintf(stderr, "expected exactly one copy-on-write (got %d, %d)\n", src, src0);
+    return 1;
+  }
+  const int64_t pair[2] = {src, dst};
+  CUDA(cudaMemcpy(pair_d, pair, sizeof(pair), cudaMemcpyHostToDevice));
+  void* kcs[1] = {kc};
+  void* vcs[1] = {vc};
+  CHECK(block_copy(kcs, vcs, 1, pair_d, 1, kHeads, kDim, kBlock, kBlocks, PA_F16, rec, nullptr));
+  const std::vector<__half> kn = random_rows(g, 1), vn = random_rows(g, 1);
+  const int64_t new_slots[2] = {slot1, slot0};
+  for (int i = 0; i < 2; ++i) {
+    CUDA(cudaMemcpy(k + i * row, kn.data(), row * sizeof(__half), cudaMemcpyHostToDevice));
+    CUDA(cudaMemcpy(v + i * row, vn.data(), row * sizeof(__half), cudaMemcpyHostToDevice));
+  }
+  CUDA(cudaMemcpy(slot_d, new_slots, sizeof(new_slots), cudaMemcpyHostToDevice));
+  CHECK(kv_cache_append(k, v, slot_d, 2, kc, vc, kHeads, kDim, kBlock, kBlocks, PA_F16, rec,
+                        nullptr));
+
+  // tables and lengths of sequences 0, 1, 2
+  std::vector<int32_t> tables(3 * kMaxBlocks, -1), lens(3);
+  for (int s = 0; s < 3; ++s) {
+    int32_t nb = 0;
+    CHECK(pa_seq_block_table(alloc, s, tables.data() + s * kMaxBlocks, kMaxBlocks, &nb));
+    CHECK(pa_seq_len(alloc, s, &lens[s]));
+  }
+  CUDA(cudaMemcpy(tables_d, tables.data(), tables.size() * 4, cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(lens_d, lens.data(), lens.size() * 4, cudaMemcpyHostToDevice));
+
+  // the same query for sequences 0 and 1
+  std::vector<__half> qh = random_rows(g, 3);
+  std::memcpy(qh.data() + row, qh.data(), row * sizeof(__half));
+  CUDA(cudaMemcpy(q, qh.data(), qh.size() * sizeof(__half), cudaMemcpyHostToDevice));
+  const size_t ws = paged_attn_workspace_size(3, kHeads, kDim, kBlock, kMaxBlocks, 0);
+  void* workspace = nullptr;
+  if (ws) CUDA(cudaMalloc(&workspace, ws));
+  CHECK(paged_attn_decode(q, kc, vc, tables_d, lens_d, 3, kHeads, kDim, kBlock, kMaxBlocks,
+                          kBlocks, 1.0f / 11.3137085f, PA_F16, out, PA_F32, 0, workspace, ws, rec,
+                          nullptr));
+  CUDA(cudaDeviceSynchronize());
+  int32_t err[4];
+  CHECK(pa_error_read(rec, err, nullptr));
+  if (err[0] != 0) {
+    std::fprintf(stderr, "device error record: %d %d %d %d\n", err[0], err[1], err[2], err[3]);
+    return 1;
+  }
+
+  std::vector<float> o(3 * row);
+  CUDA(cudaMemcpy(o.data(), out, o.size() * sizeof(float), cudaMemcpyDeviceToHost));
+  if (std::memcmp(o.data(), o.data() + row, row * sizeof(float)) != 0) {
+    std::fprintf(stderr, "forked sequence decodes differently from its parent\n");
+    return 1;
+  }
+  for (size_t i = 0; i < row; ++i) {
+    if (o[2 * row + i] != __half2float(v0[prompt * row + i])) {
+      std::fprintf(stderr, "one-token sequence: element %zu is %g, value row holds %g\n", i,
+                   o[2 * row + i], __half2float(v0[prompt * row + i]));
+      return 1;
+    }
+  }
+  CHECK(pa_alloc_check(alloc));
+  pa_alloc_destroy(alloc);
+  for (void* p : {static_cast<void*>(kc), static_cast<void*>(vc), static_cast<void*>(k),
+                  static_cast<void*>(v), static_cast<void*>(q), static_cast<void*>(slot_d),
+                  static_cast<void*>(pair_d), static_cast<void*>(tables_d),
+                  static_cast<void*>(lens_d), static_cast<void*>(out), static_cast<void*>(rec),
+                  workspace})
+    if (p) cudaFree(p);
+  std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact\n");
+  return 0;
+}
