@@ -767,6 +767,46 @@ def run_workload(args, rank, world, local_rank):
                         "note": "the append is fused into the decode launch"},
                     note="value counts logical K/V bytes (beams share prefix blocks, so part "
                          "of them is served from L2)")
+    elif w in ("append", "copy"):
+        # the two cache kernels at sizes where bandwidth matters: the K/V rows of a
+        # 16 x 512-token prefill chunk written into scattered slots, or 2000
+        # copy-on-write block pairs; both are pure copies, so the measured copy
+        # bandwidth is their roofline
+        H, D, bs = 40, 128, 16
+        g = WL.gen._torch_gen(8, dev)
+        rng = np.random.default_rng(8)
+        if w == "append":
+            T = 16 * 512
+            nb = int(1.5 * T / bs)
+            kc = torch.zeros((nb, H, bs, D), dtype=torch.bfloat16, device=dev)
+            vc = torch.zeros_like(kc)
+            k = WL.gen.randn_rounded((T, H, D), torch.bfloat16, g, dev)
+            v = WL.gen.randn_rounded((T, H, D), torch.bfloat16, g, dev)
+            slots = torch.from_numpy(rng.choice(nb * bs, size=T, replace=False)).to(dev)
+            fn = lambda: B.kv_cache_append(k, v, slots, kc, vc, error_record=rec)
+            moved = 2 * (2 * T * H * D * 2) + T * 8        # K and V read + written, slots
+            desc = f"KV append of a 16 x 512-token chunk ({T} tokens, 40 x 128, bf16) into scattered slots"
+            kernel = "kv_append_kernel"
+        else:
+            n_pairs, nb = 2000, 6000
+            kc = WL.gen.randn_rounded((nb, H, bs, D), torch.bfloat16, g, dev)
+            vc = WL.gen.randn_rounded((nb, H, bs, D), torch.bfloat16, g, dev)
+            pick = rng.choice(nb, size=2 * n_pairs, replace=False)
+            pairs = torch.from_numpy(np.stack([pick[:n_pairs], pick[n_pairs:]], 1)).to(dev)
+            fn = lambda: B.block_copy([kc], [vc], pairs, error_record=rec)
+            moved = 2 * (2 * n_pairs * H * bs * D * 2) + n_pairs * 16
+            desc = "copy-on-write block copy: 2000 pairs of 40 x 16 x 128 bf16 blocks (K and V)"
+            kernel = "block_copy_kernel"
+        ms = _time_device(fn, K, W, stream)
+        value = moved / (ms * 1e-3) / 1e9
+        tokens = 0
+        peak, peak_kind = measured_hbm_peak()
+        line.update(config={"workload": desc, "l2": "inputs larger than L2"}, dtype="bf16",
+                    roofline={"kernel": kernel, "bound": "hbm", "achieved": round(value, 2),
+                              "peak": peak, "unit": "GB/s", "frac": round(value / peak, 4),
+                              "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                              "algorithmic_bytes_per_launch": moved},
+                    note="value = bytes read + written per launch / device time")
     elif w == "prefill":
         # chunked prefill: 16 sequences append a 512-token chunk to contexts of 512..2048
         rng = np.random.default_rng(70)
@@ -925,7 +965,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="13b",
                     choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "beam",
-                             "prefill"],
+                             "prefill", "append", "copy"],
                     help="13b (default, the headline line) or another seeded workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
