@@ -28,6 +28,10 @@ import sys
 import tempfile
 import time
 
+# The CPU baseline reports the oracle on one core: keep numpy's BLAS (OpenBLAS) on
+# one thread.  It reads this when numpy is first imported, which is below.
+os.environ["OPENBLAS_NUM_THREADS"] = "1"
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

@@ -83,3 +83,15 @@ def test_clock_records_that_are_rejected():
     assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))          # locked low, no reason
     assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None,
                                       "reasons": ["nvidia-smi unavailable"]})
+
+
+def test_bench_keeps_the_oracle_on_one_blas_thread():
+    import subprocess
+    import sys
+    code = ("import bench, numpy as np; a = np.random.rand(3000, 256); "
+            "[a @ a.T for _ in range(3)]; "
+            "print([l for l in open('/proc/self/status') if l.startswith('Threads')][0].split()[1])")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "1"
