@@ -68,3 +68,37 @@ def test_fused_13b_full_size(B):
     assert torch.equal(fused, plain)
     assert_matches_oracle(fused[seqs], ref, "fused 13B")
 
+
+
+def test_bench_step_configuration(B):
+    """The step bench.py times, on the batch it times: 13B-shaped lengths (seed 2),
+    fused append, (sequence, partition) work items longest first, 512-token
+    partitions, bf16 output, partition pass then merge pass with a preallocated
+    workspace.  Sampled rows against the oracle; appended rows bit for bit."""
+    import numpy as np
+    from paged_kv_cache_317_gb300.binding import partition_work_items
+    b = decode_13b(seed=2, device="cuda", poison=False)
+    N, H, D, bs, MB, pt = b.num_seqs, b.num_heads, b.head_dim, b.block_size, \
+        b.max_blocks_per_seq, 512
+    lens = b.context_lens
+    seqs = sorted(set(range(0, N, 13)) | {int(np.argmax(lens)), int(np.argmin(lens))})
+    ref = oracle_decode(b, seqs)
+    bt = torch.from_numpy(b.block_tables).cuda()
+    sl = torch.from_numpy(lens).cuda()
+    items = torch.from_numpy(partition_work_items(
+        lens, pt, MB, bs, order=np.argsort(-lens, kind="stable"))).cuda()
+    out = torch.empty((N, H, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, MB, pt), dtype=torch.uint8,
+                     device="cuda")
+    rec = B.new_error_record()
+    for phases in (1, 2):
+        B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                   out=out, partition_tokens=pt, workspace=ws, error_record=rec,
+                                   phases=phases, work_items=items if phases == 1 else None)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    slots = torch.from_numpy(b.slot_mapping).cuda()
+    blk, row = slots // bs, slots % bs
+    assert torch.equal(b.k_cache[blk, :, row, :].view(torch.int16), b.new_k.view(torch.int16))
+    assert torch.equal(b.v_cache[blk, :, row, :].view(torch.int16), b.new_v.view(torch.int16))
+    assert_matches_oracle(out[seqs], ref, "bench step")
