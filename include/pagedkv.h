@@ -234,6 +234,23 @@ int paged_attn_prefill(const void* q, const int32_t* query_start, int total_quer
                        int num_blocks, float scale, int dtype, void* out, int out_dtype,
                        int32_t* error_record, void* stream);
 
+/* paged_attn_prefill with scheduling options (opts may be NULL).
+ *   seq_order  NULL, or device int32 [num_seqs]: a permutation of 0..num_seqs-1
+ *              giving the order in which sequences' blocks are dispatched (results
+ *              are identical, bit for bit).  Longest first shortens the ragged
+ *              tail.  An entry outside [0, num_seqs) is recorded as
+ *              PA_ERR_BAD_SEQ_LEN (index = position, value = entry) and skipped. */
+typedef struct pa_prefill_opts {
+  const int32_t* seq_order;
+} pa_prefill_opts;
+
+int paged_attn_prefill_ex(const void* q, const int32_t* query_start, int total_queries,
+                          int max_query_len, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                          int num_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                          int num_blocks, float scale, int dtype, void* out, int out_dtype,
+                          int32_t* error_record, void* stream, const pa_prefill_opts* opts);
+
 /* Decode without allocation.  No counterpart in the paper: this is a library
  * convenience.  Some callers cannot allocate device memory - code running
  * inside another runtime whose pool owns all device memory, a serving loop that

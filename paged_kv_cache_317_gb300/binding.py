@@ -32,6 +32,10 @@ STATUS = {
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 
+class pa_prefill_opts(ctypes.Structure):
+    _fields_ = [("seq_order", c_void_p)]
+
+
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
                 ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int)]
@@ -86,6 +90,9 @@ SIGNATURES = {
     "paged_attn_prefill": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                    c_float, c_int, c_void_p, c_int, c_void_p, c_void_p]),
+    "paged_attn_prefill_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                   c_float, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "paged_attn_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                           c_int, c_int, c_int, c_int, c_int, c_int, c_float,
                                           c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]),
@@ -269,8 +276,9 @@ def paged_attn_prefill(q: torch.Tensor, query_start: torch.Tensor, max_query_len
                        k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
                        seq_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                        out_dtype=torch.float32, error_record: Optional[torch.Tensor] = None,
-                       stream=None) -> torch.Tensor:
-    """Causal multi-query attention: q [total,H,D]; query_start int32 [N+1] (device)."""
+                       seq_order: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal multi-query attention: q [total,H,D]; query_start int32 [N+1] (device);
+    seq_order: optional int32 [N] dispatch order of the sequences on the device."""
     T, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     N = seq_lens.shape[0]
@@ -282,10 +290,14 @@ def paged_attn_prefill(q: torch.Tensor, query_start: torch.Tensor, max_query_len
     if out is None:
         out = torch.empty((T, H, D), dtype=out_dtype, device=q.device)
     _need(out, "out")
-    st = load_library().paged_attn_prefill(
+    if seq_order is not None:
+        _need(seq_order, "seq_order", torch.int32)
+    opts = pa_prefill_opts(None if seq_order is None else seq_order.data_ptr())
+    st = load_library().paged_attn_prefill_ex(
         _ptr(q), _ptr(query_start), T, int(max_query_len), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), _ptr(seq_lens), N, H, D, bs, block_tables.shape[1], B, float(scale),
-        _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(error_record), _stream(stream))
+        _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(error_record), _stream(stream),
+        ctypes.byref(opts))
     _check(st, "paged_attn_prefill")
     return out
 

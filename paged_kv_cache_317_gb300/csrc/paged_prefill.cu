@@ -105,6 +105,7 @@ struct Bars {
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct PrefillParams {
+  const int32_t* seq_order;  // optional dispatch order of the sequences
   const int32_t* query_start;
   const int32_t* seq_lens;
   const int32_t* block_tables;
@@ -266,8 +267,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using C = Cfg<D>;
-  const int qt = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int qt = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int seq = blockIdx.z;
+  if (p.seq_order != nullptr) {
+    seq = __ldg(p.seq_order + blockIdx.z);
+    if (static_cast<unsigned>(seq) >= gridDim.z) {
+      if (threadIdx.x == 0 && qt == 0 && h == 0)
+        report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.z, seq);
+      return;
+    }
+  }
 
   int L = p.seq_lens[seq];
   const int q_begin = p.query_start[seq];
@@ -680,6 +690,20 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
                                   int num_seqs, int num_heads, int head_dim, int block_size,
                                   int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                   void* out, int out_dtype, int32_t* error_record, void* stream) {
+  return paged_attn_prefill_ex(q, query_start, total_queries, max_query_len, k_cache, v_cache,
+                               block_tables, seq_lens, num_seqs, num_heads, head_dim,
+                               block_size, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                               out_dtype, error_record, stream, nullptr);
+}
+
+extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
+                                     int total_queries, int max_query_len, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* seq_lens, int num_seqs, int num_heads,
+                                     int head_dim, int block_size, int max_blocks_per_seq,
+                                     int num_blocks, float scale, int dtype, void* out,
+                                     int out_dtype, int32_t* error_record, void* stream,
+                                     const pa_prefill_opts* opts) {
   NvtxRange range("paged_attn_prefill");
   if (num_seqs < 0 || total_queries < 0 || max_query_len < 0 || num_heads <= 0 ||
       block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
@@ -719,6 +743,7 @@ extern "C" int paged_attn_prefill(const void* q, const int32_t* query_start, int
     return PA_ERR_CUDA;
 
   PrefillParams p{};
+  p.seq_order = opts ? opts->seq_order : nullptr;
   p.query_start = query_start;
   p.seq_lens = seq_lens;
   p.block_tables = block_tables;

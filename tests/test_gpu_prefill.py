@@ -186,3 +186,29 @@ def test_prefill_other_head_dims(B, D, dtype):
     again = _run(B, b, q, starts)
     torch.cuda.synchronize()
     assert torch.equal(out, again)
+
+
+def test_prefill_seq_order_changes_nothing_but_the_schedule(B):
+    rng = np.random.default_rng(99)
+    lens = rng.integers(200, 1500, size=9)
+    nq = np.minimum(lens, rng.integers(1, 300, size=9))
+    b, q, starts = _case(99, lens, nq, 4, 16, "bf16", poison=False)
+    plain = _run(B, b, q, starts)
+    for order in (np.argsort(-lens, kind="stable"), rng.permutation(9)):
+        got = B.paged_attn_prefill(q, torch.from_numpy(starts).cuda(), int(nq.max()), b.k_cache,
+                                   b.v_cache, torch.from_numpy(b.block_tables).cuda(),
+                                   torch.from_numpy(b.context_lens).cuda(), b.scale,
+                                   seq_order=torch.from_numpy(order.astype(np.int32)).cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(plain, got)
+    bad = torch.tensor([0, 1, 2, 3, 40, 5, 6, 7, 8], dtype=torch.int32, device="cuda")
+    rec = B.new_error_record()
+    out = torch.zeros_like(plain)
+    B.paged_attn_prefill(q, torch.from_numpy(starts).cuda(), int(nq.max()), b.k_cache, b.v_cache,
+                         torch.from_numpy(b.block_tables).cuda(),
+                         torch.from_numpy(b.context_lens).cuda(), b.scale, out=out,
+                         seq_order=bad, error_record=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [6, 1, 4, 40]
+    assert not out[starts[4]:starts[5]].any()                # sequence 4 was not dispatched
+    assert torch.equal(out[: starts[4]], plain[: starts[4]])
