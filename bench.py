@@ -260,10 +260,11 @@ def run_ours(args, rank, world, local_rank):
     B.load_library()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    b = decode_13b(seed=rank_seed(2, rank), device=dev, poison=False)
+    b = decode_13b(seed=rank_seed(args.seed, rank), device=dev, block_size=args.block_size,
+                   poison=False)
     N, H, D, bs = b.num_seqs, b.num_heads, b.head_dim, b.block_size
     MB = b.max_blocks_per_seq
-    pt = 512
+    pt = args.partition
     bt = torch.from_numpy(b.block_tables).to(dev)
     sl = torch.from_numpy(b.context_lens).to(dev)
     # The host knows the lengths it built the tables from: it lists the (sequence,
@@ -394,7 +395,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(b, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(b, budget_s=args.cpu_seconds, partition_tokens=pt)
 
     if rank == 0:
         line = {
@@ -411,6 +412,7 @@ def run_ours(args, rank, world, local_rank):
                 "context_tokens_per_gpu": int(b.context_lens.sum()),
                 "lengths": "lognormal(median 350, sigma 0.75) clipped to [16, 2048]",
                 "pool_blocks": b.num_blocks, "partition_tokens": pt, "out_dtype": "bf16",
+                "seed": args.seed,
                 "schedule": "(sequence, partition) work items holding tokens, longest "
                             "sequences first (work_items)",
                 "l2": "inputs larger than L2 (2.4 GB of K/V read per step); no flush",
@@ -867,30 +869,31 @@ def _oracle_sample(b, seqs):
     """Host inputs for the oracle on the listed sequences (outside any timing)."""
     import numpy as np
     import torch
-    used = sorted({int(x) for i in seqs for x in b.block_tables[i][: -(-int(b.context_lens[i]) // 16)]})
+    bs = b.block_size
+    used = sorted({int(x) for i in seqs for x in b.block_tables[i][: -(-int(b.context_lens[i]) // bs)]})
     remap = {x: j for j, x in enumerate(used)}
     idx = torch.tensor(used, dtype=torch.long, device=b.k_cache.device)
     to_bits = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
     kc, vc = to_bits(b.k_cache.index_select(0, idx)), to_bits(b.v_cache.index_select(0, idx))
     sel = torch.tensor(seqs, device=b.q.device)
-    tables = np.array([[remap[int(x)] for x in b.block_tables[i][: -(-int(b.context_lens[i]) // 16)]]
-                       + [-1] * (b.max_blocks_per_seq - (-(-int(b.context_lens[i]) // 16)))
+    tables = np.array([[remap[int(x)] for x in b.block_tables[i][: -(-int(b.context_lens[i]) // bs)]]
+                       + [-1] * (b.max_blocks_per_seq - (-(-int(b.context_lens[i]) // bs)))
                        for i in seqs], dtype=np.int64)
-    slots = np.array([remap[int(b.slot_mapping[i]) // 16] * 16 + int(b.slot_mapping[i]) % 16
+    slots = np.array([remap[int(b.slot_mapping[i]) // bs] * bs + int(b.slot_mapping[i]) % bs
                       for i in seqs], dtype=np.int64)
     return dict(q=to_bits(b.q[sel]), k=to_bits(b.new_k[sel]), v=to_bits(b.new_v[sel]), kc=kc,
-                vc=vc, tables=tables, lens=b.context_lens[seqs], slots=slots)
+                vc=vc, tables=tables, lens=b.context_lens[seqs], slots=slots, bs=bs)
 
 
 def _oracle_step(s, scale):
     from oracle import attention as OA
     from oracle import cache_ops as OC
     kc, vc = s["kc"].copy(), s["vc"].copy()
-    OC.kv_append(kc, vc, s["k"], s["v"], s["slots"], 16)
-    return OA.paged_decode_attention(s["q"], kc, vc, s["tables"], s["lens"], scale, 16, "bf16")
+    OC.kv_append(kc, vc, s["k"], s["v"], s["slots"], s["bs"])
+    return OA.paged_decode_attention(s["q"], kc, vc, s["tables"], s["lens"], scale, s["bs"], "bf16")
 
 
-def cpu_baseline(b, budget_s=15.0):
+def cpu_baseline(b, budget_s=15.0, partition_tokens=512):
     """The oracle, as it stands, on a bounded sample of the same batch (single thread)."""
     import numpy as np
     rng = np.random.default_rng(0)
@@ -906,7 +909,8 @@ def cpu_baseline(b, budget_s=15.0):
     t = time.perf_counter()
     _oracle_step(s, b.scale)
     dt = time.perf_counter() - t
-    nb = step_bytes(b.context_lens[seqs], b.num_heads, b.head_dim, b.block_size)
+    nb = step_bytes(b.context_lens[seqs], b.num_heads, b.head_dim, b.block_size,
+                    partition_tokens=partition_tokens)
     return {"value": round(nb["total"] / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "host_cpus": os.cpu_count(), "cpu_model": host_cpu_model(),
             "sample": f"{n} of {b.num_seqs} sequences (all heads), append + decode, "
@@ -923,7 +927,7 @@ def run_reference(args, rank, world, local_rank):
     from workloads import decode_13b
 
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    b = decode_13b(seed=2, device=device, poison=False)
+    b = decode_13b(seed=args.seed, device=device, block_size=args.block_size, poison=False)
     rng = np.random.default_rng(1)
     order = [int(i) for i in rng.permutation(b.num_seqs)]
     one = _oracle_sample(b, order[:1])
@@ -943,7 +947,8 @@ def run_reference(args, rank, world, local_rank):
         t = time.perf_counter()
         _oracle_step(s, b.scale)
         times.append(time.perf_counter() - t)
-        nbytes += step_bytes(s["lens"], b.num_heads, b.head_dim, b.block_size)["total"]
+        nbytes += step_bytes(s["lens"], b.num_heads, b.head_dim, b.block_size,
+                             partition_tokens=args.partition)["total"]
         tokens += float(np.sum(s["lens"]))
     total = sum(times)
     value = nbytes / total / 1e9
@@ -973,6 +978,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=2,
+                    help="13B-shaped batch: seed of the lengths and values (rank r uses a "
+                         "seed derived from it)")
+    ap.add_argument("--block-size", type=int, default=16, help="13B-shaped batch: tokens per block")
+    ap.add_argument("--partition", type=int, default=512,
+                    help="13B-shaped batch: split-K partition length in tokens")
     ap.add_argument("--workload", default="13b",
                     choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "beam",
                              "prefill", "append", "copy"],

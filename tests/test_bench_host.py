@@ -4,6 +4,7 @@ multi-rank reductions (two gloo ranks on 127.0.0.1)."""
 import os
 import socket
 
+import torch
 import torch.multiprocessing as mp
 
 import bench
@@ -95,3 +96,21 @@ def test_bench_keeps_the_oracle_on_one_blas_thread():
                          cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "1"
+
+
+def test_oracle_sample_follows_the_block_size():
+    import numpy as np
+    from oracle import attention as OA
+    from oracle import cache_ops as OC
+    from workloads import decode_13b
+    for bs in (16, 32):
+        b = decode_13b(seed=3, device="cpu", num_seqs=6, block_size=bs, poison=False)
+        seqs = [0, 2, 5]
+        got = bench._oracle_step(bench._oracle_sample(b, seqs), b.scale)
+        # the same step on the whole pool, without the compaction
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+        kc, vc = bits(b.k_cache), bits(b.v_cache)
+        OC.kv_append(kc, vc, bits(b.new_k), bits(b.new_v), b.slot_mapping, bs)
+        want = OA.paged_decode_attention(bits(b.q), kc, vc, b.block_tables, b.context_lens,
+                                         b.scale, bs, "bf16")[seqs]
+        assert np.array_equal(got, want)
