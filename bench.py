@@ -423,7 +423,10 @@ def run_ours(args, rank, world, local_rank):
                 "kernel": "paged_attn_partition_kernel", "bound": "hbm",
                 "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                "traffic": recorded_traffic("paged_attn_partition_kernel"),
+                # the recorded capture is of the default batch (seed 2, block 16, 512)
+                "traffic": (recorded_traffic("paged_attn_partition_kernel")
+                            if (args.seed, args.block_size, args.partition) == (2, 16, 512)
+                            else None),
                 "algorithmic_bytes_per_launch": nbytes["decode_partition"],
                 "avg_launch_ms": round(part_ms, 5),
             },
