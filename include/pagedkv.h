@@ -6,10 +6,10 @@
  * Serving with PagedAttention" (SOSP 2023).  Citations below name the web page
  * that restates it and the section on that page:
  *   [P1]  phantomic12.github.io, paper note, method paragraph
- *   [P3a] zeroshotmind.com, "Paging the cache"
- *   [P3b] zeroshotmind.com, "Block tables: logical order, physical scatter"
- *   [P3c] zeroshotmind.com, "Sharing a prefix without copying it"
- *   [P3d] zeroshotmind.com, "The fragmentation arithmetic"
+ *   [P3b] zeroshotmind.com, "Paging the cache"
+ *   [P3c] zeroshotmind.com, "Block tables: logical order, physical scatter"
+ *   [P3d] zeroshotmind.com, "Sharing a prefix without copying it"
+ *   [P3e] zeroshotmind.com, "The fragmentation arithmetic"
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -36,7 +36,7 @@
  *   32 bits).  May be NULL: checks still clamp/skip, nothing is recorded.
  * - Cache layout (one layer): k_cache and v_cache are each
  *   [num_blocks][num_heads][block_size][head_dim], contiguous, row-major.
- *   Slot s is row (s % block_size) of physical block (s / block_size) [P3a].
+ *   Slot s is row (s % block_size) of physical block (s / block_size) [P3b].
  * - dtypes: K/V/Q storage is PA_F16 or PA_BF16; outputs may also be PA_F32.
  *   All attention arithmetic is fp32.
  */
@@ -97,14 +97,14 @@ int pa_selftest_bounded_wait(int32_t* error_record, int arrive, unsigned long lo
                              void* stream);
 
 /* ---------------------------------------------------------------------------
- * Decode attention through a block table  [P1], [P3b]
+ * Decode attention through a block table  [P1], [P3c]
  *
  * For every sequence i and head h, with L = seq_lens[i]:
  *   token t (0 <= t < L) is row (t % block_size) of physical block
  *   block_tables[i * max_blocks_per_seq + t / block_size];
  *   s_t = scale * <q[i][h], k_t>,  out[i][h] = sum_t softmax(s)_t * v_t.
  * Attention walks the logical blocks in order; where they sit in the pool does
- * not matter [P3b].  L = 0 gives an all-zero output row.
+ * not matter [P3c].  L = 0 gives an all-zero output row.
  *
  * Arguments
  *   q             device, [num_seqs][num_heads][head_dim] in `dtype`, 16-byte aligned
@@ -181,7 +181,7 @@ int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache
                          int partition_tokens, void* workspace, size_t workspace_bytes,
                          int32_t* error_record, void* stream, const pa_decode_opts* opts);
 
-/* Fused KV append + decode  [P3b], [P3c]
+/* Fused KV append + decode  [P3c], [P3d]
  *
  * One decode step in one pass: for every sequence i with L = seq_lens[i] >= 1,
  * the token at position L - 1 is the one being appended.  Its rows new_k[i] and
@@ -276,7 +276,7 @@ int paged_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_
                               int partition_tokens, int32_t* error_record, void* stream);
 
 /* ---------------------------------------------------------------------------
- * KV append into slot-mapped blocks  [P3a]
+ * KV append into slot-mapped blocks  [P3b]
  *
  * For each token t < num_tokens with slot = slot_mapping[t] >= 0, and every head h:
  *   k_cache[slot / block_size][h][slot % block_size][:] = k[t][h][:]   (bit copy)
@@ -293,7 +293,7 @@ int kv_cache_append(const void* k, const void* v, const int64_t* slot_mapping, i
                     int num_blocks, int dtype, int32_t* error_record, void* stream);
 
 /* ---------------------------------------------------------------------------
- * Copy-on-write block copy  [P3c]
+ * Copy-on-write block copy  [P3d]
  *
  * For each pair j < num_pairs, (src, dst) = (pairs[2j], pairs[2j+1]), and each
  * layer l < num_layers: block dst of k_caches[l] and of v_caches[l] becomes a bit
@@ -313,17 +313,17 @@ int block_copy(void* const* k_caches, void* const* v_caches, int num_layers,
                int num_blocks, int dtype, int32_t* error_record, void* stream);
 
 /* ---------------------------------------------------------------------------
- * Host block allocator  [P1], [P3a], [P3c], [P3d]
+ * Host block allocator  [P1], [P3b], [P3d], [P3e]
  *
  * Host-only C++ (no device code, no CUDA calls).  Tracks, for a pool of
  * num_blocks blocks of block_size tokens: a free list, a reference count per
  * block, and per sequence (an int64 id) its block table and length.
  *  - A sequence holds exactly ceil(len / block_size) blocks, so at most
- *    block_size - 1 slots are unused, all in its last block [P3a], [P3d].
- *  - A block's reference count is the number of sequences holding it [P3c].
+ *    block_size - 1 slots are unused, all in its last block [P3b], [P3e].
+ *  - A block's reference count is the number of sequences holding it [P3d].
  *  - Appending into a partly filled last block that others also hold first
  *    moves the appender onto a fresh copy of that one block (copy-on-write):
- *    the call returns the (src, dst) pair for block_copy [P3c].
+ *    the call returns the (src, dst) pair for block_copy [P3d].
  *  - The free list is a stack.  Blocks are first handed out in `free_order`
  *    order (or 0, 1, 2, ... when NULL) and freed blocks go back on top.
  * An allocator object is not thread-safe; calls on distinct objects are
@@ -377,7 +377,7 @@ int pa_batch_free(pa_allocator* a, const int64_t* seqs, int32_t n);
  * does not fit. */
 int pa_batch_block_tables(const pa_allocator* a, const int64_t* seqs, int32_t n,
                           int32_t max_blocks, int32_t* tables, int32_t* seq_lens);
-/* Occupancy of the pool [P3a], [P3e].  All outputs optional (NULL to skip):
+/* Occupancy of the pool [P3b], [P3e].  All outputs optional (NULL to skip):
  *   blocks_used      blocks held by at least one sequence
  *   tokens_logical   sum of all sequences' lengths
  *   slots_logical    sum over sequences of ceil(len / block_size) * block_size
