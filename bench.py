@@ -42,6 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 PREFILL_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_prefill.cu",
                    "paged_kv_cache_317_gb300/csrc/common.cuh")
 DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_attn_decode.cu",
+                  "paged_kv_cache_317_gb300/csrc/decode_config.h",
                   "paged_kv_cache_317_gb300/csrc/common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
@@ -470,6 +471,36 @@ def _time_device(fn, K, W, stream, flush=None):
     return statistics.mean(times)
 
 
+def _time_graph(fns, K, W, stream, calls_per_graph=32):
+    """Mean device time per call, in ms, of the calls fns[0], fns[1], ... taken in
+    turn, captured into one CUDA graph of `calls_per_graph` calls and replayed
+    (after W warm-up replays) until at least K calls ran: what a serving loop
+    that captures its step sees, without the host's launch cost."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for j in range(calls_per_graph):
+            fns[j % len(fns)]()
+    for _ in range(W):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, -(-K // calls_per_graph))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (reps * calls_per_graph)
+
+
 def run_workload(args, rank, world, local_rank):
     """Device time of one step of the other seeded workloads (decode attention,
     plus the allocator, copies and appends where the workload has them)."""
@@ -523,6 +554,63 @@ def run_workload(args, rank, world, local_rank):
                     dtype="f16" if b.dtype == torch.float16 else "bf16")
         tokens = int(b.context_lens.sum())
         value = total / (ms * 1e-3) / 1e9
+    elif w == "small":
+        # small decode batches: 16 sequences (13B-shaped lengths: log-normal around 350,
+        # sigma 0.75, clipped to [16, 2048]), 40 heads x 128, bf16, fused append.  The
+        # split-K partition length and work list come from the host schedule
+        # (pa_decode_partition_tokens, pa_decode_work_items); a fixed 512 is timed
+        # beside it.  Four independent batches (0.44 GB of K/V) are called in turn so
+        # that each call's inputs have left L2, and the calls replay from a CUDA graph.
+        import numpy as np
+        H, D, bs = 40, 128, 16
+        batches = []
+        for j in range(4):
+            lens = WL.lognormal_lengths(np.random.default_rng(args.seed * 100 + j), 16, 350.0,
+                                        0.75, 16, 2048)
+            batches.append(WL.random_decode_batch(args.seed * 100 + j, lens, H, D, bs,
+                                                  dtype="bf16", device=dev, with_append=True,
+                                                  poison=False))
+
+        def calls(choose):
+            fns, pts = [], []
+            for b in batches:
+                pt = B.decode_partition_tokens(b.context_lens, H) if choose else 512
+                items = torch.from_numpy(B.partition_work_items(
+                    b.context_lens, pt, b.max_blocks_per_seq, bs)).to(dev)
+                bt = torch.from_numpy(b.block_tables).to(dev)
+                sl = torch.from_numpy(b.context_lens).to(dev)
+                out = torch.empty(b.q.shape, dtype=b.q.dtype, device=dev)
+                ws = torch.empty(max(16, B.paged_attn_workspace_size(
+                    b.num_seqs, H, D, bs, b.max_blocks_per_seq, pt)), dtype=torch.uint8,
+                    device=dev)
+                fns.append(lambda b=b, bt=bt, sl=sl, out=out, ws=ws, pt=pt, items=items:
+                           B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache,
+                                                      b.v_cache, bt, sl, b.scale, out=out,
+                                                      partition_tokens=pt, workspace=ws,
+                                                      error_record=rec, work_items=items))
+                pts.append(pt)
+            return fns, pts
+
+        fns, pts = calls(True)
+        ms = _time_graph(fns, K, W, stream)
+        fixed_ms = _time_graph(calls(False)[0], K, W, stream)
+        tokens = statistics.mean(int(b.context_lens.sum()) for b in batches)
+        total = statistics.mean(
+            step_bytes(b.context_lens, H, D, bs, partition_tokens=p)["total"]
+            for b, p in zip(batches, pts))
+        value = total / (ms * 1e-3) / 1e9
+        line.update(config={"workload": "small decode batches: 16 seqs, lengths lognormal("
+                                        "median 350, sigma 0.75) clipped to [16, 2048], 40 "
+                                        "heads x 128, bf16, block 16, fused append",
+                            "batches": len(batches), "context_tokens": tokens,
+                            "partition_tokens": pts,
+                            "schedule": "host-chosen partition length and work list",
+                            "timing": "CUDA graph of 32 calls, replayed",
+                            "l2": "four batches in turn, 0.44 GB of K/V (inputs larger "
+                                  "than L2)"},
+                    dtype="bf16",
+                    fixed_partition_512={"ms_per_step": round(fixed_ms, 5),
+                                         "speedup_of_schedule": round(fixed_ms / ms, 3)})
     elif w == "sampling":
         plan = WL.parallel_sampling(device=dev)
         S, bs = plan.samples, plan.block_size
@@ -988,8 +1076,8 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=512,
                     help="13B-shaped batch: split-K partition length in tokens")
     ap.add_argument("--workload", default="13b",
-                    choices=["13b", "tiny", "long16", "long32", "sampling", "mixed", "beam",
-                             "prefill", "append", "copy"],
+                    choices=["13b", "tiny", "small", "long16", "long32", "sampling", "mixed",
+                             "beam", "prefill", "append", "copy"],
                     help="13b (default, the headline line) or another seeded workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -205,6 +205,49 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
                              size_t workspace_bytes, int32_t* error_record, void* stream,
                              const pa_decode_opts* opts);
 
+/* Decode schedule, host side  [P3c]
+ *
+ * The host holds every sequence's length (it builds the block tables), so it
+ * can shape a decode launch to the batch: pick the split-K partition length and
+ * list the (sequence, partition) work items.  Both functions are host code only:
+ * they read host arrays, write host arrays and enqueue nothing.  Results feed
+ * paged_attn_workspace_size, partition_tokens and pa_decode_opts.work_items of
+ * paged_attn_decode_ex / paged_attn_decode_append; the outputs of the decode are
+ * the same whatever is chosen, up to fp32 rounding order across partitions.
+ *
+ * pa_decode_partition_tokens: writes to *partition_tokens the longest of 512,
+ * 256 and 128 for which the heaviest block, min(partition, max_i L_i) tokens,
+ * is at most 1/3.5 of the average work per SM, sum_i L_i * num_heads /
+ * heads_per_cta / num_sms; else 64.  A batch with a lot of work per SM keeps 512;
+ * a few short sequences get short partitions so that every SM has blocks.
+ *   seq_lens       host int32 [num_seqs], the lengths the decode will see (for
+ *                  the fused append: including the appended token); each >= 0
+ *   heads_per_cta  as in pa_decode_opts (0 = the automatic choice)
+ *   num_sms        SMs of the device the decode runs on; 0 = ask the current
+ *                  CUDA device (PA_ERR_CUDA if that fails)
+ * Returns PA_OK, or PA_ERR_INVALID_ARG (a negative length, heads_per_cta not
+ * dividing num_heads or above 8, NULL pointers) with nothing written.
+ *
+ * pa_decode_work_items: the work list item = i * P + p for every sequence i,
+ * taken in `order`, and every partition p < max(1, ceil(L_i / partition_tokens)),
+ * partitions of a sequence in increasing order; P = ceil(max_blocks_per_seq *
+ * block_size / partition_tokens).  A sequence with L_i = 0 keeps one item, which
+ * writes its zero output row.
+ *   partition_tokens  0 = 512 (the decode's automatic length), else a positive
+ *                  multiple of 16; must equal the decode call's
+ *   order          host int32 [num_seqs], a permutation of 0..num_seqs-1; or NULL
+ *                  for longest first (equal lengths in index order)
+ *   items          host int32 [capacity], or NULL to only count
+ *   num_items      out: the number of items (the decode accepts at most 65535)
+ * Returns PA_OK; PA_ERR_INVALID_ARG (a length outside [0, max_blocks_per_seq *
+ * block_size], `order` not a permutation, capacity below the count: *num_items
+ * still holds the count, items untouched). */
+int pa_decode_partition_tokens(const int32_t* seq_lens, int num_seqs, int num_heads,
+                               int heads_per_cta, int num_sms, int32_t* partition_tokens);
+int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int partition_tokens,
+                         int max_blocks_per_seq, int block_size, const int32_t* order,
+                         int32_t* items, int32_t capacity, int32_t* num_items);
+
 /* Chunked prefill / multi-query attention through the block table  [P1], [P3c]
  *
  * Several query tokens per sequence, on the tensor cores (tcgen05).  Sequence i

@@ -28,6 +28,7 @@ SOURCES = [
     "block_copy.cu",
     "api.cu",
     "allocator.cpp",
+    "decode_schedule.cpp",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3", "-I", INCLUDE, "-I", CSRC,

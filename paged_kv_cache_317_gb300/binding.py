@@ -52,19 +52,48 @@ def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items):
                           0 if work_items is None else int(work_items.numel()))
 
 
+def _host_int32(values, name: str) -> "np.ndarray":
+    import numpy as np
+    a = np.asarray(values, dtype=np.int64).reshape(-1)
+    if a.size and (a.min() < -2**31 or a.max() >= 2**31):
+        raise ValueError(f"{name}: values do not fit int32")
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def decode_partition_tokens(seq_lens, num_heads: int, heads_per_cta: int = 0,
+                            num_sms: int = 0) -> int:
+    """Split-K partition length for a decode over these (host) lengths, chosen by
+    pa_decode_partition_tokens: 512 for batches with plenty of work per SM, down
+    to 64 for a few short sequences.  num_sms 0 asks the current device."""
+    lens = _host_int32(seq_lens, "seq_lens")
+    out = ctypes.c_int32()
+    _check(load_library().pa_decode_partition_tokens(
+        lens.ctypes.data_as(P_int32), len(lens), num_heads, heads_per_cta, num_sms,
+        ctypes.byref(out)), "pa_decode_partition_tokens")
+    return out.value
+
+
 def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: int,
                          block_size: int, order=None) -> "np.ndarray":
-    """Host helper: the (sequence, partition) items that hold tokens, item =
-    i * P + p, in the given sequence order (default: longest first)."""
+    """The (sequence, partition) work list of a decode launch, item = i * P + p,
+    sequences in the given order (default: longest first); built by
+    pa_decode_work_items."""
     import numpy as np
-    lens = np.asarray(seq_lens, dtype=np.int64)
-    pt = partition_tokens if partition_tokens > 0 else 512
-    P = max(1, -(-max_blocks_per_seq * block_size // pt))
-    order = np.argsort(-lens, kind="stable") if order is None else np.asarray(order, np.int64)
-    nparts = np.maximum(1, -(-lens[order] // pt))
-    first = np.repeat(np.cumsum(nparts) - nparts, nparts)
-    part = np.arange(int(nparts.sum()), dtype=np.int64) - first
-    return (np.repeat(order, nparts) * P + part).astype(np.int32)
+    lens = _host_int32(seq_lens, "seq_lens")
+    ordp = None
+    if order is not None:
+        ordarr = _host_int32(order, "order")
+        if ordarr.shape != lens.shape:
+            raise ValueError("order must hold one entry per sequence")
+        ordp = ordarr.ctypes.data_as(P_int32)
+    lib, n = load_library(), ctypes.c_int32()
+    args = (lens.ctypes.data_as(P_int32), len(lens), partition_tokens, max_blocks_per_seq,
+            block_size, ordp)
+    _check(lib.pa_decode_work_items(*args, None, 0, ctypes.byref(n)), "pa_decode_work_items")
+    items = np.empty(n.value, dtype=np.int32)
+    _check(lib.pa_decode_work_items(*args, items.ctypes.data_as(P_int32), n.value,
+                                    ctypes.byref(n)), "pa_decode_work_items")
+    return items
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
@@ -100,6 +129,9 @@ SIGNATURES = {
                                 c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "block_copy": (c_int, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int, c_void_p,
                            c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "pa_decode_partition_tokens": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32]),
+    "pa_decode_work_items": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32, P_int32,
+                                     c_int32, P_int32]),
     "pa_alloc_create": (c_void_p, [c_int32, c_int32, P_int32]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_seq_add": (c_int, [c_void_p, c_int64, c_int32]),

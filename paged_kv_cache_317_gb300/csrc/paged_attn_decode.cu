@@ -33,15 +33,14 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "decode_config.h"
 
 namespace pagedkv {
 namespace {
 
 constexpr int kChunk = 16;           // tokens per pipeline stage and head
 constexpr int kHeaderBytes = 256;    // mbarriers + abort flag at the front of shared memory
-constexpr int kMaxHeadsPerCta = 8;
 constexpr int kMaxStages = 8;
-constexpr int kDefaultPartition = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -477,12 +476,6 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem, cudaStr
   }
   return PA_OK;
 }
-
-// Two heads per block and two stages keep each block at ~32 KB of shared
-// memory, so six blocks (twelve consumer warps) share an SM: measured on GB300,
-// more resident consumer warps beat deeper pipelines, because each warp's
-// per-chunk work is a chain of dependent shuffles and exponentials.
-int auto_heads_per_cta(int num_heads) { return num_heads % 2 == 0 ? 2 : 1; }
 
 }  // namespace
 }  // namespace pagedkv

@@ -1,6 +1,7 @@
 // A decode step driven through the C ABI alone (include/pagedkv.h and
 // libpagedkv.so; no Python): host allocator, KV append, copy-on-write block
-// copy and paged decode attention.  It checks two exact properties:
+// copy, the host decode schedule and paged decode attention.  It checks two
+// exact properties:
 //  * a sequence forked from another and given the same next token decodes to
 //    the same bits as its parent, although its last block is a private copy;
 //  * a one-token sequence returns its value row exactly (one weight of 1).
@@ -138,12 +139,27 @@ int main() {
   std::vector<__half> qh = random_rows(g, 3);
   std::memcpy(qh.data() + row, qh.data(), row * sizeof(__half));
   CUDA(cudaMemcpy(q, qh.data(), qh.size() * sizeof(__half), cudaMemcpyHostToDevice));
-  const size_t ws = paged_attn_workspace_size(3, kHeads, kDim, kBlock, kMaxBlocks, 0);
+  // split-K partition length and (sequence, partition) work list from the host
+  // lengths: a batch this small gets short partitions, so the split path runs
+  int32_t pt = 0, n_items = 0;
+  CHECK(pa_decode_partition_tokens(lens.data(), 3, kHeads, 0, 0, &pt));
+  CHECK(pa_decode_work_items(lens.data(), 3, pt, kMaxBlocks, kBlock, nullptr, nullptr, 0,
+                             &n_items));
+  std::vector<int32_t> items(n_items);
+  CHECK(pa_decode_work_items(lens.data(), 3, pt, kMaxBlocks, kBlock, nullptr, items.data(),
+                             n_items, &n_items));
+  int32_t* items_d = nullptr;
+  CUDA(cudaMalloc(&items_d, items.size() * sizeof(int32_t)));
+  CUDA(cudaMemcpy(items_d, items.data(), items.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  pa_decode_opts opts{};
+  opts.work_items = items_d;
+  opts.num_work_items = n_items;
+  const size_t ws = paged_attn_workspace_size(3, kHeads, kDim, kBlock, kMaxBlocks, pt);
   void* workspace = nullptr;
   if (ws) CUDA(cudaMalloc(&workspace, ws));
-  CHECK(paged_attn_decode(q, kc, vc, tables_d, lens_d, 3, kHeads, kDim, kBlock, kMaxBlocks,
-                          kBlocks, 1.0f / 11.3137085f, PA_F16, out, PA_F32, 0, workspace, ws, rec,
-                          nullptr));
+  CHECK(paged_attn_decode_ex(q, kc, vc, tables_d, lens_d, 3, kHeads, kDim, kBlock, kMaxBlocks,
+                             kBlocks, 1.0f / 11.3137085f, PA_F16, out, PA_F32, pt, workspace, ws,
+                             rec, nullptr, &opts));
   CUDA(cudaDeviceSynchronize());
   int32_t err[4];
   CHECK(pa_error_read(rec, err, nullptr));
@@ -171,8 +187,9 @@ int main() {
                   static_cast<void*>(v), static_cast<void*>(q), static_cast<void*>(slot_d),
                   static_cast<void*>(pair_d), static_cast<void*>(tables_d),
                   static_cast<void*>(lens_d), static_cast<void*>(out), static_cast<void*>(rec),
-                  workspace})
+                  static_cast<void*>(items_d), workspace})
     if (p) cudaFree(p);
-  std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact\n");
+  std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact; "
+              "%d-token partitions, %d work items\n", pt, n_items);
   return 0;
 }

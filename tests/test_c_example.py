@@ -35,3 +35,4 @@ def test_c_example_runs(lib, tmp_path):
     r = subprocess.run([_build(tmp_path)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "ok:" in r.stdout
+    assert "64-token partitions" in r.stdout        # the split path with a work list

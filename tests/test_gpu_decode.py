@@ -280,3 +280,23 @@ def test_bad_work_item_is_recorded_and_skipped(B):
     assert B.pa_error_read(rec) == [6, 1, 1, 3 * P + 5]
     assert_matches_oracle(out[[0, 2]], oracle_decode(b, [0, 2]), "valid items")
     assert not out[1].any()
+
+
+@pytest.mark.parametrize("lens", [[1500], [900, 3, 2048, 40], [1, 17, 64, 65, 300] * 8,
+                                  [700] * 40 + [5, 2000]])
+def test_host_schedule_matches_oracle(B, lens):
+    """The partition length and work list the host schedule picks (short partitions
+    for small batches) give the oracle's outputs, fused append included."""
+    b = random_decode_batch(31 + len(lens), lens, 8, 128, 16, dtype="bf16", device="cuda",
+                            with_append=True)
+    pt = B.decode_partition_tokens(b.context_lens, 8)
+    assert pt in (64, 128, 256, 512)
+    items = B.partition_work_items(b.context_lens, pt, b.max_blocks_per_seq, 16)
+    bt, sl = device_tables(b)
+    rec = B.new_error_record()
+    out = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl,
+                                     b.scale, out_dtype=torch.float32, partition_tokens=pt,
+                                     work_items=torch.from_numpy(items).cuda(), error_record=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert_matches_oracle(out, oracle_decode(b), f"host schedule pt {pt}")
