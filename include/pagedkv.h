@@ -117,7 +117,8 @@ int pa_selftest_bounded_wait(int32_t* error_record, int arrive, unsigned long lo
  *   scale         the softmax scale, usually 1/sqrt(head_dim)
  *   out           device [num_seqs][num_heads][head_dim] in `out_dtype`, 16-byte aligned
  *   partition_tokens  split-K partition length: 0 = automatic (512); otherwise a
- *                 positive multiple of 16.  When max_blocks_per_seq * block_size
+ *                 positive multiple of 16 (pa_decode_partition_tokens chooses one
+ *                 from the host's lengths).  When max_blocks_per_seq * block_size
  *                 fits in one partition, a single pass writes `out` directly.
  *                 Otherwise a first kernel computes per-partition partials and a
  *                 second merges them by log-sum-exp.
@@ -217,9 +218,10 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  *
  * pa_decode_partition_tokens: writes to *partition_tokens the longest of 512,
  * 256 and 128 for which the heaviest block, min(partition, max_i L_i) tokens,
- * is at most 1/3.5 of the average work per SM, sum_i L_i * num_heads /
- * heads_per_cta / num_sms; else 64.  A batch with a lot of work per SM keeps 512;
- * a few short sequences get short partitions so that every SM has blocks.
+ * is at most 1/c of the average work per SM, sum_i L_i * num_heads /
+ * heads_per_cta / num_sms, with c = 3.5 for 512 and 256 and c = 2 for 128; else
+ * 64.  A batch with a lot of work per SM keeps 512; a few short sequences get
+ * short partitions so that every SM has blocks.
  *   seq_lens       host int32 [num_seqs], the lengths the decode will see (for
  *                  the fused append: including the appended token); each >= 0
  *   heads_per_cta  as in pa_decode_opts (0 = the automatic choice)

@@ -15,21 +15,25 @@
 
 namespace {
 
-// Candidate partition lengths, longest first.  Shorter partitions add merge
-// work and per-block start-up cost, so the longest one that balances is best.
-constexpr int kCandidates[] = {512, 256, 128};
-constexpr int kShortest = 64;
-
-// Balance rule: the heaviest block (min(partition, longest length) tokens of
-// heads_per_cta heads) must be at most 1/3.5 of the work an SM gets on average
-// (total tokens x heads / heads_per_cta, over the SMs).  Then every SM holds
-// several blocks' worth of work and the last block to start does not set the
-// launch's length.  Measured on GB300 with CUDA-graph replays over 30 batches
+// Candidate partition lengths, longest first, each with its balance constant
+// c: a candidate is taken when the heaviest block (min(partition, longest
+// length) tokens of heads_per_cta heads) is at most 1/c of the work an SM gets
+// on average (total tokens x heads / heads_per_cta, over the SMs).  Then every
+// SM holds several blocks' worth of work and the last block to start does not
+// set the launch's length.  Shorter partitions add merge work and per-block
+// start-up cost, so the longest one that balances is best; a 128-token block
+// is cheap enough to start that it needs less balance (c = 2) than the longer
+// ones (c = 3.5).  Measured on GB300 with CUDA-graph replays over 39 batches
 // (1 to 512 sequences, medians of 30 to 30000 tokens, 40 heads x 128): on
-// average within 1.3 % of the best of 32..512 for each batch, at worst 13 %
+// average within 1.1 % of the best of 32..512 for each batch, at worst 13 %
 // (a 10 us call over 2 short sequences), where a fixed 512 is up to 2.4x slower
-// on batches of 1 to 24 sequences.  The constant is flat between 3 and 3.5.
-constexpr long long kBalanceNum = 7, kBalanceDen = 2;  // 3.5
+// on batches of 1 to 24 sequences.
+struct Candidate {
+  int tokens;
+  long long num, den;  // c = num / den
+};
+constexpr Candidate kCandidates[] = {{512, 7, 2}, {256, 7, 2}, {128, 2, 1}};
+constexpr int kShortest = 64;
 
 bool valid_partition(int pt) { return pt > 0 && pt % 16 == 0; }
 
@@ -59,10 +63,10 @@ extern "C" int pa_decode_partition_tokens(const int32_t* seq_lens, int num_seqs,
     longest = std::max(longest, static_cast<int>(seq_lens[i]));
   }
   const long long work = tokens * (num_heads / G);
-  for (int pt : kCandidates) {
-    const long long heaviest = std::min(pt, longest);
-    if (kBalanceNum * heaviest * num_sms <= kBalanceDen * work) {
-      *partition_tokens = pt;
+  for (const Candidate& c : kCandidates) {
+    const long long heaviest = std::min(c.tokens, longest);
+    if (c.num * heaviest * num_sms <= c.den * work) {
+      *partition_tokens = c.tokens;
       return PA_OK;
     }
   }

@@ -14,8 +14,8 @@ def rule(lens, num_heads, heads_per_cta, num_sms):
     G = heads_per_cta or (2 if num_heads % 2 == 0 else 1)
     work = int(np.sum(lens)) * (num_heads // G)
     longest = int(np.max(lens)) if len(lens) else 0
-    for pt in (512, 256, 128):
-        if min(pt, longest) * num_sms * 3.5 <= work:
+    for pt, c in ((512, 3.5), (256, 3.5), (128, 2.0)):
+        if min(pt, longest) * num_sms * c <= work:
             return pt
     return 64
 
@@ -46,6 +46,9 @@ def test_partition_choice_at_the_ends():
     # (7 x 512 tokens x 2 heads = 3.5 x 4 SMs x 512)
     assert B.decode_partition_tokens([512] * 7, 2, 1, 4) == 512
     assert B.decode_partition_tokens([512] * 6, 2, 1, 4) == 256
+    # 128 needs only half the work per SM: 2 x 4 SMs x 128 = 1024 = 4 x 128 x 2 heads
+    assert B.decode_partition_tokens([128] * 4, 2, 1, 4) == 128
+    assert B.decode_partition_tokens([128] * 3, 2, 1, 4) == 64
 
 
 def test_partition_choice_rejects_bad_arguments():
