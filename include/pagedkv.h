@@ -50,8 +50,10 @@
 extern "C" {
 #endif
 
-#define PAGEDKV_VERSION 1
+#define PAGEDKV_VERSION 2
 #define PA_ERROR_RECORD_WORDS 4
+#define PA_SHARE_MAX_MEMBERS 16
+#define PA_SHARE_RECORD_WORDS (2 + PA_SHARE_MAX_MEMBERS)
 
 typedef enum pa_status {
   PA_OK = 0,
@@ -158,6 +160,26 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  pair must appear exactly once for `out` to be complete.  An
  *                  item outside [0, num_seqs * P) is recorded as PA_ERR_BAD_SEQ_LEN
  *                  (index = position, value = item) and skipped.  At most 65535.
+ *   shared_records NULL, or device int32 [num_shared][PA_SHARE_RECORD_WORDS]:
+ *                  partitions that several sequences share [P3d].  Record r =
+ *                  {p, m, s_0, ..., s_{m-1}, unused...}: partition p of the m
+ *                  (1..PA_SHARE_MAX_MEMBERS) member sequences s_j, whose block
+ *                  tables name the same physical blocks over that partition.  One
+ *                  thread block per (record, head pair) reads each K/V chunk once
+ *                  for all members' queries (mma.sync, P as high + low half-
+ *                  precision parts, fp32 accumulation) and writes every member's
+ *                  partial for partition p, or its output row when p is its only
+ *                  partition.  Blocks are looked up in s_0's table only.  Each
+ *                  member must cover the whole partition: (p + 1) *
+ *                  partition_tokens <= L (<= L - 1 for paged_attn_decode_append,
+ *                  whose appended token must lie past it).  A record that breaks
+ *                  these rules is recorded as PA_ERR_BAD_SEQ_LEN (index = record,
+ *                  value = the offending field) and skipped.  Requires work_items
+ *                  (the pairs not covered by a record; when there are none, any
+ *                  non-NULL pointer with num_work_items = 0); every pair that
+ *                  holds tokens must appear exactly once across both.  At most
+ *                  65535 records.
+ *                  pa_decode_share_plan builds both lists.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -173,6 +195,8 @@ typedef struct pa_decode_opts {
   const int32_t* seq_order;
   const int32_t* work_items;
   int num_work_items;
+  const int32_t* shared_records;
+  int num_shared;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -249,6 +273,30 @@ int pa_decode_partition_tokens(const int32_t* seq_lens, int num_seqs, int num_he
 int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int partition_tokens,
                          int max_blocks_per_seq, int block_size, const int32_t* order,
                          int32_t* items, int32_t capacity, int32_t* num_items);
+
+/* pa_decode_share_plan: the work list and shared-partition records of a decode
+ * over sequences that share blocks [P3d] (parallel samples, beam candidates).
+ * For each partition p, the sequences that hold all of it ((p + 1) *
+ * partition_tokens <= L_i, or <= L_i - 1 with fused_append) and whose block
+ * tables name the same blocks over it are grouped, PA_SHARE_MAX_MEMBERS at most
+ * per record; a group of one stays in the work list.  The work list holds every
+ * other (sequence, partition) pair as in pa_decode_work_items (same order).
+ * Records come partition by partition; unused member slots are -1.
+ *   block_tables   host int32 [num_seqs][max_blocks_per_seq], the tables the
+ *                  decode will read (entries past a sequence's blocks are not read)
+ *   seq_lens, order, partition_tokens  as for pa_decode_work_items
+ *   fused_append   nonzero when the plan feeds paged_attn_decode_append
+ *   work_items     host int32 [items_capacity]; records: host int32
+ *                  [records_capacity][PA_SHARE_RECORD_WORDS]; both NULL to count
+ *   num_items, num_records  out: the counts
+ * Returns PA_OK or PA_ERR_INVALID_ARG (as for pa_decode_work_items, or a
+ * capacity below a count: the counts are still written, the arrays untouched).
+ * Host work: one pass over the table entries of every shareable partition. */
+int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                         int max_blocks_per_seq, int block_size, int partition_tokens,
+                         int fused_append, const int32_t* order, int32_t* work_items,
+                         int32_t items_capacity, int32_t* num_items, int32_t* records,
+                         int32_t records_capacity, int32_t* num_records);
 
 /* Chunked prefill / multi-query attention through the block table  [P1], [P3c]
  *

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(PKG, "libpagedkv.so")
 SOURCES = [
     "paged_attn_decode.cu",
     "paged_attn_decode_noalloc.cu",
+    "paged_attn_shared.cu",
     "paged_prefill.cu",
     "kv_cache_append.cu",
     "block_copy.cu",

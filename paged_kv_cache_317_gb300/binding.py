@@ -38,18 +38,32 @@ class pa_prefill_opts(ctypes.Structure):
 
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
-                ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int)]
+                ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int),
+                ("shared_records", c_void_p), ("num_shared", c_int)]
 
 
-def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items):
+PA_SHARE_MAX_MEMBERS = 16
+PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
+
+
+def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_records=None):
     if seq_order is not None:
         _need(seq_order, "seq_order", torch.int32)
     if work_items is not None:
         _need(work_items, "work_items", torch.int32)
+    if shared_records is not None:
+        _need(shared_records, "shared_records", torch.int32)
+        if shared_records.dim() != 2 or shared_records.shape[1] != PA_SHARE_RECORD_WORDS:
+            raise ValueError(f"shared_records must be [n, {PA_SHARE_RECORD_WORDS}]")
+    items_ptr = None if work_items is None else work_items.data_ptr()
+    if work_items is not None and not items_ptr and shared_records is not None:
+        items_ptr = shared_records.data_ptr() or None   # an empty list still counts as given
     return pa_decode_opts(heads_per_cta, stages, phases,
                           None if seq_order is None else seq_order.data_ptr(),
-                          None if work_items is None else work_items.data_ptr(),
-                          0 if work_items is None else int(work_items.numel()))
+                          items_ptr,
+                          0 if work_items is None else int(work_items.numel()),
+                          None if shared_records is None else shared_records.data_ptr(),
+                          0 if shared_records is None else int(shared_records.shape[0]))
 
 
 def _host_int32(values, name: str) -> "np.ndarray":
@@ -96,6 +110,37 @@ def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: in
     return items
 
 
+def share_plan(block_tables, seq_lens, partition_tokens: int, block_size: int,
+               fused_append: bool = True, order=None):
+    """Work list and shared-partition records (pa_decode_share_plan) for a decode
+    over host tables [N, max_blocks] and lengths: (work_items int32 [n],
+    shared_records int32 [r, PA_SHARE_RECORD_WORDS])."""
+    import numpy as np
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    if tables.ndim != 2:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    lens = _host_int32(seq_lens, "seq_lens")
+    if len(lens) != tables.shape[0]:
+        raise ValueError("one length per table row")
+    ordp = None
+    if order is not None:
+        ordarr = _host_int32(order, "order")
+        if ordarr.shape != lens.shape:
+            raise ValueError("order must hold one entry per sequence")
+        ordp = ordarr.ctypes.data_as(P_int32)
+    lib, ni, nr = load_library(), ctypes.c_int32(), ctypes.c_int32()
+    args = (tables.ctypes.data_as(P_int32), lens.ctypes.data_as(P_int32), len(lens),
+            tables.shape[1], block_size, partition_tokens, int(bool(fused_append)), ordp)
+    _check(lib.pa_decode_share_plan(*args, None, 0, ctypes.byref(ni), None, 0,
+                                    ctypes.byref(nr)), "pa_decode_share_plan")
+    items = np.empty(ni.value, dtype=np.int32)
+    recs = np.empty((nr.value, PA_SHARE_RECORD_WORDS), dtype=np.int32)
+    _check(lib.pa_decode_share_plan(*args, items.ctypes.data_as(P_int32), ni.value,
+                                    ctypes.byref(ni), recs.ctypes.data_as(P_int32), nr.value,
+                                    ctypes.byref(nr)), "pa_decode_share_plan")
+    return items, recs
+
+
 # name -> (restype, argtypes); mirrors include/pagedkv.h
 SIGNATURES = {
     "pa_version": (c_int, []),
@@ -132,6 +177,9 @@ SIGNATURES = {
     "pa_decode_partition_tokens": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32]),
     "pa_decode_work_items": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32, P_int32,
                                      c_int32, P_int32]),
+    "pa_decode_share_plan": (c_int, [P_int32, P_int32, c_int, c_int, c_int, c_int, c_int,
+                                     P_int32, P_int32, c_int32, P_int32, P_int32, c_int32,
+                                     P_int32]),
     "pa_alloc_create": (c_void_p, [c_int32, c_int32, P_int32]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_seq_add": (c_int, [c_void_p, c_int64, c_int32]),
@@ -240,10 +288,14 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                       error_record: Optional[torch.Tensor] = None, heads_per_cta: int = 0,
                       stages: int = 0, phases: int = 0, seq_order: Optional[torch.Tensor] = None,
-                      work_items: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                      work_items: Optional[torch.Tensor] = None,
+                      shared_records: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
     """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
     seq_order: optional int32 [N] scheduling permutation on the device; work_items:
-    optional int32 list of (sequence * P + partition) on the device."""
+    optional int32 list of (sequence * P + partition) on the device; shared_records:
+    optional int32 [r, PA_SHARE_RECORD_WORDS] shared partitions on the device
+    (share_plan builds both)."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -258,7 +310,8 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items)
+    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
+                        shared_records)
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -276,6 +329,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              stages: int = 0, phases: int = 0,
                              seq_order: Optional[torch.Tensor] = None,
                              work_items: Optional[torch.Tensor] = None,
+                             shared_records: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
@@ -294,7 +348,8 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items)
+    opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
+                        shared_records)
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),

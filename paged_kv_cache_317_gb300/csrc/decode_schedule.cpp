@@ -7,7 +7,9 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <numeric>
+#include <unordered_map>
 #include <vector>
 
 #include "decode_config.h"
@@ -36,6 +38,28 @@ constexpr Candidate kCandidates[] = {{512, 7, 2}, {256, 7, 2}, {128, 2, 1}};
 constexpr int kShortest = 64;
 
 bool valid_partition(int pt) { return pt > 0 && pt % 16 == 0; }
+
+// Sequence indices in launch order: `order` if given (checked to be a
+// permutation), else longest first with equal lengths in index order.
+bool launch_order(const int32_t* seq_lens, int num_seqs, const int32_t* order,
+                  std::vector<int32_t>& seqs) {
+  seqs.resize(static_cast<size_t>(num_seqs));
+  if (order) {
+    std::vector<char> seen(static_cast<size_t>(num_seqs), 0);
+    for (int k = 0; k < num_seqs; ++k) {
+      const int32_t i = order[k];
+      if (i < 0 || i >= num_seqs || seen[i]) return false;
+      seen[i] = 1;
+      seqs[k] = i;
+    }
+  } else {
+    // Long sequences start early and the short ones fill the launch's tail.
+    std::iota(seqs.begin(), seqs.end(), 0);
+    std::stable_sort(seqs.begin(), seqs.end(),
+                     [&](int32_t a, int32_t b) { return seq_lens[a] > seq_lens[b]; });
+  }
+  return true;
+}
 
 }  // namespace
 
@@ -87,22 +111,8 @@ extern "C" int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int p
   const long long P = (cap + pt - 1) / pt;
   if (static_cast<long long>(num_seqs) * P > INT32_MAX) return PA_ERR_INVALID_ARG;
 
-  std::vector<int32_t> seqs(static_cast<size_t>(num_seqs));
-  if (order) {
-    std::vector<char> seen(static_cast<size_t>(num_seqs), 0);
-    for (int k = 0; k < num_seqs; ++k) {
-      const int32_t i = order[k];
-      if (i < 0 || i >= num_seqs || seen[i]) return PA_ERR_INVALID_ARG;
-      seen[i] = 1;
-      seqs[k] = i;
-    }
-  } else {
-    // Longest first, ties in index order: long sequences start early and the
-    // short ones fill the launch's tail.
-    std::iota(seqs.begin(), seqs.end(), 0);
-    std::stable_sort(seqs.begin(), seqs.end(),
-                     [&](int32_t a, int32_t b) { return seq_lens[a] > seq_lens[b]; });
-  }
+  std::vector<int32_t> seqs;
+  if (!launch_order(seq_lens, num_seqs, order, seqs)) return PA_ERR_INVALID_ARG;
   long long count = 0;
   for (int i = 0; i < num_seqs; ++i) {
     if (seq_lens[i] < 0 || seq_lens[i] > cap) return PA_ERR_INVALID_ARG;
@@ -117,5 +127,102 @@ extern "C" int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int p
     const long long parts = std::max<long long>(1, (seq_lens[i] + pt - 1) / pt);
     for (long long p = 0; p < parts; ++p) *w++ = static_cast<int32_t>(i * P + p);
   }
+  return PA_OK;
+}
+
+extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens,
+                                    int num_seqs, int max_blocks_per_seq, int block_size,
+                                    int partition_tokens, int fused_append, const int32_t* order,
+                                    int32_t* work_items, int32_t items_capacity,
+                                    int32_t* num_items, int32_t* records,
+                                    int32_t records_capacity, int32_t* num_records) {
+  if (!num_items || !num_records || num_seqs < 0 ||
+      (num_seqs > 0 && (!seq_lens || !block_tables)) || max_blocks_per_seq <= 0 ||
+      block_size <= 0 || items_capacity < 0 || records_capacity < 0)
+    return PA_ERR_INVALID_ARG;
+  const int pt = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+  if (!valid_partition(pt)) return PA_ERR_INVALID_ARG;
+  const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+  if (cap > (1ll << 30)) return PA_ERR_INVALID_ARG;
+  const long long P = (cap + pt - 1) / pt;
+  if (static_cast<long long>(num_seqs) * P > INT32_MAX) return PA_ERR_INVALID_ARG;
+  std::vector<int32_t> seqs;
+  if (!launch_order(seq_lens, num_seqs, order, seqs)) return PA_ERR_INVALID_ARG;
+
+  // partitions of each sequence, and how many of them (from the first) a record
+  // may take: whole partitions, before the appended token if there is one
+  std::vector<long long> first_part(static_cast<size_t>(num_seqs) + 1, 0);
+  std::vector<int> shareable(static_cast<size_t>(num_seqs), 0);
+  int most = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int L = seq_lens[i];
+    if (L < 0 || L > cap) return PA_ERR_INVALID_ARG;
+    first_part[i + 1] = first_part[i] + std::max(1, (L + pt - 1) / pt);
+    shareable[i] = std::max(0, (L - (fused_append ? 1 : 0)) / pt);
+    most = std::max(most, shareable[i]);
+  }
+  const long long total = first_part[num_seqs];
+  std::vector<char> covered(static_cast<size_t>(total), 0);
+
+  // Group, partition by partition, the sequences whose tables name the same
+  // blocks over it (exact comparison; a hash only narrows the candidates).
+  std::vector<int32_t> recs;
+  for (int part = 0; part < most; ++part) {
+    const long long b0 = static_cast<long long>(part) * pt / block_size;
+    const long long b1 = (static_cast<long long>(part + 1) * pt - 1) / block_size;  // inclusive
+    const size_t n = static_cast<size_t>(b1 - b0 + 1);
+    std::unordered_map<uint64_t, std::vector<int>> by_hash;  // hash -> group indices
+    std::vector<std::vector<int32_t>> groups;
+    for (int i = 0; i < num_seqs; ++i) {
+      if (shareable[i] <= part) continue;
+      const int32_t* slice = block_tables + static_cast<size_t>(i) * max_blocks_per_seq + b0;
+      uint64_t h = 1469598103934665603ull;  // FNV-1a over the entries
+      for (size_t k = 0; k < n; ++k) {
+        h ^= static_cast<uint32_t>(slice[k]);
+        h *= 1099511628211ull;
+      }
+      std::vector<int>& cands = by_hash[h];
+      int found = -1;
+      for (int gi : cands) {
+        const int32_t* other =
+            block_tables + static_cast<size_t>(groups[gi][0]) * max_blocks_per_seq + b0;
+        if (std::memcmp(slice, other, n * sizeof(int32_t)) == 0) {
+          found = gi;
+          break;
+        }
+      }
+      if (found < 0) {
+        found = static_cast<int>(groups.size());
+        groups.emplace_back();
+        cands.push_back(found);
+      }
+      groups[found].push_back(i);
+    }
+    for (const std::vector<int32_t>& grp : groups) {
+      // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
+      for (size_t at = 0; at + 1 < grp.size(); at += PA_SHARE_MAX_MEMBERS) {
+        const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, grp.size() - at);
+        recs.push_back(part);
+        recs.push_back(static_cast<int32_t>(m));
+        for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
+          recs.push_back(j < m ? grp[at + j] : -1);
+        for (size_t j = 0; j < m; ++j) covered[first_part[grp[at + j]] + part] = 1;
+      }
+    }
+  }
+  const long long nrec = static_cast<long long>(recs.size()) / PA_SHARE_RECORD_WORDS;
+  const long long nitems = total - std::count(covered.begin(), covered.end(), 1);
+  if (nrec > INT32_MAX || nitems > INT32_MAX) return PA_ERR_INVALID_ARG;
+  *num_items = static_cast<int32_t>(nitems);
+  *num_records = static_cast<int32_t>(nrec);
+  if (!work_items && !records) return PA_OK;  // size query
+  if (!work_items || !records || nitems > items_capacity || nrec > records_capacity)
+    return PA_ERR_INVALID_ARG;
+  int32_t* w = work_items;
+  for (int32_t i : seqs) {
+    for (long long part = 0; part < first_part[i + 1] - first_part[i]; ++part)
+      if (!covered[first_part[i] + part]) *w++ = static_cast<int32_t>(i * P + part);
+  }
+  if (!recs.empty()) std::memcpy(records, recs.data(), recs.size() * sizeof(int32_t));
   return PA_OK;
 }

@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "decode_config.h"
+#include "decode_shared.h"
 
 namespace pagedkv {
 namespace {
@@ -452,10 +453,17 @@ cudaError_t ensure_smem_attr(int device) {
 }
 
 template <class Tag, int D>
-int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem, cudaStream_t stream) {
+int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
+           const SharedParams* shared, int dtype, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (phases & 1) {
+    // Partitions shared by several sequences first (uniform, full partitions),
+    // then the per-sequence work; the two write disjoint partials.
+    if (shared != nullptr) {
+      const int st = launch_shared_partitions(*shared, dtype, D, stream);
+      if (st != PA_OK) return st;
+    }
     if (ensure_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(p.num_heads / p.heads_per_cta, p.num_partitions, num_seqs);
     if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
@@ -574,18 +582,51 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   p.out_dtype = out_dtype;
   p.qscale = scale * kLog2e;
 
+  // Partitions that several sequences share (records built on the host); the
+  // remaining (sequence, partition) pairs must then come as a work list.
+  SharedParams sp{};
+  const SharedParams* shared = nullptr;
+  if (opts && opts->shared_records && opts->num_shared != 0) {
+    if (opts->num_shared < 0 || opts->num_shared > 65535 || !p.work_items)
+      return PA_ERR_INVALID_ARG;
+    sp.q = q;
+    sp.k_cache = k_cache;
+    sp.v_cache = v_cache;
+    sp.block_tables = block_tables;
+    sp.seq_lens = seq_lens;
+    sp.records = opts->shared_records;
+    sp.num_records = opts->num_shared;
+    sp.num_seqs = num_seqs;
+    sp.num_heads = num_heads;
+    sp.block_size = block_size;
+    sp.max_blocks = max_blocks_per_seq;
+    sp.num_blocks = num_blocks;
+    sp.partition_tokens = pt;
+    sp.num_partitions = P;
+    sp.heads_per_cta = num_heads % 2 == 0 ? 2 : 1;
+    sp.stages = shared_kernel_smem_bytes(head_dim, sp.heads_per_cta, S) <= 227 * 1024 ? S : 2;
+    sp.fused_append = new_k != nullptr ? 1 : 0;
+    sp.out_dtype = out_dtype;
+    sp.qscale = p.qscale;
+    sp.out = out;
+    sp.ws_acc = p.ws_acc;
+    sp.ws_ml = p.ws_ml;
+    sp.err = error_record;
+    shared = &sp;
+  }
+
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == PA_BF16) {
     switch (head_dim) {
-      case 64: return launch<BF16, 64>(p, num_seqs, phases, smem, st);
-      case 128: return launch<BF16, 128>(p, num_seqs, phases, smem, st);
-      default: return launch<BF16, 256>(p, num_seqs, phases, smem, st);
+      case 64: return launch<BF16, 64>(p, num_seqs, phases, smem, shared, dtype, st);
+      case 128: return launch<BF16, 128>(p, num_seqs, phases, smem, shared, dtype, st);
+      default: return launch<BF16, 256>(p, num_seqs, phases, smem, shared, dtype, st);
     }
   }
   switch (head_dim) {
-    case 64: return launch<F16, 64>(p, num_seqs, phases, smem, st);
-    case 128: return launch<F16, 128>(p, num_seqs, phases, smem, st);
-    default: return launch<F16, 256>(p, num_seqs, phases, smem, st);
+    case 64: return launch<F16, 64>(p, num_seqs, phases, smem, shared, dtype, st);
+    case 128: return launch<F16, 128>(p, num_seqs, phases, smem, shared, dtype, st);
+    default: return launch<F16, 256>(p, num_seqs, phases, smem, shared, dtype, st);
   }
 }
 

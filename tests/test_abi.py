@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     from paged_kv_cache_317_gb300.binding import STATUS
-    assert lib.pa_version() == 1
+    assert lib.pa_version() == 2
     for code in STATUS:
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(999) == b"unknown status"
@@ -246,7 +246,24 @@ def test_decode_opts_layout_matches_the_header():
     names = [ln.strip().rstrip(";").split()[-1].lstrip("*") for ln in body.splitlines()[1:]
              if ln.strip()]
     assert names == [f[0] for f in pa_decode_opts._fields_]
-    assert ctypes.sizeof(pa_decode_opts) == 40
+    # size and offsets as a C compiler lays the header's struct out
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    prog = ("#include <stdio.h>\n#include <stddef.h>\n#include \"pagedkv.h\"\n"
+            "int main(void) { printf(\"%zu" + " %zu" * len(names) + "\\n\", sizeof(pa_decode_opts)"
+            + "".join(f", offsetof(pa_decode_opts, {n})" for n in names) + "); return 0; }\n")
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(src, "w").write(prog)
+        subprocess.run([cc, "-I", HEADER_DIR, src, "-o", exe], check=True)
+        got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    assert got == [ctypes.sizeof(pa_decode_opts)] + [getattr(pa_decode_opts, n).offset
+                                                      for n in names]
 
 
 def test_batch_fork_and_free_match_single_calls(lib):

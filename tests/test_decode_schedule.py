@@ -109,3 +109,111 @@ def test_work_items_reject_bad_arguments():
         B.partition_work_items([10], 24, 4, 16)                          # not a multiple of 16
     with pytest.raises(ValueError):
         B.partition_work_items([10, 20], 16, 4, 16, order=[0])
+
+
+def _plan_by_definition(tables, lens, pt, bs, fused, order=None):
+    """Brute-force restatement of the share plan: records as a set of
+    (partition, members), and the work list."""
+    N, MB = tables.shape
+    P = max(1, -(-MB * bs // pt))
+    nparts = [max(1, -(-int(L) // pt)) for L in lens]
+    share = [max(0, (int(L) - (1 if fused else 0)) // pt) for L in lens]
+    covered, recs = set(), set()
+    for p in range(max(share, default=0)):
+        b0, b1 = p * pt // bs, ((p + 1) * pt - 1) // bs
+        groups = {}
+        for i in range(N):
+            if share[i] > p:
+                groups.setdefault(tuple(tables[i, b0:b1 + 1]), []).append(i)
+        for grp in groups.values():
+            for at in range(0, len(grp) - 1, 16):
+                mem = tuple(grp[at:at + 16])
+                recs.add((p, mem))
+                covered.update((i, p) for i in mem)
+    order = sorted(range(N), key=lambda i: (-int(lens[i]), i)) if order is None else order
+    items = [i * P + p for i in order for p in range(nparts[i]) if (i, p) not in covered]
+    return recs, np.array(items, dtype=np.int32)
+
+
+def _records_as_set(recs):
+    return {(int(r[0]), tuple(int(x) for x in r[2:2 + r[1]])) for r in recs}
+
+
+def test_share_plan_matches_its_definition():
+    rng = np.random.default_rng(5)
+    for trial in range(150):
+        bs = int(rng.choice([16, 32]))
+        pt = int(rng.choice([16, 32, 64, 128]))
+        N = int(rng.integers(1, 40))
+        MB = int(rng.integers(1, 24))
+        # a few "prompts" whose block lists sequences copy (with private tails)
+        prompts = rng.integers(0, 500, size=(4, MB)).astype(np.int32)
+        tables = rng.integers(0, 500, size=(N, MB)).astype(np.int32)
+        lens = rng.integers(0, MB * bs + 1, size=N)
+        for i in range(N):
+            if rng.random() < 0.7:
+                k = int(rng.integers(0, MB + 1))
+                tables[i, :k] = prompts[int(rng.integers(0, 4)), :k]
+        fused = bool(rng.integers(0, 2))
+        if fused:
+            lens = np.maximum(lens, 1)
+        order = None if trial % 4 else list(rng.permutation(N))
+        items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused, order=order)
+        want_recs, want_items = _plan_by_definition(tables, lens, pt, bs, fused, order)
+        assert recs.shape[1] == B.PA_SHARE_RECORD_WORDS
+        assert _records_as_set(recs) == want_recs, trial
+        assert np.array_equal(items, want_items), trial
+        for r in recs:
+            assert 2 <= r[1] <= 16 and (r[2 + r[1]:] == -1).all()
+
+
+def test_share_plan_on_forked_sequences():
+    """Sequences forked from one prompt by the allocator share their prompt's full
+    partitions; each pair that holds tokens is computed exactly once."""
+    bs, pt = 16, 64
+    alloc = B.BlockAllocator(4000, bs)
+    ids = []
+    for k, prompt in enumerate((300, 70, 1000)):
+        alloc.add(100 * k, prompt)
+        for s in range(1, 21 if k == 2 else 5):          # 20 samples of the long prompt
+            alloc.fork(100 * k, 100 * k + s)
+            ids.append(100 * k + s)
+        ids.append(100 * k)
+    rng = np.random.default_rng(2)
+    for _ in range(int(rng.integers(1, 40))):
+        alloc.batch_append(ids)                            # one token each, copy-on-write
+    for i in ids[::3]:                                     # ragged tails
+        for _ in range(int(rng.integers(0, 90))):
+            alloc.append(i)
+    alloc.batch_append(ids)                                # the token this step appends
+    MB = 80
+    tables, lens = alloc.batch_block_tables(ids, MB)
+    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
+    P = -(-MB * bs // pt)
+    pairs = [(int(x) // P, int(x) % P) for x in items]
+    for r in recs:
+        p, m = int(r[0]), int(r[1])
+        mem = [int(x) for x in r[2:2 + m]]
+        b0, b1 = p * pt // bs, ((p + 1) * pt - 1) // bs
+        assert all((tables[i, b0:b1 + 1] == tables[mem[0], b0:b1 + 1]).all() for i in mem)
+        assert all((p + 1) * pt <= lens[i] - 1 for i in mem)
+        pairs += [(i, p) for i in mem]
+    want = [(i, p) for i in range(len(ids)) for p in range(max(1, -(-int(lens[i]) // pt)))]
+    assert sorted(pairs) == sorted(want)
+    # the 21 holders of the long prompt share its 15 full partitions: 16 + 5 members each
+    sizes = sorted(int(r[1]) for r in recs if int(r[1]) in (16, 5))
+    assert sizes.count(16) >= 15 and sizes.count(5) >= 15
+
+
+def test_share_plan_rejects_bad_arguments():
+    t = np.zeros((2, 4), np.int32)
+    with pytest.raises(B.PagedKVError, match="INVALID_ARG"):
+        B.share_plan(t, [10, 65], 16, 16)                  # longer than 4 blocks
+    with pytest.raises(B.PagedKVError, match="INVALID_ARG"):
+        B.share_plan(t, [10, 20], 24, 16)                  # partition not a multiple of 16
+    with pytest.raises(B.PagedKVError, match="INVALID_ARG"):
+        B.share_plan(t, [10, 20], 16, 16, order=[1, 1])
+    with pytest.raises(ValueError):
+        B.share_plan(t, [10], 16, 16)
+    items, recs = B.share_plan(t, [0, 0], 16, 16)
+    assert list(items) == [0, 4] and recs.shape == (0, B.PA_SHARE_RECORD_WORDS)

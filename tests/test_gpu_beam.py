@@ -51,6 +51,7 @@ def test_beam_search_churn(lib):
     step_v = torch.empty_like(step_k)
     max_blocks = int(-(-(plan.prompt_lens.max() + plan.steps + 1) // bs))
     total_copies = 0
+    shared_parts = 0
     free_start = alloc.num_free()
     for s in range(plan.steps):
         new_beams = []
@@ -81,6 +82,14 @@ def test_beam_search_churn(lib):
         tables, lens = alloc.batch_block_tables(ids, max_blocks)
         out = B.paged_attn_decode(q, kc, vc, torch.from_numpy(tables).cuda(),
                                   torch.from_numpy(lens).cuda(), plan.scale, error_record=rec)
+        # and with the partitions the beams share read once per group
+        items, recs = B.share_plan(tables, lens, 64, bs, fused_append=False)
+        shared_parts += len(recs)
+        out_sh = B.paged_attn_decode(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                     torch.from_numpy(lens).cuda(), plan.scale,
+                                     partition_tokens=64, work_items=torch.from_numpy(items).cuda(),
+                                     shared_records=torch.from_numpy(recs).cuda(),
+                                     error_record=rec)
         alloc.check()
         if s % 5 == 4 or s == plan.steps - 1:
             k_st = [(0, plan.prompt_k), (base, step_k)]
@@ -89,8 +98,9 @@ def test_beam_search_churn(lib):
                 assert lens[n] == content.length(i)
                 ref = _oracle_logical(q[n], content, i, k_st, v_st, plan.scale)
                 assert_matches_oracle(out[n], ref, f"step {s} beam {i}")
+                assert_matches_oracle(out_sh[n], ref, f"step {s} beam {i}, shared partitions")
     assert B.pa_error_read(rec) == [0, 0, 0, 0]
-    assert total_copies > 0
+    assert total_copies > 0 and shared_parts > 0
     for grp in beams:
         for i in grp:
             alloc.free(i)

@@ -42,12 +42,17 @@ def test_decode_random_configuration(B, seed):
     pt = int(rng.choice([0, 16, 64, 256, 512]))
     out_dtype = [torch.float32, torch.float16, torch.bfloat16][int(rng.integers(0, 3))]
     sched = {}
-    choice = int(rng.integers(0, 3))
+    choice = int(rng.integers(0, 4))
     if choice == 1:
         sched["seq_order"] = torch.from_numpy(rng.permutation(N).astype(np.int32)).cuda()
     elif choice == 2:
         items = partition_work_items(b.context_lens, pt, b.max_blocks_per_seq, bs)
         sched["work_items"] = torch.from_numpy(rng.permutation(items).astype(np.int32)).cuda()
+    elif choice == 3:
+        # the host schedule; a random SM count spreads its choice over 64..512
+        pt = B.decode_partition_tokens(b.context_lens, H, G, int(rng.choice([1, 4, 152])))
+        items = partition_work_items(b.context_lens, pt, b.max_blocks_per_seq, bs)
+        sched["work_items"] = torch.from_numpy(items).cuda()
     rec = B.new_error_record()
     if append:
         out = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl,

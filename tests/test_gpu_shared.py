@@ -1,0 +1,188 @@
+"""Decode over partitions that several sequences share (shared_records built by
+share_plan): families of sequences forked from one prompt with private,
+copy-on-write tails, checked against the oracle over each sequence's logical
+tokens (PagedAttention, zeroshotmind.com page, "Sharing a prefix without copying
+it")."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_matches_oracle
+from oracle.content import LogicalSequences
+from test_gpu_workloads import _oracle_logical
+from workloads.gen import DTYPES, _torch_gen, randn_rounded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B(lib):
+    from paged_kv_cache_317_gb300 import binding
+    return binding
+
+
+class Families:
+    """Sequences forked from shared prompts, written through the library's own
+    append and copy kernels; `store` holds every row ever written, in order."""
+
+    def __init__(self, B, seed, prompts, members, tail_max, H, D, bs, dtype, fused):
+        rng = np.random.default_rng(seed)
+        self.H, self.D, self.bs, self.fused = H, D, bs, fused
+        dt = DTYPES[dtype]
+        total = int(sum(prompts) + len(prompts) * members * (tail_max + 2))
+        self.store_k = randn_rounded((total, H, D), dt, _torch_gen(seed, "cuda"), "cuda")
+        self.store_v = randn_rounded((total, H, D), dt, _torch_gen(seed + 1, "cuda"), "cuda")
+        nb = 2 * (total // bs + len(prompts) * members + 8)
+        self.alloc = B.BlockAllocator(nb, bs, rng.permutation(nb).astype(np.int32))
+        self.kc = torch.full((nb, H, bs, D), float("nan"), dtype=dt, device="cuda")
+        self.vc = torch.full_like(self.kc, float("nan"))
+        self.content = LogicalSequences()
+        self.rec = B.new_error_record()
+        self.B, self.next_row, self.ids = B, 0, []
+        for f, Lp in enumerate(prompts):
+            root = 1000 * f
+            self.alloc.add(root, Lp)
+            self._write(range(self.next_row, self.next_row + Lp), self.alloc.slots(root, 0, Lp))
+            self.content.add(root, range(self.next_row, self.next_row + Lp))
+            self.next_row += Lp
+            fam = [root]
+            for s in range(1, members):
+                self.alloc.fork(root, root + s)
+                self.content.fork(root, root + s)
+                fam.append(root + s)
+            self.ids += fam
+        for i in self.ids:                                  # private tails
+            for _ in range(int(rng.integers(0, tail_max + 1))):
+                self._append_one(i)
+        self.new_rows = None
+        if fused:                                           # the token this step appends
+            slots, pairs = self.alloc.batch_append(self.ids)
+            if len(pairs):
+                B.block_copy([self.kc], [self.vc], torch.from_numpy(pairs).cuda(),
+                             error_record=self.rec)
+            self.new_rows = np.arange(self.next_row, self.next_row + len(self.ids))
+            for i, r in zip(self.ids, self.new_rows):
+                self.content.append(i, int(r))
+            self.next_row += len(self.ids)
+        self.q = randn_rounded((len(self.ids), H, D), dt, _torch_gen(seed + 2, "cuda"), "cuda")
+        self.scale = D ** -0.5
+
+    def _write(self, rows, slots):
+        r = torch.as_tensor(list(rows), dtype=torch.long, device="cuda")
+        self.B.kv_cache_append(self.store_k[r], self.store_v[r],
+                               torch.as_tensor(np.asarray(slots), dtype=torch.int64).cuda(),
+                               self.kc, self.vc, error_record=self.rec)
+
+    def _append_one(self, i):
+        slot, cow = self.alloc.append(i)
+        if cow is not None:
+            self.B.block_copy([self.kc], [self.vc],
+                              torch.tensor([cow], dtype=torch.int64, device="cuda"),
+                              error_record=self.rec)
+        self._write([self.next_row], [slot])
+        self.content.append(i, self.next_row)
+        self.next_row += 1
+
+    def tables(self, max_blocks=None):
+        mb = max_blocks or max(len(self.alloc.block_table(i)) for i in self.ids)
+        return self.alloc.batch_block_tables(self.ids, mb)
+
+    def decode(self, tables, lens, pt, items=None, recs=None, out_dtype=torch.float32):
+        B = self.B
+        kw = dict(partition_tokens=pt, error_record=self.rec, out_dtype=out_dtype)
+        if items is not None:
+            kw["work_items"] = torch.from_numpy(items).cuda()
+        if recs is not None:
+            kw["shared_records"] = torch.from_numpy(recs).cuda()
+        bt, sl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+        if self.fused:
+            nr = torch.from_numpy(self.new_rows).cuda()
+            out = B.paged_attn_decode_append(self.q, self.store_k[nr], self.store_v[nr], self.kc,
+                                             self.vc, bt, sl, self.scale, **kw)
+        else:
+            out = B.paged_attn_decode(self.q, self.kc, self.vc, bt, sl, self.scale, **kw)
+        torch.cuda.synchronize()
+        return out
+
+    def check(self, out, lens, what, seqs=None):
+        st_k, st_v = [(0, self.store_k)], [(0, self.store_v)]
+        for n in (range(len(self.ids)) if seqs is None else seqs):
+            i = self.ids[n]
+            assert lens[n] == self.content.length(i)
+            ref = _oracle_logical(self.q[n], self.content, i, st_k, st_v, self.scale)
+            assert_matches_oracle(out[n], ref, f"{what} seq {i}")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("dtype,D,bs", [("bf16", 128, 16), ("f16", 128, 32), ("bf16", 64, 16),
+                                        ("f16", 256, 16)])
+def test_shared_partitions_match_oracle(B, fused, dtype, D, bs):
+    fam = Families(B, 7 + D + bs, prompts=[700, 300, 1300], members=6, tail_max=150, H=4, D=D,
+                   bs=bs, dtype=dtype, fused=fused)
+    tables, lens = fam.tables()
+    pt = 128
+    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused)
+    assert len(recs) >= (700 // pt) + (300 // pt) + (1300 // pt) - 3
+    out = fam.decode(tables, lens, pt, items, recs)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, f"shared {dtype} D{D} bs{bs} fused={fused}")
+
+
+def test_shared_and_plain_paths_agree(B):
+    fam = Families(B, 21, prompts=[1100, 900], members=8, tail_max=300, H=8, D=128, bs=16,
+                   dtype="bf16", fused=True)
+    tables, lens = fam.tables()
+    items, recs = B.share_plan(tables, lens, 256, 16)
+    # the cache is written by the fused append on the first call; both calls write
+    # the same rows, and read the same values
+    plain = fam.decode(tables, lens, 256, B.partition_work_items(lens, 256, tables.shape[1], 16))
+    shared = fam.decode(tables, lens, 256, items, recs)
+    again = fam.decode(tables, lens, 256, items, recs)
+    assert torch.equal(shared, again)                   # repeatable bit for bit
+    assert (shared - plain).abs().max().item() < 2e-3
+    fam.check(shared, lens, "shared vs plain")
+
+
+def test_more_than_sixteen_members_split_into_records(B):
+    fam = Families(B, 33, prompts=[600], members=21, tail_max=40, H=2, D=128, bs=16,
+                   dtype="bf16", fused=True)
+    tables, lens = fam.tables()
+    items, recs = B.share_plan(tables, lens, 64, 16)
+    assert sorted(set(int(r[1]) for r in recs)) == [5, 16]
+    out = fam.decode(tables, lens, 64, items, recs)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, "21 members")
+
+
+def test_single_partition_members_get_their_output_directly(B):
+    """With one partition per sequence (capacity = partition), a shared record
+    holds the whole sequence and writes the output row itself."""
+    fam = Families(B, 41, prompts=[64, 64], members=3, tail_max=0, H=2, D=64, bs=16,
+                   dtype="f16", fused=False)
+    tables, lens = fam.tables(max_blocks=4)
+    items, recs = B.share_plan(tables, lens, 64, 16, fused_append=False)
+    assert len(items) == 0 and len(recs) == 2
+    assert B.paged_attn_workspace_size(len(lens), 2, 64, 16, 4, 64) == 0
+    out = fam.decode(tables, lens, 64, items, recs, out_dtype=torch.float16)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, "direct output")
+
+
+def test_bad_shared_record_is_recorded_and_skipped(B):
+    fam = Families(B, 51, prompts=[400], members=4, tail_max=20, H=2, D=128, bs=16,
+                   dtype="bf16", fused=False)
+    tables, lens = fam.tables()
+    items, recs = B.share_plan(tables, lens, 128, 16, fused_append=False)
+    bad = recs.copy()
+    bad[0, 3] = 99                                      # a member that does not exist
+    out = torch.zeros(len(lens), 2, 128, device="cuda")
+    B.paged_attn_decode(fam.q, fam.kc, fam.vc, torch.from_numpy(tables).cuda(),
+                        torch.from_numpy(lens).cuda(), fam.scale, out=out, partition_tokens=128,
+                        work_items=torch.from_numpy(items).cuda(),
+                        shared_records=torch.from_numpy(bad).cuda(), error_record=fam.rec)
+    assert B.pa_error_read(fam.rec) == [6, 1, 0, 99]
+    with pytest.raises(B.PagedKVError, match="INVALID_ARG"):     # records need a work list
+        B.paged_attn_decode(fam.q, fam.kc, fam.vc, torch.from_numpy(tables).cuda(),
+                            torch.from_numpy(lens).cuda(), fam.scale, partition_tokens=128,
+                            shared_records=torch.from_numpy(recs).cuda())

@@ -173,10 +173,19 @@ def test_parallel_sampling_with_copy_on_write(B, partial):
     k_st = [(0, plan.prompt_k), (tail_base, plan.tail_k)]
     v_st = [(0, plan.prompt_v), (tail_base, plan.tail_v)]
     seqs = _sample(N, 40, 3, always=range(S))
+    # the same decode reading each prompt's shared partitions once for all samples
+    items, recs = B.share_plan(tables, lens, 512, bs, fused_append=False)
+    assert len(recs) == P * 2 and (recs[:, 1] == S).all()      # tokens 0..1023 of each prompt
+    out_sh = B.paged_attn_decode(plan.q, kc, vc, torch.from_numpy(tables).cuda(),
+                                 torch.from_numpy(lens).cuda(), plan.scale, partition_tokens=512,
+                                 work_items=torch.from_numpy(items).cuda(),
+                                 shared_records=torch.from_numpy(recs).cuda(), error_record=rec)
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
     for i in seqs:
         assert lens[i] == content.length(i)
         ref = _oracle_logical(plan.q[i], content, i, k_st, v_st, plan.scale)
         assert_matches_oracle(out[i], ref, f"sampling seq {i}")
+        assert_matches_oracle(out_sh[i], ref, f"sampling seq {i}, shared partitions")
 
 
 # --------------------------------------------------------------- mixed serving
