@@ -646,7 +646,22 @@ def run_workload(args, rank, world, local_rank):
         out = torch.empty(plan.q.shape, dtype=plan.dtype, device=dev)
         fn = lambda: B.paged_attn_decode(plan.q, kc, vc, bt, sl, plan.scale, out=out,
                                          error_record=rec)
-        ms = _time_device(fn, K, W, stream)
+        plain_ms = _time_device(fn, K, W, stream)
+        ms, sched = plain_ms, "full grid, 512-token partitions"
+        if not args.no_share:
+            # each prompt's full partitions read once for its 8 samples
+            pt = args.serving_partition or B.decode_partition_tokens(lens, plan.num_heads)
+            items, recs = B.share_plan(tables, lens, pt, bs, fused_append=False)
+            it_d, rc_d = torch.from_numpy(items).to(dev), torch.from_numpy(recs).to(dev)
+            ws = torch.empty(max(16, B.paged_attn_workspace_size(
+                plan.num_seqs, plan.num_heads, plan.head_dim, bs, mb, pt)), dtype=torch.uint8,
+                device=dev)
+            fn = lambda: B.paged_attn_decode(plan.q, kc, vc, bt, sl, plan.scale, out=out,
+                                             partition_tokens=pt, workspace=ws, work_items=it_d,
+                                             shared_records=rc_d, error_record=rec)
+            ms = _time_device(fn, K, W, stream)
+            sched = (f"{len(recs)} shared-partition records + {len(items)} work items, "
+                     f"{pt}-token partitions")
         nb = step_bytes(lens, plan.num_heads, plan.head_dim, bs)
         total = nb["total"] - nb["append_write"]
         st = alloc.stats()
@@ -656,8 +671,10 @@ def run_workload(args, rank, world, local_rank):
         line.update(config={"workload": "parallel sampling: 32 prompts x 8 samples, shared "
                                         "1024+U[1,15]-token prefixes, tails U[1,512]",
                             "num_seqs": plan.num_seqs, "copies": int(len(pairs)),
-                            "context_tokens": tokens, "l2": "inputs larger than L2"},
+                            "context_tokens": tokens, "schedule": sched,
+                            "l2": "inputs larger than L2"},
                     dtype="bf16", block_copy_ms=round(copy_ms, 5),
+                    without_sharing_ms=round(plain_ms, 5),
                     unique_kv_bytes=unique_kv,
                     unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
                     unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4))
@@ -679,21 +696,26 @@ def run_workload(args, rank, world, local_rank):
         max_blocks = int(-(-(plan.init_lens.max() + plan.steps) // bs))
         tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
         out = torch.empty((N, plan.num_heads, plan.head_dim), dtype=plan.dtype, device=dev)
+        pt = args.serving_partition or 512
         ws = torch.empty(B.paged_attn_workspace_size(N, plan.num_heads, plan.head_dim, bs,
-                                                     max_blocks, 0), dtype=torch.uint8, device=dev)
+                                                     max_blocks, pt), dtype=torch.uint8,
+                         device=dev)
         torch.cuda.synchronize()
         # per-step host inputs staged in pinned memory (two sets, reused once the
         # copy that read them two steps back has finished)
-        n_items_max = N * int(-(-max_blocks * bs // 512))
+        n_items_max = N * int(-(-max_blocks * bs // pt))
+        RW = B.PA_SHARE_RECORD_WORDS
         pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
                      "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
                      "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
+                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32).pin_memory(),
                      "done": torch.cuda.Event()} for _ in range(2)]
         dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
                      "sl": torch.empty(N, dtype=torch.int32, device=dev),
-                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev)}
+                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev),
+                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32, device=dev)}
                     for _ in range(2)]
-        host_s, stage_s, lens_seen = 0.0, 0.0, 0
+        host_s, stage_s, plan_s, lens_seen, n_shared = 0.0, 0.0, 0.0, 0, 0
         split = []   # per step: events before copies, before table uploads, before decode, after
         t0 = time.perf_counter()
         ev0 = torch.cuda.Event(enable_timing=True)
@@ -718,21 +740,32 @@ def run_workload(args, rank, world, local_rank):
             evs[1].record(stream)
             q, k, v = tokens_all[s_]
             hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
-            items = B.partition_work_items(lens, 0, max_blocks, plan.block_size)
+            h2 = time.perf_counter()
+            if args.no_share:
+                items = B.partition_work_items(lens, pt, max_blocks, plan.block_size)
+                recs = np.empty((0, RW), dtype=np.int32)
+            else:   # partitions that forked sequences still share are read once
+                items, recs = B.share_plan(tables, lens, pt, plan.block_size, fused_append=True)
+            plan_s += time.perf_counter() - h2
+            n_shared += len(recs)
             hs["done"].synchronize()            # the copy that read this buffer set
             h1 = time.perf_counter()
             hs["bt"].numpy()[:] = tables
             hs["sl"].numpy()[:] = lens
             hs["it"].numpy()[: len(items)] = items
+            hs["rc"].numpy()[: len(recs)] = recs
             stage_s += time.perf_counter() - h1
             ds["bt"].copy_(hs["bt"], non_blocking=True)
             ds["sl"].copy_(hs["sl"], non_blocking=True)
             ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
+            ds["rc"][: len(recs)].copy_(hs["rc"][: len(recs)], non_blocking=True)
             hs["done"].record(stream)
             bt_d, sl_d, it_d = ds["bt"], ds["sl"], ds["it"][: len(items)]
             evs[2].record(stream)
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
-                                       workspace=ws, error_record=rec, work_items=it_d)
+                                       partition_tokens=pt, workspace=ws, error_record=rec,
+                                       work_items=it_d,
+                                       shared_records=ds["rc"][: len(recs)] if len(recs) else None)
             evs[3].record(stream)
             split.append(evs)
         ev1 = torch.cuda.Event(enable_timing=True)
@@ -746,9 +779,14 @@ def run_workload(args, rank, world, local_rank):
         value = total / (ms * 1e-3) / 1e9
         line.update(config={"workload": "mixed serving: 512 seqs, 70% U[32,256] / 30% "
                                         "U[1024,4096], 26 forks/step, fused append+decode",
-                            "steps_run": plan.steps, "l2": "inputs larger than L2"},
+                            "steps_run": plan.steps, "partition_tokens": pt,
+                            "schedule": ("work list only" if args.no_share else
+                                         f"shared partitions ({n_shared / plan.steps:.1f} "
+                                         "records per step) + work list"),
+                            "l2": "inputs larger than L2"},
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
+                    host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     device_ms_per_step_split={
                         "block_copy": seg(0, 1), "table_uploads": seg(1, 2),
@@ -785,19 +823,23 @@ def run_workload(args, rank, world, local_rank):
         max_blocks = int(-(-(plan.prompt_lens.max() + plan.steps + 1) // bs))
         tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
         out = torch.empty((N, H, D), dtype=plan.dtype, device=dev)
-        ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, max_blocks, 0),
+        pt = args.serving_partition or 512
+        ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, max_blocks, pt),
                          dtype=torch.uint8, device=dev)
-        n_items_max = N * int(-(-max_blocks * bs // 512))
+        n_items_max = N * int(-(-max_blocks * bs // pt))
+        RW = B.PA_SHARE_RECORD_WORDS
         pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
                      "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
                      "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
+                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32).pin_memory(),
                      "done": torch.cuda.Event()} for _ in range(2)]
         dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
                      "sl": torch.empty(N, dtype=torch.int32, device=dev),
-                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev)}
+                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev),
+                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32, device=dev)}
                     for _ in range(2)]
         torch.cuda.synchronize()
-        host_s, stage_s, lens_seen, copies = 0.0, 0.0, 0, 0
+        host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
         split = []
         t0 = time.perf_counter()
         ev0 = torch.cuda.Event(enable_timing=True)
@@ -824,21 +866,31 @@ def run_workload(args, rank, world, local_rank):
             evs[1].record(stream)
             q, k, v = tokens_all[s_]
             hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
-            items = B.partition_work_items(lens, 0, max_blocks, bs)
+            h2 = time.perf_counter()
+            if args.no_share:
+                items = B.partition_work_items(lens, pt, max_blocks, bs)
+                recs = np.empty((0, RW), dtype=np.int32)
+            else:   # the partitions a group's beams share are read once for the group
+                items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
+            plan_s += time.perf_counter() - h2
+            n_shared += len(recs)
             hs["done"].synchronize()            # the copy that read this buffer set
             h1 = time.perf_counter()
             hs["bt"].numpy()[:] = tables
             hs["sl"].numpy()[:] = lens
             hs["it"].numpy()[: len(items)] = items
+            hs["rc"].numpy()[: len(recs)] = recs
             stage_s += time.perf_counter() - h1
             ds["bt"].copy_(hs["bt"], non_blocking=True)
             ds["sl"].copy_(hs["sl"], non_blocking=True)
             ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
+            ds["rc"][: len(recs)].copy_(hs["rc"][: len(recs)], non_blocking=True)
             hs["done"].record(stream)
             evs[2].record(stream)
             B.paged_attn_decode_append(q, k, v, kc, vc, ds["bt"], ds["sl"], plan.scale, out=out,
-                                       workspace=ws, error_record=rec,
-                                       work_items=ds["it"][: len(items)])
+                                       partition_tokens=pt, workspace=ws, error_record=rec,
+                                       work_items=ds["it"][: len(items)],
+                                       shared_records=ds["rc"][: len(recs)] if len(recs) else None)
             evs[3].record(stream)
             split.append(evs)
         ev1 = torch.cuda.Event(enable_timing=True)
@@ -857,9 +909,14 @@ def run_workload(args, rank, world, local_rank):
             raise RuntimeError("beam workload leaked blocks")
         line.update(config={"workload": "beam-search churn: 64 groups x 4 beams, prompts "
                                         "U[500,1500], 40 heads x 128, bf16, block 16",
-                            "steps_run": plan.steps, "l2": "inputs larger than L2"},
+                            "steps_run": plan.steps, "partition_tokens": pt,
+                            "schedule": ("work list only" if args.no_share else
+                                         f"shared partitions ({n_shared / plan.steps:.1f} "
+                                         "records per step) + work list"),
+                            "l2": "inputs larger than L2"},
                     dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
+                    host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     copies_per_step=round(copies / plan.steps, 2),
                     device_ms_per_step_split={
@@ -1075,6 +1132,12 @@ def main(argv=None):
     ap.add_argument("--block-size", type=int, default=16, help="13B-shaped batch: tokens per block")
     ap.add_argument("--partition", type=int, default=512,
                     help="13B-shaped batch: split-K partition length in tokens")
+    ap.add_argument("--no-share", action="store_true",
+                    help="sampling/beam/mixed: read shared partitions once per sequence "
+                         "instead of once per group")
+    ap.add_argument("--serving-partition", type=int, default=0,
+                    help="sampling/beam/mixed: split-K partition length (0: the host rule "
+                         "for sampling, 512 for beam and mixed)")
     ap.add_argument("--workload", default="13b",
                     choices=["13b", "tiny", "small", "long16", "long32", "sampling", "mixed",
                              "beam", "prefill", "append", "copy"],

@@ -68,6 +68,9 @@ def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_re
 
 def _host_int32(values, name: str) -> "np.ndarray":
     import numpy as np
+    if isinstance(values, np.ndarray) and values.dtype == np.int32 and values.ndim == 1 \
+            and values.flags.c_contiguous:
+        return values
     a = np.asarray(values, dtype=np.int64).reshape(-1)
     if a.size and (a.min() < -2**31 or a.max() >= 2**31):
         raise ValueError(f"{name}: values do not fit int32")
@@ -131,14 +134,15 @@ def share_plan(block_tables, seq_lens, partition_tokens: int, block_size: int,
     lib, ni, nr = load_library(), ctypes.c_int32(), ctypes.c_int32()
     args = (tables.ctypes.data_as(P_int32), lens.ctypes.data_as(P_int32), len(lens),
             tables.shape[1], block_size, partition_tokens, int(bool(fused_append)), ordp)
-    _check(lib.pa_decode_share_plan(*args, None, 0, ctypes.byref(ni), None, 0,
+    # one call with room for every (sequence, partition) pair; records hold >= 2 each
+    pt = partition_tokens or 512
+    pairs = len(lens) * max(1, -(-tables.shape[1] * block_size // pt)) if pt > 0 else 0
+    items = np.empty(pairs, dtype=np.int32)
+    recs = np.empty((pairs // 2, PA_SHARE_RECORD_WORDS), dtype=np.int32)
+    _check(lib.pa_decode_share_plan(*args, items.ctypes.data_as(P_int32), len(items),
+                                    ctypes.byref(ni), recs.ctypes.data_as(P_int32), len(recs),
                                     ctypes.byref(nr)), "pa_decode_share_plan")
-    items = np.empty(ni.value, dtype=np.int32)
-    recs = np.empty((nr.value, PA_SHARE_RECORD_WORDS), dtype=np.int32)
-    _check(lib.pa_decode_share_plan(*args, items.ctypes.data_as(P_int32), ni.value,
-                                    ctypes.byref(ni), recs.ctypes.data_as(P_int32), nr.value,
-                                    ctypes.byref(nr)), "pa_decode_share_plan")
-    return items, recs
+    return items[: ni.value], recs[: nr.value]
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h

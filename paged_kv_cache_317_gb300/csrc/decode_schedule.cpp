@@ -9,7 +9,6 @@
 #include <cstdint>
 #include <cstring>
 #include <numeric>
-#include <unordered_map>
 #include <vector>
 
 #include "decode_config.h"
@@ -165,49 +164,54 @@ extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* 
   std::vector<char> covered(static_cast<size_t>(total), 0);
 
   // Group, partition by partition, the sequences whose tables name the same
-  // blocks over it (exact comparison; a hash only narrows the candidates).
+  // blocks over it.  Sequences share a physical block only through forks, so
+  // candidates are sorted by the partition's first block and only runs with an
+  // equal first block are compared entry by entry.
   std::vector<int32_t> recs;
+  std::vector<std::pair<int32_t, int32_t>> keyed;  // (first block of the slice, sequence)
+  std::vector<int32_t> run, group;
   for (int part = 0; part < most; ++part) {
     const long long b0 = static_cast<long long>(part) * pt / block_size;
     const long long b1 = (static_cast<long long>(part + 1) * pt - 1) / block_size;  // inclusive
     const size_t n = static_cast<size_t>(b1 - b0 + 1);
-    std::unordered_map<uint64_t, std::vector<int>> by_hash;  // hash -> group indices
-    std::vector<std::vector<int32_t>> groups;
-    for (int i = 0; i < num_seqs; ++i) {
-      if (shareable[i] <= part) continue;
-      const int32_t* slice = block_tables + static_cast<size_t>(i) * max_blocks_per_seq + b0;
-      uint64_t h = 1469598103934665603ull;  // FNV-1a over the entries
-      for (size_t k = 0; k < n; ++k) {
-        h ^= static_cast<uint32_t>(slice[k]);
-        h *= 1099511628211ull;
-      }
-      std::vector<int>& cands = by_hash[h];
-      int found = -1;
-      for (int gi : cands) {
-        const int32_t* other =
-            block_tables + static_cast<size_t>(groups[gi][0]) * max_blocks_per_seq + b0;
-        if (std::memcmp(slice, other, n * sizeof(int32_t)) == 0) {
-          found = gi;
-          break;
+    keyed.clear();
+    for (int i = 0; i < num_seqs; ++i)
+      if (shareable[i] > part)
+        keyed.emplace_back(block_tables[static_cast<size_t>(i) * max_blocks_per_seq + b0], i);
+    std::sort(keyed.begin(), keyed.end());
+    for (size_t a = 0; a < keyed.size();) {
+      size_t e = a + 1;
+      while (e < keyed.size() && keyed[e].first == keyed[a].first) ++e;
+      if (e - a >= 2) {
+        run.clear();
+        for (size_t k = a; k < e; ++k) run.push_back(keyed[k].second);
+        // split the run into groups of identical slices (members in index order)
+        while (run.size() >= 2) {
+          const int32_t* ref =
+              block_tables + static_cast<size_t>(run[0]) * max_blocks_per_seq + b0;
+          group.clear();
+          size_t keep = 0;
+          for (size_t k = 0; k < run.size(); ++k) {
+            const int32_t* slice =
+                block_tables + static_cast<size_t>(run[k]) * max_blocks_per_seq + b0;
+            if (k == 0 || std::memcmp(slice, ref, n * sizeof(int32_t)) == 0)
+              group.push_back(run[k]);
+            else
+              run[keep++] = run[k];
+          }
+          run.resize(keep);
+          // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
+          for (size_t at = 0; at + 1 < group.size(); at += PA_SHARE_MAX_MEMBERS) {
+            const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, group.size() - at);
+            recs.push_back(part);
+            recs.push_back(static_cast<int32_t>(m));
+            for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
+              recs.push_back(j < m ? group[at + j] : -1);
+            for (size_t j = 0; j < m; ++j) covered[first_part[group[at + j]] + part] = 1;
+          }
         }
       }
-      if (found < 0) {
-        found = static_cast<int>(groups.size());
-        groups.emplace_back();
-        cands.push_back(found);
-      }
-      groups[found].push_back(i);
-    }
-    for (const std::vector<int32_t>& grp : groups) {
-      // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
-      for (size_t at = 0; at + 1 < grp.size(); at += PA_SHARE_MAX_MEMBERS) {
-        const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, grp.size() - at);
-        recs.push_back(part);
-        recs.push_back(static_cast<int32_t>(m));
-        for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
-          recs.push_back(j < m ? grp[at + j] : -1);
-        for (size_t j = 0; j < m; ++j) covered[first_part[grp[at + j]] + part] = 1;
-      }
+      a = e;
     }
   }
   const long long nrec = static_cast<long long>(recs.size()) / PA_SHARE_RECORD_WORDS;
