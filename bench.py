@@ -40,6 +40,7 @@ METRIC = "paged-attn decode KV GB/s (% of HBM peak), seq-tokens/s at 13B shape"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PREFILL_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_prefill.cu",
+                   "paged_kv_cache_317_gb300/csrc/tma.cuh",
                    "paged_kv_cache_317_gb300/csrc/common.cuh")
 DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_attn_decode.cu",
                   "paged_kv_cache_317_gb300/csrc/decode_config.h",
@@ -820,6 +821,7 @@ def run_workload(args, rank, world, local_rank):
                 next_id += 1
             alloc.free(root)
             beams.append(grp)
+        beams = np.asarray(beams, dtype=np.int64)                      # [groups, width]
         max_blocks = int(-(-(plan.prompt_lens.max() + plan.steps + 1) // bs))
         tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
         out = torch.empty((N, H, D), dtype=plan.dtype, device=dev)
@@ -846,14 +848,13 @@ def run_workload(args, rank, world, local_rank):
         ev0.record(stream)
         for s_ in range(plan.steps):
             h0 = time.perf_counter()
-            old = np.asarray(beams, dtype=np.int64)                    # [groups, width]
-            parents = np.take_along_axis(old, plan.parents[s_], axis=1).ravel()
+            parents = np.take_along_axis(beams, plan.parents[s_], axis=1).ravel()
             children = np.arange(next_id, next_id + N, dtype=np.int64)
             next_id += N
             alloc.batch_fork(parents, children)
-            alloc.batch_free(old.ravel())
-            beams = children.reshape(G_, Wd).tolist()
-            ids = [i for grp in beams for i in grp]
+            alloc.batch_free(beams.ravel())
+            beams = children.reshape(G_, Wd)
+            ids = children
             slots, pairs = alloc.batch_append(ids)
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
@@ -902,9 +903,7 @@ def run_workload(args, rank, world, local_rank):
         tokens = lens_seen / plan.steps
         total = tokens * H * D * 4
         value = total / (ms * 1e-3) / 1e9
-        for grp in beams:
-            for i in grp:
-                alloc.free(i)
+        alloc.batch_free(beams.ravel())
         if alloc.num_free() != plan.num_blocks:
             raise RuntimeError("beam workload leaked blocks")
         line.update(config={"workload": "beam-search churn: 64 groups x 4 beams, prompts "

@@ -116,6 +116,9 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   static_assert(TPL * 2 == TPR, "lane split");
 
   extern __shared__ __align__(128) uint8_t smem[];
+  // A pass over shared partitions may follow as a programmatic dependent (it
+  // reads nothing this kernel writes): let it start once every block here has.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int G = p.heads_per_cta;
   const int S = p.stages;
   const int hg = blockIdx.x;
@@ -458,12 +461,12 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (phases & 1) {
-    // Partitions shared by several sequences first (uniform, full partitions),
-    // then the per-sequence work; the two write disjoint partials.
-    if (shared != nullptr) {
-      const int st = launch_shared_partitions(*shared, dtype, D, stream);
-      if (st != PA_OK) return st;
-    }
+    // The per-sequence partition pass first; the pass over shared partitions
+    // (if any) follows as its programmatic dependent, so its long, uniform blocks
+    // start as soon as every block of the first pass has started and fill the
+    // SMs that pass's ragged last wave leaves idle.  The two write disjoint
+    // partials; the shared pass's blocks wait for the first pass to complete
+    // before they exit, so the merge after it follows both.
     if (ensure_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(p.num_heads / p.heads_per_cta, p.num_partitions, num_seqs);
     if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
@@ -471,6 +474,10 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
     if (grid.y > 0) {
       paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
       if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (shared != nullptr) {
+      const int st = launch_shared_partitions(*shared, dtype, D, grid.y > 0, stream);
+      if (st != PA_OK) return st;
     }
   }
   if ((phases & 2) && p.num_partitions > 1) {
@@ -603,7 +610,9 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
     sp.num_blocks = num_blocks;
     sp.partition_tokens = pt;
     sp.num_partitions = P;
-    sp.heads_per_cta = num_heads % 2 == 0 ? 2 : 1;
+    // one head per block: twice the blocks at ~6 per SM instead of ~4 (register
+    // bound), so the shared pass's equal-sized blocks leave a smaller last wave
+    sp.heads_per_cta = 1;
     sp.stages = shared_kernel_smem_bytes(head_dim, sp.heads_per_cta, S) <= 227 * 1024 ? S : 2;
     sp.fused_append = new_k != nullptr ? 1 : 0;
     sp.out_dtype = out_dtype;

@@ -7,10 +7,11 @@
 // sequences ("members": their tables name the same physical blocks over the
 // whole partition) and reads each K/V chunk once for all of their queries.
 //  * Producer warp: per 16-token chunk, looks the block up in the first
-//    member's table and copies the chunk's K and V rows of its G heads into a
-//    ring of S shared-memory stages with 1-D bulk copies, one per row, at a
-//    pitch of row bytes + 16, so that the consumers' 8x8 matrix loads
-//    (ldmatrix) hit 32 different banks.
+//    member's table and loads the chunk's K and V rows of its G heads into a
+//    ring of S shared-memory stages with 2-D TMA boxes of 16 rows x 64 columns
+//    (128-byte swizzle), so that the consumers' 8x8 matrix loads (ldmatrix)
+//    hit 32 different banks.  (One 1-D bulk copy per row at a padded pitch
+//    does the same with 8x as many copies, and ran at 2.8 TB/s.)
 //  * One consumer warp per head: the members' queries are the 16 rows of the A
 //    operand of mma.sync m16n8k16 (rows past the member count are zero).  Per
 //    chunk: S = Q.K^T in fp32 (2 x D/16 MMAs), the online softmax of each row in
@@ -31,16 +32,19 @@
 
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "decode_config.h"
 #include "decode_shared.h"
+#include "tma.cuh"
 
 namespace pagedkv {
 namespace {
 
 constexpr int kChunk = 16;             // tokens per pipeline stage
 constexpr int kHeader = 256;           // mbarriers (2 x kMaxRing x 8 B) + abort flag
+constexpr int kAlign = 1024;           // a swizzled box must start on 1024 bytes
 constexpr int kMaxRing = 8;
 constexpr int kMaxG = 2;               // heads per block
 constexpr int kMembers = PA_SHARE_MAX_MEMBERS;
@@ -48,9 +52,9 @@ constexpr int kRecord = PA_SHARE_RECORD_WORDS;
 
 template <int D>
 struct Geo {
-  static constexpr int kRowBytes = D * 2;
-  static constexpr int kPitch = kRowBytes + 16;       // padded row in shared memory
-  static constexpr int kTileBytes = kChunk * kPitch;  // one head's K (or V) chunk
+  static constexpr int kGroups = D / 64;                   // 64-column groups (128 B rows)
+  static constexpr int kGroupBytes = kChunk * 128;         // one TMA box: 16 rows x 128 B
+  static constexpr int kTileBytes = kGroups * kGroupBytes;  // one head's K (or V) chunk
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -100,6 +104,16 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// This kernel may run as a programmatic dependent of the per-sequence partition
+// pass (it reads nothing that pass writes, so it starts early and fills the
+// SMs the pass's last wave leaves idle).  Each block waits for that pass to
+// complete before it exits, so that whatever follows this kernel in the stream
+// or graph (the merge) also follows the partition pass.  Without a
+// prerequisite grid the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_pair(const char* base, int seq, int num_heads, int h,
                                             int d, int row_bytes) {
   if (seq < 0) return 0u;
@@ -109,8 +123,10 @@ __device__ __forceinline__ uint32_t ld_pair(const char* base, int seq, int num_h
 
 template <class Tag, int D>
 __global__ void __launch_bounds__((kMaxG + 1) * 32)
-    paged_attn_shared_kernel(const SharedParams p) {
+    paged_attn_shared_kernel(const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const SharedParams p) {
   using Gm = Geo<D>;
+  constexpr int kRowBytes = D * 2;
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
   const int S = p.stages;
@@ -145,6 +161,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
   }
   if (bad) {
     if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, bad_value);
+    grid_dependency_wait();
     return;
   }
   const int first = __ldg(rec + 2);
@@ -154,7 +171,8 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 2 * kMaxRing * 8);
-  uint8_t* ring = smem + kHeader;
+  const uint32_t smem_base = smem_addr(smem);
+  uint8_t* ring = smem + (((smem_base + kHeader + kAlign - 1) & ~uint32_t(kAlign - 1)) - smem_base);
   const int stage_bytes = G * 2 * Gm::kTileBytes;
 
   if (threadIdx.x == 0) {
@@ -170,12 +188,8 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
   int issued = 0;  // producer lane 0 only: chunks whose copies were issued
   if (warp == G) {
     // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
     const int32_t* table = p.block_tables + static_cast<size_t>(first) * p.max_blocks;
-    const char* kbase = static_cast<const char*>(p.k_cache);
-    const char* vbase = static_cast<const char*>(p.v_cache);
     const int h0 = hg * G;
-    const int copies = G * 2 * kChunk;  // one bulk copy per row
     bool stop = false;
     for (int c0 = 0; c0 < nchunks && !stop; c0 += 32) {
       int blk = 0;
@@ -192,33 +206,30 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
         const int b = __shfl_sync(kFullMask, blk, j);
         const int chunk = c0 + j;
         const int s = chunk % S;
-        int ok = 1;
         if (lane == 0) {
-          if (chunk >= S) ok = mbar_wait_bounded(&empty[s], ((chunk / S) - 1) & 1) ? 1 : 0;
+          bool ok = true;
+          if (chunk >= S) ok = mbar_wait_bounded(&empty[s], ((chunk / S) - 1) & 1);
           if (!ok) {
             *abort_flag = 1;
             report_error(p.err, PA_ERR_TIMEOUT, first, chunk);
           } else {
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(copies) * Gm::kRowBytes);
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
+            // the chunk's rows of (block b, head h) are rows y .. y + 15 of the
+            // cache viewed as [num_blocks * H * bs][D]
+            const int row0 = (tok_begin + chunk * kChunk) % p.block_size;
+            uint8_t* dst = ring + s * stage_bytes;
+            for (int w = 0; w < G; ++w) {
+              const int y = (b * p.num_heads + h0 + w) * p.block_size + row0;
+#pragma unroll
+              for (int cg = 0; cg < Gm::kGroups; ++cg) {
+                tma_load_2d(dst + (w * 2) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_k, cg * 64,
+                            y, &full[s]);
+                tma_load_2d(dst + (w * 2 + 1) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_v,
+                            cg * 64, y, &full[s]);
+              }
+            }
             ++issued;
           }
-        }
-        __syncwarp();
-        if (!__shfl_sync(kFullMask, ok, 0)) {
-          stop = true;
-          break;
-        }
-        const int row0 = (tok_begin + chunk * kChunk) % p.block_size;
-        uint8_t* dst = ring + s * stage_bytes;
-        for (int i = lane; i < copies; i += 32) {
-          const int w = i / (2 * kChunk);
-          const int kv = (i / kChunk) & 1;
-          const int row = i % kChunk;
-          const size_t off =
-              ((static_cast<size_t>(b) * p.num_heads + h0 + w) * p.block_size + row0 + row) *
-              Gm::kRowBytes;
-          bulk_g2s(dst + (w * 2 + kv) * Gm::kTileBytes + row * Gm::kPitch,
-                   (kv ? vbase : kbase) + off, Gm::kRowBytes, &full[s], policy);
         }
         __syncwarp();
         if (__shfl_sync(kFullMask, *abort_flag, 0)) {
@@ -238,10 +249,10 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int d0 = kk * 16 + 2 * tq;
-      qa[kk][0] = ld_pair(qb, seq_lo, p.num_heads, h, d0, Gm::kRowBytes);
-      qa[kk][1] = ld_pair(qb, seq_hi, p.num_heads, h, d0, Gm::kRowBytes);
-      qa[kk][2] = ld_pair(qb, seq_lo, p.num_heads, h, d0 + 8, Gm::kRowBytes);
-      qa[kk][3] = ld_pair(qb, seq_hi, p.num_heads, h, d0 + 8, Gm::kRowBytes);
+      qa[kk][0] = ld_pair(qb, seq_lo, p.num_heads, h, d0, kRowBytes);
+      qa[kk][1] = ld_pair(qb, seq_hi, p.num_heads, h, d0, kRowBytes);
+      qa[kk][2] = ld_pair(qb, seq_lo, p.num_heads, h, d0 + 8, kRowBytes);
+      qa[kk][3] = ld_pair(qb, seq_hi, p.num_heads, h, d0 + 8, kRowBytes);
     }
     float o[D / 8][4];
 #pragma unroll
@@ -252,9 +263,12 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
     // matrix i.  K (B operand of S, no transpose): matrices (tokens 0-7, d+0..7),
     // (0-7, d+8..15), (8-15, d+0..7), (8-15, d+8..15).  V (B operand of P.V,
     // transposed): (tokens 0-7, d+0..7), (8-15, d+0..7), (0-7, d+8..15), (8-15, d+8..15).
+    // Token t's 16-byte chunk c of a 64-column group sits at t * 128 + (c ^ (t & 7)) * 16,
+    // and t & 7 is this lane's r8.
     const int mi = lane >> 3, r8 = lane & 7;
-    const uint32_t k_lane = static_cast<uint32_t>(((mi >> 1) * 8 + r8) * Gm::kPitch + (mi & 1) * 16);
-    const uint32_t v_lane = static_cast<uint32_t>(((mi & 1) * 8 + r8) * Gm::kPitch + (mi >> 1) * 16);
+    const uint32_t k_row = static_cast<uint32_t>(((mi >> 1) * 8 + r8) * 128);
+    const uint32_t v_row = static_cast<uint32_t>(((mi & 1) * 8 + r8) * 128);
+    const int k_half = mi & 1, v_half = mi >> 1;
     const uint32_t ring_addr = smem_addr(ring);
 
     for (int chunk = 0; chunk < nchunks; ++chunk) {
@@ -275,7 +289,8 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         uint32_t b[4];
-        ldsm_x4(kt + k_lane + kk * 32, b);
+        const int c = ((kk & 3) << 1) | k_half;
+        ldsm_x4(kt + (kk >> 2) * Gm::kGroupBytes + k_row + ((c ^ r8) << 4), b);
         mma(sc[0], qa[kk], b[0], b[1], Tag{});
         mma(sc[1], qa[kk], b[2], b[3], Tag{});
       }
@@ -325,7 +340,8 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
 #pragma unroll
       for (int dd = 0; dd < D / 16; ++dd) {
         uint32_t b[4];
-        ldsm_x4_trans(vt + v_lane + dd * 32, b);
+        const int c = ((dd & 3) << 1) | v_half;
+        ldsm_x4_trans(vt + (dd >> 2) * Gm::kGroupBytes + v_row + ((c ^ r8) << 4), b);
         mma(o[2 * dd], ph, b[0], b[1], Tag{});
         mma(o[2 * dd], pl, b[0], b[1], Tag{});
         mma(o[2 * dd + 1], ph, b[2], b[3], Tag{});
@@ -379,6 +395,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
       mbar_wait_bounded(&full[s], (last / S) & 1);
     }
   }
+  grid_dependency_wait();
 }
 
 template <class Tag, int D>
@@ -396,25 +413,45 @@ cudaError_t ensure_shared_smem_attr(int device) {
 }
 
 template <class Tag, int D>
-int launch_t(const SharedParams& p, cudaStream_t stream) {
+int launch_t(const SharedParams& p, bool programmatic, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (ensure_shared_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
-  const dim3 grid(p.num_heads / p.heads_per_cta, p.num_records);
-  const dim3 block((p.heads_per_cta + 1) * 32);
-  paged_attn_shared_kernel<Tag, D><<<grid, block,
-                                     shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages),
-                                     stream>>>(p);
+  // the caches as [num_blocks * H * bs][D] row-major, boxes of 16 rows x 64 columns
+  const unsigned long long rows =
+      static_cast<unsigned long long>(p.num_blocks) * p.num_heads * p.block_size;
+  if (rows >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, kChunk};
+  CUtensorMap tk, tv;
+  const bool bf16 = std::is_same<Tag, BF16>::value;
+  if (!encode_tensor_map(&tk, bf16, p.k_cache, 2, dims, strides, box) ||
+      !encode_tensor_map(&tv, bf16, p.v_cache, 2, dims, strides, box))
+    return PA_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.num_heads / p.heads_per_cta, p.num_records);
+  cfg.blockDim = dim3((p.heads_per_cta + 1) * 32);
+  cfg.dynamicSmemBytes = shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_attn_shared_kernel<Tag, D>, tk, tv, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
 
 size_t shared_kernel_smem_bytes(int head_dim, int heads_per_cta, int stages) {
-  return kHeader + static_cast<size_t>(stages) * heads_per_cta * 2 * kChunk * (head_dim * 2 + 16);
+  return kHeader + kAlign + static_cast<size_t>(stages) * heads_per_cta * 2 * kChunk * head_dim * 2;
 }
 
-int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, cudaStream_t stream) {
+int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, bool programmatic,
+                             cudaStream_t stream) {
   if (p.num_records == 0) return PA_OK;
   if (p.num_records < 0 || p.num_records > 65535 || p.heads_per_cta < 1 ||
       p.heads_per_cta > kMaxG || p.num_heads % p.heads_per_cta != 0 || p.stages < 2 ||
@@ -424,9 +461,15 @@ int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, cud
     return PA_ERR_INVALID_ARG;
   const bool bf16 = dtype == PA_BF16;
   switch (head_dim) {
-    case 64: return bf16 ? launch_t<BF16, 64>(p, stream) : launch_t<F16, 64>(p, stream);
-    case 128: return bf16 ? launch_t<BF16, 128>(p, stream) : launch_t<F16, 128>(p, stream);
-    case 256: return bf16 ? launch_t<BF16, 256>(p, stream) : launch_t<F16, 256>(p, stream);
+    case 64:
+      return bf16 ? launch_t<BF16, 64>(p, programmatic, stream)
+                  : launch_t<F16, 64>(p, programmatic, stream);
+    case 128:
+      return bf16 ? launch_t<BF16, 128>(p, programmatic, stream)
+                  : launch_t<F16, 128>(p, programmatic, stream);
+    case 256:
+      return bf16 ? launch_t<BF16, 256>(p, programmatic, stream)
+                  : launch_t<F16, 256>(p, programmatic, stream);
     default: return PA_ERR_UNSUPPORTED;
   }
 }

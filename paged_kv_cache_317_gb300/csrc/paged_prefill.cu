@@ -38,13 +38,12 @@
 //    TMEM and returns.  Nothing traps.
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace pagedkv {
 namespace {
@@ -117,24 +116,6 @@ struct PrefillParams {
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -634,31 +615,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-bool encode(CUtensorMap* map, bool bf16, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  const cuuint32_t elem[3] = {1, 1, 1};
-  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-            static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, elem,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool BF16, int D>
 cudaError_t ensure_prefill_smem(int device) {
   static std::atomic<uint64_t> done{0};
@@ -737,9 +693,9 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   const cuuint64_t cdims[2] = {static_cast<cuuint64_t>(head_dim), cache_rows};
   const cuuint64_t cstr[1] = {static_cast<cuuint64_t>(head_dim) * 2};
   const cuuint32_t cbox[2] = {64, 16};
-  if (!encode(&tq, bf16, q, 3, qdims, qstr, qbox) ||
-      !encode(&tk, bf16, k_cache, 2, cdims, cstr, cbox) ||
-      !encode(&tv, bf16, v_cache, 2, cdims, cstr, cbox))
+  if (!encode_tensor_map(&tq, bf16, q, 3, qdims, qstr, qbox) ||
+      !encode_tensor_map(&tk, bf16, k_cache, 2, cdims, cstr, cbox) ||
+      !encode_tensor_map(&tv, bf16, v_cache, 2, cdims, cstr, cbox))
     return PA_ERR_CUDA;
 
   PrefillParams p{};

@@ -186,3 +186,44 @@ def test_bad_shared_record_is_recorded_and_skipped(B):
         B.paged_attn_decode(fam.q, fam.kc, fam.vc, torch.from_numpy(tables).cuda(),
                             torch.from_numpy(lens).cuda(), fam.scale, partition_tokens=128,
                             shared_records=torch.from_numpy(recs).cuda())
+
+
+def test_long_shared_pass_eager_and_in_a_cuda_graph(B):
+    """Almost all the work in shared partitions and a short per-sequence pass: the
+    merge must still follow the shared pass, launched eagerly or replayed from a
+    CUDA graph."""
+    fam = Families(B, 61, prompts=[2000, 1600], members=12, tail_max=3, H=8, D=128, bs=16,
+                   dtype="bf16", fused=True)
+    tables, lens = fam.tables()
+    pt = 128
+    items, recs = B.share_plan(tables, lens, pt, 16)
+    assert len(recs) >= 2 * 12 and len(items) <= len(lens) * 2
+    eager = fam.decode(tables, lens, pt, items, recs)
+    fam.check(eager, lens, "long shared pass, eager")
+    bt, sl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    it, rc = torch.from_numpy(items).cuda(), torch.from_numpy(recs).cuda()
+    nr = torch.from_numpy(fam.new_rows).cuda()
+    nk, nv = fam.store_k[nr], fam.store_v[nr]
+    ws = torch.empty(B.paged_attn_workspace_size(len(lens), 8, 128, 16, tables.shape[1], pt),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(eager)
+    step = lambda: B.paged_attn_decode_append(fam.q, nk, nv, fam.kc, fam.vc, bt, sl, fam.scale,
+                                              out=out, partition_tokens=pt, workspace=ws,
+                                              work_items=it, shared_records=rc,
+                                              error_record=fam.rec)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        out.zero_()
+        ws.fill_(0xff)                                   # stale partials would show as NaN
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
