@@ -227,3 +227,26 @@ def test_long_shared_pass_eager_and_in_a_cuda_graph(B):
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_shared_random_configuration(B, seed):
+    rng = np.random.default_rng(7000 + seed)
+    D = int(rng.choice([64, 128, 256]))
+    bs = int(rng.choice([16, 32]))
+    H = int(rng.choice([1, 2, 3, 4, 8]))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    fused = bool(rng.integers(0, 2))
+    pt = int(rng.choice([16, 64, 128, 256]))
+    families = int(rng.integers(1, 4))
+    prompts = [int(x) for x in rng.integers(1, 900, size=families)]
+    fam = Families(B, 8000 + seed, prompts=prompts, members=int(rng.integers(1, 20)),
+                   tail_max=int(rng.integers(0, 200)), H=H, D=D, bs=bs, dtype=dtype, fused=fused)
+    tables, lens = fam.tables()
+    order = None if seed % 3 else rng.permutation(len(lens))
+    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused, order=order)
+    out_dtype = [torch.float32, torch.float16, torch.bfloat16][int(rng.integers(0, 3))]
+    out = fam.decode(tables, lens, pt, items, recs, out_dtype=out_dtype)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, f"seed {seed}: D{D} bs{bs} H{H} {dtype} pt{pt} fused={fused} "
+                         f"{len(recs)} records")
