@@ -250,3 +250,27 @@ def test_shared_random_configuration(B, seed):
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, f"seed {seed}: D{D} bs{bs} H{H} {dtype} pt{pt} fused={fused} "
                          f"{len(recs)} records")
+
+
+def test_single_member_records_match_oracle(B):
+    """A record may hold one sequence (the plan never makes one, a caller may): it
+    computes that sequence's partition like the per-sequence pass."""
+    fam = Families(B, 91, prompts=[900, 500], members=2, tail_max=100, H=4, D=128, bs=16,
+                   dtype="f16", fused=True)
+    tables, lens = fam.tables()
+    pt = 128
+    P = -(-tables.shape[1] * 16 // pt)
+    items = B.partition_work_items(lens, pt, tables.shape[1], 16)
+    keep, recs = [], []
+    for it in items:
+        i, p = divmod(int(it), P)
+        if (p + 1) * pt <= int(lens[i]) - 1 and p % 2 == 0:     # every other full partition
+            r = np.full(B.PA_SHARE_RECORD_WORDS, -1, dtype=np.int32)
+            r[:3] = (p, 1, i)
+            recs.append(r)
+        else:
+            keep.append(it)
+    assert len(recs) >= 4
+    out = fam.decode(tables, lens, pt, np.array(keep, dtype=np.int32), np.stack(recs))
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, "single-member records")
