@@ -52,7 +52,7 @@ extern "C" {
 
 #define PAGEDKV_VERSION 2
 #define PA_ERROR_RECORD_WORDS 4
-#define PA_SHARE_MAX_MEMBERS 16
+#define PA_SHARE_MAX_MEMBERS 8
 #define PA_SHARE_RECORD_WORDS (2 + PA_SHARE_MAX_MEMBERS)
 
 typedef enum pa_status {

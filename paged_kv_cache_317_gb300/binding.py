@@ -42,7 +42,7 @@ class pa_decode_opts(ctypes.Structure):
                 ("shared_records", c_void_p), ("num_shared", c_int)]
 
 
-PA_SHARE_MAX_MEMBERS = 16
+PA_SHARE_MAX_MEMBERS = 8
 PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
 
 

@@ -3,7 +3,7 @@
 // and beam candidates point their block tables at the same physical blocks).
 //
 // The plain partition kernel streams a shared block once for every sequence
-// that holds it.  Here one thread block takes one shared partition of up to 16
+// that holds it.  Here one thread block takes one shared partition of up to 8
 // sequences ("members": their tables name the same physical blocks over the
 // whole partition) and reads each K/V chunk once for all of their queries.
 //  * Producer warp: per 16-token chunk, looks the block up in the first
@@ -12,17 +12,22 @@
 //    (128-byte swizzle), so that the consumers' 8x8 matrix loads (ldmatrix)
 //    hit 32 different banks.  (One 1-D bulk copy per row at a padded pitch
 //    does the same with 8x as many copies, and ran at 2.8 TB/s.)
-//  * One consumer warp per head: the members' queries are the 16 rows of the A
-//    operand of mma.sync m16n8k16 (rows past the member count are zero).  Per
-//    chunk: S = Q.K^T in fp32 (2 x D/16 MMAs), the online softmax of each row in
-//    log2 units, then O += P.V with P split into a high and a low half-precision
-//    part (2 x 2 x D/16 MMAs), so that P keeps about 16 significant bits and the
-//    result stays well inside the fp32 path's error.
+//  * One consumer warp per head, on mma.sync m16n8k16 with the chunk's 16
+//    tokens as the M rows and the (up to 8) members as the N columns: S^T =
+//    K.Q^T in fp32 (D/16 MMAs per chunk), the online softmax of each member's
+//    column in log2 units, then O^T += V^T.P^T with P split into a high and a
+//    low half-precision part (2 x D/16 MMAs; an 8x8 register transpose turns
+//    P's accumulator layout into the B operand), so that P keeps about 16
+//    significant bits and the result stays well inside the fp32 path's error.
+//    (Members as the 16 M rows instead take twice the MMAs and registers for
+//    the <= 8 members that forked samples and beams have; both run at the
+//    same speed on GB300, where this pass is bound by memory latency and the
+//    last wave of its equal-length blocks, not by the tensor pipe.)
 //  * Each member gets the same (m, l, acc) partial the plain kernel would write
 //    for that partition, so the log-sum-exp merge combines it with the member's
 //    other partitions.  A member whose only partition this is gets its output
 //    row directly.
-// The contraction is 16 x 16 x D per chunk and head, below the smallest tcgen05
+// The contraction is 16 x 8 x D per chunk and head, below the smallest tcgen05
 // tile, and the kernel is bound by HBM, so the warp-level MMA is enough.
 // Every wait is bounded, every index read from device memory is checked, and a
 // record that breaks the rules is recorded and skipped.
@@ -104,6 +109,25 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
+// (lane 4 r + c holds elements (r, 2 c) and (r, 2 c + 1)).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// One fp32 value stored as `dtype` at element `elem` of `out`.
+__device__ __forceinline__ void store_one(void* out, size_t elem, float v, int dtype) {
+  if (dtype == PA_F32) {
+    static_cast<float*>(out)[elem] = v;
+  } else if (dtype == PA_BF16) {
+    static_cast<__nv_bfloat16*>(out)[elem] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[elem] = __float2half_rn(v);
+  }
+}
+
 // This kernel may run as a programmatic dependent of the per-sequence partition
 // pass (it reads nothing that pass writes, so it starts early and fills the
 // SMs the pass's last wave leaves idle).  Each block waits for that pass to
@@ -122,7 +146,7 @@ __device__ __forceinline__ uint32_t ld_pair(const char* base, int seq, int num_h
 }
 
 template <class Tag, int D>
-__global__ void __launch_bounds__((kMaxG + 1) * 32)
+__global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
     paged_attn_shared_kernel(const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const SharedParams p) {
   using Gm = Geo<D>;
@@ -135,7 +159,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
   const int32_t* rec = p.records + static_cast<size_t>(blockIdx.y) * kRecord;
 
   // Check the record (every thread reaches the same verdict): partition in
-  // range, 1..16 members, each a valid sequence whose length covers the whole
+  // range, 1..8 members, each a valid sequence whose length covers the whole
   // partition (and, with a fused append, the appended token lies past it).
   const int part = __ldg(rec);
   const int m = __ldg(rec + 1);
@@ -240,35 +264,38 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
     }
   } else {
     // ------------------------------------------------------------ consumer
+    // Per chunk, on mma.sync m16n8k16 with the chunk's 16 tokens as the M rows and
+    // the (up to 8) members as the N columns: S^T = K.Q^T (K as the A operand,
+    // Q^T as B), the online softmax of each member's column in log2 units, then
+    // O^T += V^T.P^T (V^T as A, P^T as B, P in high + low half-precision parts).
+    // Lane (g, tq), g = lane / 4, tq = lane % 4, holds the scores of tokens g and
+    // g + 8 for members 2 tq and 2 tq + 1, and the output of dims 16 dd + g and
+    // 16 dd + g + 8 for the same two members.
     const int h = hg * G + warp;
     const int g = lane >> 2, tq = lane & 3;
-    const int seq_lo = g < m ? __ldg(rec + 2 + g) : -1;          // member of row g
-    const int seq_hi = g + 8 < m ? __ldg(rec + 2 + g + 8) : -1;  // member of row g + 8
     const char* qb = static_cast<const char*>(p.q);
-    uint32_t qa[D / 16][4];
+    const int seq_b = g < m ? __ldg(rec + 2 + g) : -1;  // member of B column g
+    uint32_t qf[D / 16][2];                              // Q^T as B fragments
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const int d0 = kk * 16 + 2 * tq;
-      qa[kk][0] = ld_pair(qb, seq_lo, p.num_heads, h, d0, kRowBytes);
-      qa[kk][1] = ld_pair(qb, seq_hi, p.num_heads, h, d0, kRowBytes);
-      qa[kk][2] = ld_pair(qb, seq_lo, p.num_heads, h, d0 + 8, kRowBytes);
-      qa[kk][3] = ld_pair(qb, seq_hi, p.num_heads, h, d0 + 8, kRowBytes);
+      qf[kk][0] = ld_pair(qb, seq_b, p.num_heads, h, kk * 16 + 2 * tq, kRowBytes);
+      qf[kk][1] = ld_pair(qb, seq_b, p.num_heads, h, kk * 16 + 8 + 2 * tq, kRowBytes);
     }
-    float o[D / 8][4];
+    float o[D / 16][4];
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    for (int dd = 0; dd < D / 16; ++dd) o[dd][0] = o[dd][1] = o[dd][2] = o[dd][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // members 2 tq, 2 tq + 1
 
     // ldmatrix row addresses of this lane: lanes 8i..8i+7 name the rows of
-    // matrix i.  K (B operand of S, no transpose): matrices (tokens 0-7, d+0..7),
-    // (0-7, d+8..15), (8-15, d+0..7), (8-15, d+8..15).  V (B operand of P.V,
-    // transposed): (tokens 0-7, d+0..7), (8-15, d+0..7), (0-7, d+8..15), (8-15, d+8..15).
+    // matrix i.  K (A operand, no transpose): matrices (tokens 0-7, d+0..7),
+    // (8-15, d+0..7), (0-7, d+8..15), (8-15, d+8..15).  V (A operand of V^T,
+    // transposed): (tokens 0-7, d+0..7), (0-7, d+8..15), (8-15, d+0..7), (8-15, d+8..15).
     // Token t's 16-byte chunk c of a 64-column group sits at t * 128 + (c ^ (t & 7)) * 16,
     // and t & 7 is this lane's r8.
     const int mi = lane >> 3, r8 = lane & 7;
-    const uint32_t k_row = static_cast<uint32_t>(((mi >> 1) * 8 + r8) * 128);
-    const uint32_t v_row = static_cast<uint32_t>(((mi & 1) * 8 + r8) * 128);
-    const int k_half = mi & 1, v_half = mi >> 1;
+    const uint32_t k_row = static_cast<uint32_t>(((mi & 1) * 8 + r8) * 128);
+    const uint32_t v_row = static_cast<uint32_t>(((mi >> 1) * 8 + r8) * 128);
+    const int k_half = mi >> 1, v_half = mi & 1;
     const uint32_t ring_addr = smem_addr(ring);
 
     for (int chunk = 0; chunk < nchunks; ++chunk) {
@@ -284,103 +311,94 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32)
       const uint32_t kt = ring_addr + s * stage_bytes + warp * 2 * Gm::kTileBytes;
       const uint32_t vt = kt + Gm::kTileBytes;
 
-      // scores of the 16 tokens: sc[j] covers tokens 8j..8j+7
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};  // (token g, 2 tq), (g, 2 tq + 1), (g + 8, ...)
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t b[4];
+        uint32_t a[4];
         const int c = ((kk & 3) << 1) | k_half;
-        ldsm_x4(kt + (kk >> 2) * Gm::kGroupBytes + k_row + ((c ^ r8) << 4), b);
-        mma(sc[0], qa[kk], b[0], b[1], Tag{});
-        mma(sc[1], qa[kk], b[2], b[3], Tag{});
+        ldsm_x4(kt + (kk >> 2) * Gm::kGroupBytes + k_row + ((c ^ r8) << 4), a);
+        mma(sc, a, qf[kk][0], qf[kk][1], Tag{});
       }
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[j][e] *= p.qscale;
+      for (int e = 0; e < 4; ++e) sc[e] *= p.qscale;
 
-      // online softmax of rows g (elements 0, 1) and g + 8 (elements 2, 3); a
-      // row's 16 scores sit on the four lanes of a quad
-      float cm_lo = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      float cm_hi = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-      cm_lo = fmaxf(cm_lo, __shfl_xor_sync(kFullMask, cm_lo, 1));
-      cm_hi = fmaxf(cm_hi, __shfl_xor_sync(kFullMask, cm_hi, 1));
-      cm_lo = fmaxf(cm_lo, __shfl_xor_sync(kFullMask, cm_lo, 2));
-      cm_hi = fmaxf(cm_hi, __shfl_xor_sync(kFullMask, cm_hi, 2));
-      const float mn_lo = fmaxf(m_lo, cm_lo), mn_hi = fmaxf(m_hi, cm_hi);
-      const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);
-      float pr[2][4];
+      // a member's 16 scores sit on the 8 lanes of equal tq, two per lane
+      float c0 = fmaxf(sc[0], sc[2]), c1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        pr[j][0] = exp2f(sc[j][0] - mn_lo);
-        pr[j][1] = exp2f(sc[j][1] - mn_lo);
-        pr[j][2] = exp2f(sc[j][2] - mn_hi);
-        pr[j][3] = exp2f(sc[j][3] - mn_hi);
+      for (int off = 4; off < 32; off <<= 1) {
+        c0 = fmaxf(c0, __shfl_xor_sync(kFullMask, c0, off));
+        c1 = fmaxf(c1, __shfl_xor_sync(kFullMask, c1, off));
       }
-      l_lo = fmaf(l_lo, a_lo, (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]));
-      l_hi = fmaf(l_hi, a_hi, (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]));
-      if (__any_sync(kFullMask, a_lo != 1.f || a_hi != 1.f)) {
+      const float mn0 = fmaxf(m0, c0), mn1 = fmaxf(m1, c1);
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(sc[0] - mn0), p1 = exp2f(sc[1] - mn1);
+      const float p2 = exp2f(sc[2] - mn0), p3 = exp2f(sc[3] - mn1);
+      l0 = fmaf(l0, a0, p0 + p2);
+      l1 = fmaf(l1, a1, p1 + p3);
+      if (__any_sync(kFullMask, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-          o[nt][0] *= a_lo;
-          o[nt][1] *= a_lo;
-          o[nt][2] *= a_hi;
-          o[nt][3] *= a_hi;
+        for (int dd = 0; dd < D / 16; ++dd) {
+          o[dd][0] *= a0;
+          o[dd][1] *= a1;
+          o[dd][2] *= a0;
+          o[dd][3] *= a1;
         }
       }
-      m_lo = mn_lo;
-      m_hi = mn_hi;
+      m0 = mn0;
+      m1 = mn1;
 
-      // P as the A operand (keys 0..15 along k), in high and low parts
-      uint32_t ph[4], pl[4];
-      split2(pr[0][0], pr[0][1], ph[0], pl[0], Tag{});
-      split2(pr[0][2], pr[0][3], ph[1], pl[1], Tag{});
-      split2(pr[1][0], pr[1][1], ph[2], pl[2], Tag{});
-      split2(pr[1][2], pr[1][3], ph[3], pl[3], Tag{});
+      // P^T as the B operand: the C layout holds (token, two members); an 8x8
+      // transpose per half (tokens 0-7, 8-15) gives (two tokens, member)
+      uint32_t hi_a, lo_a, hi_b, lo_b;
+      split2(p0, p1, hi_a, lo_a, Tag{});
+      split2(p2, p3, hi_b, lo_b, Tag{});
+      const uint32_t bh0 = movmatrix_trans(hi_a), bh1 = movmatrix_trans(hi_b);
+      const uint32_t bl0 = movmatrix_trans(lo_a), bl1 = movmatrix_trans(lo_b);
 #pragma unroll
       for (int dd = 0; dd < D / 16; ++dd) {
-        uint32_t b[4];
+        uint32_t a[4];
         const int c = ((dd & 3) << 1) | v_half;
-        ldsm_x4_trans(vt + (dd >> 2) * Gm::kGroupBytes + v_row + ((c ^ r8) << 4), b);
-        mma(o[2 * dd], ph, b[0], b[1], Tag{});
-        mma(o[2 * dd], pl, b[0], b[1], Tag{});
-        mma(o[2 * dd + 1], ph, b[2], b[3], Tag{});
-        mma(o[2 * dd + 1], pl, b[2], b[3], Tag{});
+        ldsm_x4_trans(vt + (dd >> 2) * Gm::kGroupBytes + v_row + ((c ^ r8) << 4), a);
+        mma(o[dd], a, bh0, bh1, Tag{});
+        mma(o[dd], a, bl0, bl1, Tag{});
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
     }
 
-    l_lo += __shfl_xor_sync(kFullMask, l_lo, 1);
-    l_hi += __shfl_xor_sync(kFullMask, l_hi, 1);
-    l_lo += __shfl_xor_sync(kFullMask, l_lo, 2);
-    l_hi += __shfl_xor_sync(kFullMask, l_hi, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFullMask, l0, off);
+      l1 += __shfl_xor_sync(kFullMask, l1, off);
+    }
     if (!*abort_flag) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int seq = half ? seq_hi : seq_lo;
-        if (seq < 0) continue;
-        const float mrow = half ? m_hi : m_lo, lrow = half ? l_hi : l_lo;
+      for (int e = 0; e < 2; ++e) {
+        const int mm = 2 * tq + e;
+        if (mm >= m) continue;
+        const int seq = __ldg(rec + 2 + mm);
+        const float mrow = e ? m1 : m0, lrow = e ? l1 : l0;
         const int L = __ldg(p.seq_lens + seq);
         const int nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
+        const size_t base = (static_cast<size_t>(seq) * p.num_heads + h) * D + g;
         if (nparts == 1) {
           const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll
-          for (int nt = 0; nt < D / 8; ++nt) {
-            const float v2[2] = {o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv};
-            store_out<2>(p.out, (static_cast<size_t>(seq) * p.num_heads + h) * D + nt * 8 + 2 * tq,
-                         v2, p.out_dtype);
+          for (int dd = 0; dd < D / 16; ++dd) {
+            store_one(p.out, base + dd * 16, o[dd][e] * inv, p.out_dtype);
+            store_one(p.out, base + dd * 16 + 8, o[dd][2 + e] * inv, p.out_dtype);
           }
         } else {
           const size_t row =
               (static_cast<size_t>(seq) * p.num_heads + h) * p.num_partitions + part;
-          float* dst = p.ws_acc + row * D + 2 * tq;
+          float* dst = p.ws_acc + row * D + g;
 #pragma unroll
-          for (int nt = 0; nt < D / 8; ++nt)
-            *reinterpret_cast<float2*>(dst + nt * 8) =
-                make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
-          if (tq == 0) p.ws_ml[row] = make_float2(mrow, lrow);
+          for (int dd = 0; dd < D / 16; ++dd) {
+            dst[dd * 16] = o[dd][e];
+            dst[dd * 16 + 8] = o[dd][2 + e];
+          }
+          if (g == 0) p.ws_ml[row] = make_float2(mrow, lrow);
         }
       }
     }

@@ -126,8 +126,8 @@ def _plan_by_definition(tables, lens, pt, bs, fused, order=None):
             if share[i] > p:
                 groups.setdefault(tuple(tables[i, b0:b1 + 1]), []).append(i)
         for grp in groups.values():
-            for at in range(0, len(grp) - 1, 16):
-                mem = tuple(grp[at:at + 16])
+            for at in range(0, len(grp) - 1, B.PA_SHARE_MAX_MEMBERS):
+                mem = tuple(grp[at:at + B.PA_SHARE_MAX_MEMBERS])
                 recs.add((p, mem))
                 covered.update((i, p) for i in mem)
     order = sorted(range(N), key=lambda i: (-int(lens[i]), i)) if order is None else order
@@ -164,7 +164,7 @@ def test_share_plan_matches_its_definition():
         assert _records_as_set(recs) == want_recs, trial
         assert np.array_equal(items, want_items), trial
         for r in recs:
-            assert 2 <= r[1] <= 16 and (r[2 + r[1]:] == -1).all()
+            assert 2 <= r[1] <= B.PA_SHARE_MAX_MEMBERS and (r[2 + r[1]:] == -1).all()
 
 
 def test_share_plan_on_forked_sequences():
@@ -200,9 +200,9 @@ def test_share_plan_on_forked_sequences():
         pairs += [(i, p) for i in mem]
     want = [(i, p) for i in range(len(ids)) for p in range(max(1, -(-int(lens[i]) // pt)))]
     assert sorted(pairs) == sorted(want)
-    # the 21 holders of the long prompt share its 15 full partitions: 16 + 5 members each
-    sizes = sorted(int(r[1]) for r in recs if int(r[1]) in (16, 5))
-    assert sizes.count(16) >= 15 and sizes.count(5) >= 15
+    # the 21 holders of the long prompt share its 15 full partitions: 8 + 8 + 5 members each
+    sizes = [int(r[1]) for r in recs]
+    assert sizes.count(8) >= 30 and sizes.count(5) >= 15
 
 
 def test_share_plan_rejects_bad_arguments():

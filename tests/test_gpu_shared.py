@@ -144,12 +144,12 @@ def test_shared_and_plain_paths_agree(B):
     fam.check(shared, lens, "shared vs plain")
 
 
-def test_more_than_sixteen_members_split_into_records(B):
+def test_more_than_eight_members_split_into_records(B):
     fam = Families(B, 33, prompts=[600], members=21, tail_max=40, H=2, D=128, bs=16,
                    dtype="bf16", fused=True)
     tables, lens = fam.tables()
     items, recs = B.share_plan(tables, lens, 64, 16)
-    assert sorted(set(int(r[1]) for r in recs)) == [5, 16]
+    assert sorted(set(int(r[1]) for r in recs)) == [5, 8]
     out = fam.decode(tables, lens, 64, items, recs)
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, "21 members")
