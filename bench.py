@@ -717,7 +717,10 @@ def run_workload(args, rank, world, local_rank):
                      "rc": torch.empty((n_items_max, RW), dtype=torch.int32, device=dev)}
                     for _ in range(2)]
         host_s, stage_s, plan_s, lens_seen, n_shared = 0.0, 0.0, 0.0, 0, 0
-        split = []   # per step: events before copies, before table uploads, before decode, after
+        # per step: events before copies, before table uploads, before decode, after
+        # (created before the loop: creating events costs host time every step)
+        split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                 for _ in range(plan.steps)]
         t0 = time.perf_counter()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
@@ -734,7 +737,7 @@ def run_workload(args, rank, world, local_rank):
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs = split[s_]
             evs[0].record(stream)
             if len(pairs):
                 B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
@@ -768,7 +771,6 @@ def run_workload(args, rank, world, local_rank):
                                        work_items=it_d,
                                        shared_records=ds["rc"][: len(recs)] if len(recs) else None)
             evs[3].record(stream)
-            split.append(evs)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
@@ -842,7 +844,8 @@ def run_workload(args, rank, world, local_rank):
                     for _ in range(2)]
         torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
-        split = []
+        split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                 for _ in range(plan.steps)]
         t0 = time.perf_counter()
         ev0 = torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
@@ -860,7 +863,7 @@ def run_workload(args, rank, world, local_rank):
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
             copies += len(pairs)
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs = split[s_]
             evs[0].record(stream)
             if len(pairs):
                 B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
@@ -893,7 +896,6 @@ def run_workload(args, rank, world, local_rank):
                                        work_items=ds["it"][: len(items)],
                                        shared_records=ds["rc"][: len(recs)] if len(recs) else None)
             evs[3].record(stream)
-            split.append(evs)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
