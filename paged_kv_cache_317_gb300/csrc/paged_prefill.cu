@@ -207,6 +207,14 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float x0, float x1) {
       : "f"(x0), "f"(x1));
 }
 
+// (y0, y1) = (a0 - b0, a1 - b1), one packed instruction, same rounding as scalar fp32.
+__device__ __forceinline__ void sub2(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32;
 // relative error ~2^-22, 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -507,11 +515,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
         const float e0 = ex2_approx(x0);
         const float e1 = ex2_approx(x1);
         add2(sum4[c & 2], sum4[(c & 2) + 1], e0, e1);
-        const uint32_t hi = pack_half2<BF16>(e0, e1);
-        const float r0 = half_to_float<BF16>(hi & 0xffffu);
-        const float r1 = half_to_float<BF16>(hi >> 16);
-        hi_f[c / 2] = __uint_as_float(hi);
-        lo_f[c / 2] = __uint_as_float(pack_half2<BF16>(e0 - r0, e1 - r1));
+        if constexpr (BF16) {
+          // hi = the upper 16 bits of each fp32 p (a bf16 truncation), one byte
+          // permute for the pair; lo = RN(p - hi), where p - hi is exact in fp32
+          // and below one bf16 ulp of p, so hi + lo keeps ~16 significant bits
+          const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
+          float d0, d1;
+          sub2(d0, d1, e0, e1, __uint_as_float(b0 & 0xffff0000u),
+               __uint_as_float(b1 & 0xffff0000u));
+          hi_f[c / 2] = __uint_as_float(__byte_perm(b0, b1, 0x7632));
+          lo_f[c / 2] = __uint_as_float(pack_half2<true>(d0, d1));
+        } else {
+          const uint32_t hi = pack_half2<false>(e0, e1);
+          const float r0 = half_to_float<false>(hi & 0xffffu);
+          const float r1 = half_to_float<false>(hi >> 16);
+          hi_f[c / 2] = __uint_as_float(hi);
+          lo_f[c / 2] = __uint_as_float(pack_half2<false>(e0 - r0, e1 - r1));
+        }
       }
       const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // O must not change under a running P.V: rescaling waits for P.V(j-1).
