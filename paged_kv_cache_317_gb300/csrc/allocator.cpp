@@ -10,8 +10,8 @@
 #include <algorithm>
 #include <cstdint>
 #include <new>
+#include <utility>
 #include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "pagedkv.h"
@@ -21,11 +21,35 @@ struct pa_allocator {
     std::vector<int32_t> blocks;
     int32_t len = 0;
   };
+  using Map = std::unordered_map<int64_t, Seq>;
   int32_t num_blocks = 0;
   int32_t block_size = 0;
   std::vector<int32_t> free_stack;
   std::vector<int32_t> refcount;
-  std::unordered_map<int64_t, Seq> seqs;
+  Map seqs;
+  // Map nodes of freed sequences, kept for reuse with their block vectors'
+  // capacity: a loop that forks and frees about as many sequences per step (beam
+  // search) then allocates no host memory in steady state.
+  std::vector<Map::node_type> spare;
+  static constexpr size_t kMaxSpare = size_t(1) << 16;
+
+  // A new, empty sequence `id` (the caller checked that it does not exist).
+  Seq& make(int64_t id) {
+    if (!spare.empty()) {
+      Map::node_type nh = std::move(spare.back());
+      spare.pop_back();
+      nh.key() = id;
+      nh.mapped().blocks.clear();
+      nh.mapped().len = 0;
+      return seqs.insert(std::move(nh)).position->second;
+    }
+    return seqs.emplace(id, Seq{}).first->second;
+  }
+  // Drop a sequence whose blocks were released; its node goes to `spare`.
+  void retire(Map::iterator it) {
+    Map::node_type nh = seqs.extract(it);
+    if (spare.size() < kMaxSpare) spare.push_back(std::move(nh));
+  }
 
   int32_t take() {
     const int32_t b = free_stack.back();
@@ -113,11 +137,10 @@ extern "C" int pa_seq_add(pa_allocator* a, int64_t seq, int32_t num_tokens) {
   const int32_t need = a->blocks_for(num_tokens);
   if (need > static_cast<int32_t>(a->free_stack.size())) return PA_ERR_OOM;
   try {
-    pa_allocator::Seq s;
+    pa_allocator::Seq& s = a->make(seq);
     s.blocks.reserve(need);
     for (int32_t i = 0; i < need; ++i) s.blocks.push_back(a->take());
     s.len = num_tokens;
-    a->seqs.emplace(seq, std::move(s));
   } catch (...) {
     return PA_ERR_OOM;
   }
@@ -130,9 +153,11 @@ extern "C" int pa_seq_fork(pa_allocator* a, int64_t parent, int64_t child) {
   if (it == a->seqs.end()) return PA_ERR_NO_SEQ;
   if (a->seqs.count(child)) return PA_ERR_SEQ_EXISTS;
   try {
-    pa_allocator::Seq copy = it->second;
-    for (int32_t b : copy.blocks) ++a->refcount[b];
-    a->seqs.emplace(child, std::move(copy));
+    const pa_allocator::Seq& p = it->second;  // element references survive rehashing
+    pa_allocator::Seq& c = a->make(child);
+    c.blocks = p.blocks;
+    c.len = p.len;
+    for (int32_t b : c.blocks) ++a->refcount[b];
   } catch (...) {
     return PA_ERR_OOM;
   }
@@ -154,7 +179,7 @@ extern "C" int pa_seq_free(pa_allocator* a, int64_t seq) {
   int status = PA_OK;
   for (int32_t b : it->second.blocks)
     if (!a->release(b)) status = PA_ERR_REFCOUNT;
-  a->seqs.erase(it);
+  a->retire(it);
   return status;
 }
 
@@ -250,18 +275,31 @@ extern "C" int pa_batch_fork(pa_allocator* a, const int64_t* parents, const int6
   if (!a || n < 0 || (n > 0 && (!parents || !children))) return PA_ERR_INVALID_ARG;
   try {
     // Check every pair in order (a child forked earlier in the batch may be a
-    // later parent) before changing anything.
-    std::unordered_set<int64_t> added;
+    // later parent) before changing anything: children new and distinct, every
+    // parent an existing sequence or an earlier child.
+    std::vector<std::pair<int64_t, int32_t>> kids(static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i) kids[i] = {children[i], i};
+    std::sort(kids.begin(), kids.end());
+    for (int32_t i = 1; i < n; ++i)
+      if (kids[i].first == kids[i - 1].first) return PA_ERR_SEQ_EXISTS;
+    std::vector<const pa_allocator::Seq*> src(static_cast<size_t>(n), nullptr);
     for (int32_t i = 0; i < n; ++i) {
-      if (!a->seqs.count(parents[i]) && !added.count(parents[i])) return PA_ERR_NO_SEQ;
-      if (a->seqs.count(children[i]) || !added.insert(children[i]).second)
-        return PA_ERR_SEQ_EXISTS;
+      if (a->seqs.count(children[i])) return PA_ERR_SEQ_EXISTS;
+      auto it = a->seqs.find(parents[i]);
+      if (it != a->seqs.end()) {
+        src[i] = &it->second;  // element references survive rehashing
+        continue;
+      }
+      auto k = std::lower_bound(kids.begin(), kids.end(), std::make_pair(parents[i], int32_t(0)));
+      if (k == kids.end() || k->first != parents[i] || k->second >= i) return PA_ERR_NO_SEQ;
     }
     a->seqs.reserve(a->seqs.size() + static_cast<size_t>(n));
     for (int32_t i = 0; i < n; ++i) {
-      pa_allocator::Seq copy = a->seqs.at(parents[i]);
-      for (int32_t b : copy.blocks) ++a->refcount[b];
-      a->seqs.emplace(children[i], std::move(copy));
+      const pa_allocator::Seq* p = src[i] ? src[i] : &a->seqs.find(parents[i])->second;
+      pa_allocator::Seq& c = a->make(children[i]);
+      c.blocks = p->blocks;
+      c.len = p->len;
+      for (int32_t b : c.blocks) ++a->refcount[b];
     }
   } catch (...) {
     return PA_ERR_OOM;
@@ -271,21 +309,26 @@ extern "C" int pa_batch_fork(pa_allocator* a, const int64_t* parents, const int6
 
 extern "C" int pa_batch_free(pa_allocator* a, const int64_t* seqs, int32_t n) {
   if (!a || n < 0 || (n > 0 && !seqs)) return PA_ERR_INVALID_ARG;
+  std::vector<pa_allocator::Map::iterator> its;
   try {
-    std::unordered_set<int64_t> seen;
+    std::vector<int64_t> ids(seqs, seqs + n);
+    std::sort(ids.begin(), ids.end());
+    for (int32_t i = 1; i < n; ++i)
+      if (ids[i] == ids[i - 1]) return PA_ERR_NO_SEQ;  // listed twice
+    its.resize(static_cast<size_t>(n));
     for (int32_t i = 0; i < n; ++i) {
-      if (!a->seqs.count(seqs[i])) return PA_ERR_NO_SEQ;
-      if (!seen.insert(seqs[i]).second) return PA_ERR_NO_SEQ;  // listed twice
+      its[i] = a->seqs.find(seqs[i]);
+      if (its[i] == a->seqs.end()) return PA_ERR_NO_SEQ;
     }
   } catch (...) {
     return PA_ERR_OOM;
   }
+  // Retiring one sequence leaves the others' iterators valid.
   int status = PA_OK;
   for (int32_t i = 0; i < n; ++i) {
-    auto it = a->seqs.find(seqs[i]);
-    for (int32_t b : it->second.blocks)
+    for (int32_t b : its[i]->second.blocks)
       if (!a->release(b)) status = PA_ERR_REFCOUNT;
-    a->seqs.erase(it);
+    a->retire(its[i]);
   }
   return status;
 }

@@ -323,3 +323,56 @@ def test_batch_fork_and_free_are_all_or_nothing(lib):
         assert (cpp.num_seqs(), cpp.num_free()) == before[:2]
     cpp.batch_free([0, 1])
     assert cpp.num_seqs() == 0 and cpp.num_free() == 50
+
+
+def test_beam_churn_reuses_sequences_exactly(lib):
+    """Whole-batch fork/free rounds (beam search) recycle the allocator's freed
+    sequence records; tables, lengths and refcounts follow the model exactly, and
+    a refused batch changes nothing."""
+    from paged_kv_cache_317_gb300.binding import BlockAllocator, PagedKVError
+    rng = np.random.default_rng(12)
+    order = rng.permutation(3000).astype(np.int32)
+    alloc, model = BlockAllocator(3000, 16, order), BlockAllocatorModel(3000, 16, order)
+    beams, next_id = [], 0
+    for g in range(8):
+        n = int(rng.integers(20, 200))
+        alloc.add(next_id, n)
+        model.add(next_id, n)
+        beams.append(next_id)
+        next_id += 1
+    for step in range(40):
+        parents = [int(rng.choice(beams)) for _ in beams]
+        children = list(range(next_id, next_id + len(beams)))
+        next_id += len(beams)
+        alloc.batch_fork(parents, children)
+        for p, c in zip(parents, children):
+            model.fork(p, c)
+        alloc.batch_free(beams)
+        for b in beams:
+            model.free_seq(b)
+        beams = children
+        for b in beams:
+            for _ in range(int(rng.integers(0, 20))):
+                assert alloc.append(b) == model.append(b)
+        for b in beams:
+            assert alloc.block_table(b) == model.tables[b]
+            assert alloc.length(b) == model.lens[b]
+        alloc.check()
+        _same_state(alloc, model)
+    # refused batches leave everything as it was
+    before = {b: alloc.block_table(b) for b in beams}
+    free_before = alloc.num_free()
+    with pytest.raises(PagedKVError, match="SEQ_EXISTS"):
+        alloc.batch_fork([beams[0], beams[1]], [next_id, next_id])          # child twice
+    with pytest.raises(PagedKVError, match="SEQ_EXISTS"):
+        alloc.batch_fork([beams[0]], [beams[1]])                            # child exists
+    with pytest.raises(PagedKVError, match="NO_SEQ"):
+        alloc.batch_fork([next_id + 1, beams[0]], [next_id, next_id + 1])   # parent only later
+    with pytest.raises(PagedKVError, match="NO_SEQ"):
+        alloc.batch_free([beams[0], beams[0]])                              # listed twice
+    with pytest.raises(PagedKVError, match="NO_SEQ"):
+        alloc.batch_free([beams[0], next_id + 5])                           # unknown id
+    assert alloc.num_free() == free_before
+    assert {b: alloc.block_table(b) for b in beams} == before
+    alloc.batch_free(beams)
+    assert alloc.num_free() == 3000
