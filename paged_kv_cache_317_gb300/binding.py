@@ -85,7 +85,7 @@ def decode_partition_tokens(seq_lens, num_heads: int, heads_per_cta: int = 0,
     lens = _host_int32(seq_lens, "seq_lens")
     out = ctypes.c_int32()
     _check(load_library().pa_decode_partition_tokens(
-        lens.ctypes.data_as(P_int32), len(lens), num_heads, heads_per_cta, num_sms,
+        lens.ctypes.data, len(lens), num_heads, heads_per_cta, num_sms,
         ctypes.byref(out)), "pa_decode_partition_tokens")
     return out.value
 
@@ -102,13 +102,13 @@ def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: in
         ordarr = _host_int32(order, "order")
         if ordarr.shape != lens.shape:
             raise ValueError("order must hold one entry per sequence")
-        ordp = ordarr.ctypes.data_as(P_int32)
+        ordp = ordarr.ctypes.data
     lib, n = load_library(), ctypes.c_int32()
-    args = (lens.ctypes.data_as(P_int32), len(lens), partition_tokens, max_blocks_per_seq,
+    args = (lens.ctypes.data, len(lens), partition_tokens, max_blocks_per_seq,
             block_size, ordp)
     _check(lib.pa_decode_work_items(*args, None, 0, ctypes.byref(n)), "pa_decode_work_items")
     items = np.empty(n.value, dtype=np.int32)
-    _check(lib.pa_decode_work_items(*args, items.ctypes.data_as(P_int32), n.value,
+    _check(lib.pa_decode_work_items(*args, items.ctypes.data, n.value,
                                     ctypes.byref(n)), "pa_decode_work_items")
     return items
 
@@ -130,17 +130,17 @@ def share_plan(block_tables, seq_lens, partition_tokens: int, block_size: int,
         ordarr = _host_int32(order, "order")
         if ordarr.shape != lens.shape:
             raise ValueError("order must hold one entry per sequence")
-        ordp = ordarr.ctypes.data_as(P_int32)
+        ordp = ordarr.ctypes.data
     lib, ni, nr = load_library(), ctypes.c_int32(), ctypes.c_int32()
-    args = (tables.ctypes.data_as(P_int32), lens.ctypes.data_as(P_int32), len(lens),
+    args = (tables.ctypes.data, lens.ctypes.data, len(lens),
             tables.shape[1], block_size, partition_tokens, int(bool(fused_append)), ordp)
     # one call with room for every (sequence, partition) pair; records hold >= 2 each
     pt = partition_tokens or 512
     pairs = len(lens) * max(1, -(-tables.shape[1] * block_size // pt)) if pt > 0 else 0
     items = np.empty(pairs, dtype=np.int32)
     recs = np.empty((pairs // 2, PA_SHARE_RECORD_WORDS), dtype=np.int32)
-    _check(lib.pa_decode_share_plan(*args, items.ctypes.data_as(P_int32), len(items),
-                                    ctypes.byref(ni), recs.ctypes.data_as(P_int32), len(recs),
+    _check(lib.pa_decode_share_plan(*args, items.ctypes.data, len(items),
+                                    ctypes.byref(ni), recs.ctypes.data, len(recs),
                                     ctypes.byref(nr)), "pa_decode_share_plan")
     return items[: ni.value], recs[: nr.value]
 
@@ -178,11 +178,11 @@ SIGNATURES = {
                                 c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
     "block_copy": (c_int, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_int, c_void_p,
                            c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
-    "pa_decode_partition_tokens": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32]),
-    "pa_decode_work_items": (c_int, [P_int32, c_int, c_int, c_int, c_int, P_int32, P_int32,
+    "pa_decode_partition_tokens": (c_int, [c_void_p, c_int, c_int, c_int, c_int, P_int32]),
+    "pa_decode_work_items": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                                      c_int32, P_int32]),
-    "pa_decode_share_plan": (c_int, [P_int32, P_int32, c_int, c_int, c_int, c_int, c_int,
-                                     P_int32, P_int32, c_int32, P_int32, P_int32, c_int32,
+    "pa_decode_share_plan": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                     c_void_p, c_void_p, c_int32, P_int32, c_void_p, c_int32,
                                      P_int32]),
     "pa_alloc_create": (c_void_p, [c_int32, c_int32, P_int32]),
     "pa_alloc_destroy": (None, [c_void_p]),
@@ -192,14 +192,14 @@ SIGNATURES = {
     "pa_seq_free": (c_int, [c_void_p, c_int64]),
     "pa_seq_len": (c_int, [c_void_p, c_int64, P_int32]),
     "pa_seq_block_table": (c_int, [c_void_p, c_int64, P_int32, c_int32, P_int32]),
-    "pa_seq_slots": (c_int, [c_void_p, c_int64, c_int32, c_int32, P_int64]),
+    "pa_seq_slots": (c_int, [c_void_p, c_int64, c_int32, c_int32, c_void_p]),
     "pa_block_refcount": (c_int, [c_void_p, c_int32, P_int32]),
     "pa_num_free_blocks": (c_int32, [c_void_p]),
     "pa_num_seqs": (c_int32, [c_void_p]),
-    "pa_batch_append": (c_int, [c_void_p, P_int64, c_int32, P_int64, P_int64, P_int32]),
-    "pa_batch_fork": (c_int, [c_void_p, P_int64, P_int64, c_int32]),
-    "pa_batch_free": (c_int, [c_void_p, P_int64, c_int32]),
-    "pa_batch_block_tables": (c_int, [c_void_p, P_int64, c_int32, c_int32, P_int32, P_int32]),
+    "pa_batch_append": (c_int, [c_void_p, c_void_p, c_int32, c_void_p, c_void_p, P_int32]),
+    "pa_batch_fork": (c_int, [c_void_p, c_void_p, c_void_p, c_int32]),
+    "pa_batch_free": (c_int, [c_void_p, c_void_p, c_int32]),
+    "pa_batch_block_tables": (c_int, [c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
     "pa_alloc_stats": (c_int, [c_void_p, P_int32, P_int64, P_int64, P_int64]),
     "pa_alloc_check": (c_int, [c_void_p]),
 }
@@ -502,7 +502,7 @@ class BlockAllocator:
         import numpy as np
         out = np.empty(count, dtype=np.int64)
         _check(self._lib.pa_seq_slots(self._h, seq, start, count,
-                                      out.ctypes.data_as(P_int64)), "pa_seq_slots")
+                                      out.ctypes.data), "pa_seq_slots")
         return out
 
     def refcount(self, block: int) -> int:
@@ -523,9 +523,9 @@ class BlockAllocator:
         slots = np.empty(n, dtype=np.int64)
         pairs = np.empty((max(n, 1), 2), dtype=np.int64)
         nc = ctypes.c_int32()
-        _check(self._lib.pa_batch_append(self._h, ids.ctypes.data_as(P_int64), n,
-                                         slots.ctypes.data_as(P_int64),
-                                         pairs.ctypes.data_as(P_int64), ctypes.byref(nc)),
+        _check(self._lib.pa_batch_append(self._h, ids.ctypes.data, n,
+                                         slots.ctypes.data,
+                                         pairs.ctypes.data, ctypes.byref(nc)),
                "pa_batch_append")
         return slots, pairs[: nc.value].copy()
 
@@ -536,15 +536,15 @@ class BlockAllocator:
         chi = np.ascontiguousarray(children, dtype=np.int64)
         if par.shape != chi.shape:
             raise ValueError("parents and children differ in length")
-        _check(self._lib.pa_batch_fork(self._h, par.ctypes.data_as(P_int64),
-                                       chi.ctypes.data_as(P_int64), par.shape[0]),
+        _check(self._lib.pa_batch_fork(self._h, par.ctypes.data,
+                                       chi.ctypes.data, par.shape[0]),
                "pa_batch_fork")
 
     def batch_free(self, seqs) -> None:
         """End every listed sequence; all-or-nothing."""
         import numpy as np
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
-        _check(self._lib.pa_batch_free(self._h, ids.ctypes.data_as(P_int64), ids.shape[0]),
+        _check(self._lib.pa_batch_free(self._h, ids.ctypes.data, ids.shape[0]),
                "pa_batch_free")
 
     def batch_block_tables(self, seqs, max_blocks: int):
@@ -553,9 +553,9 @@ class BlockAllocator:
         n = ids.shape[0]
         tables = np.empty((n, max_blocks), dtype=np.int32)
         lens = np.empty(n, dtype=np.int32)
-        _check(self._lib.pa_batch_block_tables(self._h, ids.ctypes.data_as(P_int64), n, max_blocks,
-                                               tables.ctypes.data_as(P_int32),
-                                               lens.ctypes.data_as(P_int32)),
+        _check(self._lib.pa_batch_block_tables(self._h, ids.ctypes.data, n, max_blocks,
+                                               tables.ctypes.data,
+                                               lens.ctypes.data),
                "pa_batch_block_tables")
         return tables, lens
 
