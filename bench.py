@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 PREFILL_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_prefill.cu",
                    "paged_kv_cache_317_gb300/csrc/tma.cuh",
                    "paged_kv_cache_317_gb300/csrc/common.cuh")
-DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/paged_attn_decode.cu",
+DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/decode_partition.cuh",
                   "paged_kv_cache_317_gb300/csrc/decode_config.h",
                   "paged_kv_cache_317_gb300/csrc/common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
