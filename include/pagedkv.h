@@ -238,7 +238,9 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  * they read host arrays, write host arrays and enqueue nothing.  Results feed
  * paged_attn_workspace_size, partition_tokens and pa_decode_opts.work_items of
  * paged_attn_decode_ex / paged_attn_decode_append; the outputs of the decode are
- * the same whatever is chosen, up to fp32 rounding order across partitions.
+ * the same whatever is chosen, up to fp32 rounding order across partitions.  The
+ * lengths and tables are the same for every layer of a model, so one schedule
+ * (and one share plan) serves all the layers of a decode step.
  *
  * pa_decode_partition_tokens: writes to *partition_tokens the longest of 512,
  * 256 and 128 for which the heaviest block, min(partition, max_i L_i) tokens,
