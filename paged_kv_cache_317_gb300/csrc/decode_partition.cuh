@@ -98,6 +98,13 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[TPR / 2], int c) {
   return v[0] + __shfl_xor_sync(kFullMask, v[0], 1);
 }
 
+// Waits for the grid this pass may depend on programmatically (the pass over
+// shared partitions) to complete, so that the merge after this pass also
+// follows that one.  A no-op without such a prerequisite.
+__device__ __forceinline__ void wait_prerequisite() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int seq, bool report) {
   int L = p.seq_lens[seq];
   const int cap = p.max_blocks * p.block_size;
@@ -131,6 +138,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     const int item = __ldg(p.work_items + blockIdx.y);
     if (item < 0 || item / p.num_partitions >= p.num_seqs) {
       if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, item);
+      wait_prerequisite();
       return;
     }
     seq = item / p.num_partitions;
@@ -140,13 +148,17 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     if (static_cast<unsigned>(seq) >= static_cast<unsigned>(p.num_seqs)) {
       if (threadIdx.x == 0 && hg == 0 && part == 0)
         report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.z, seq);
+      wait_prerequisite();
       return;
     }
   }
 
   const int L = clamp_len(p, seq, threadIdx.x == 0 && hg == 0 && part == 0);
   const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
-  if (part >= nparts) return;
+  if (part >= nparts) {
+    wait_prerequisite();
+    return;
+  }
   const int tok_begin = part * p.partition_tokens;
   const int tok_end = min(L, tok_begin + p.partition_tokens);
   const int nchunks = (max(0, tok_end - tok_begin) + kChunk - 1) / kChunk;
@@ -376,6 +388,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
       mbar_wait_bounded(&full[s], (last / S) & 1);
     }
   }
+  wait_prerequisite();
 }
 
 }  // namespace

@@ -37,11 +37,9 @@ struct SharedParams {
 // Shared memory of one block of the shared-partition kernel.
 size_t shared_kernel_smem_bytes(int head_dim, int heads_per_cta, int stages);
 
-// Enqueue the kernel over all records; returns a pa_status.  With
-// `programmatic`, it is launched as a programmatic dependent of the kernel just
-// enqueued on `stream` (which must trigger its dependents) and its blocks wait
-// for that kernel to complete before they exit.
-int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, bool programmatic,
-                             cudaStream_t stream);
+// Enqueue the kernel over all records; returns a pa_status.  Its blocks trigger
+// programmatic dependents when they start (the per-sequence partition pass is
+// launched after it as one).
+int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, cudaStream_t stream);
 
 }  // namespace pagedkv

@@ -107,23 +107,39 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (phases & 1) {
-    // The per-sequence partition pass first; the pass over shared partitions
-    // (if any) follows as its programmatic dependent, so its long, uniform blocks
-    // start as soon as every block of the first pass has started and fill the
-    // SMs that pass's ragged last wave leaves idle.  The two write disjoint
-    // partials; the shared pass's blocks wait for the first pass to complete
-    // before they exit, so the merge after it follows both.
+    // The pass over shared partitions (if any) first: its blocks are long and of
+    // equal length, and trigger their dependents when they start.  The
+    // per-sequence partition pass follows as a programmatic dependent, so its
+    // blocks (longest first, then ever shorter) fill the SMs the shared pass's
+    // last wave leaves idle.  The two write disjoint partials; each block of the
+    // second pass waits for the first to complete before it exits, so the merge
+    // after it follows both.
+    if (shared != nullptr) {
+      const int st = launch_shared_partitions(*shared, dtype, D, stream);
+      if (st != PA_OK) return st;
+    }
     if (ensure_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(p.num_heads / p.heads_per_cta, p.num_partitions, num_seqs);
     if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
     dim3 block((p.heads_per_cta + 1) * 32);
     if (grid.y > 0) {
-      paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
+      if (shared != nullptr) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, paged_attn_partition_kernel<Tag, D>, p) != cudaSuccess)
+          return PA_ERR_CUDA;
+      } else {
+        paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
+      }
       if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (shared != nullptr) {
-      const int st = launch_shared_partitions(*shared, dtype, D, grid.y > 0, stream);
-      if (st != PA_OK) return st;
     }
   }
   if ((phases & 2) && p.num_partitions > 1) {

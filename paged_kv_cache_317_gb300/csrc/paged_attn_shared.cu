@@ -128,16 +128,6 @@ __device__ __forceinline__ void store_one(void* out, size_t elem, float v, int d
   }
 }
 
-// This kernel may run as a programmatic dependent of the per-sequence partition
-// pass (it reads nothing that pass writes, so it starts early and fills the
-// SMs the pass's last wave leaves idle).  Each block waits for that pass to
-// complete before it exits, so that whatever follows this kernel in the stream
-// or graph (the merge) also follows the partition pass.  Without a
-// prerequisite grid the wait returns at once.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __device__ __forceinline__ uint32_t ld_pair(const char* base, int seq, int num_heads, int h,
                                             int d, int row_bytes) {
   if (seq < 0) return 0u;
@@ -151,6 +141,11 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
                              const __grid_constant__ CUtensorMap tm_v, const SharedParams p) {
   using Gm = Geo<D>;
   constexpr int kRowBytes = D * 2;
+  // The per-sequence partition pass follows as a programmatic dependent (it
+  // reads nothing this pass writes): let it start once every block here has.
+  // Its blocks wait for this pass to complete before they exit, so the merge
+  // after it follows both.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
   const int S = p.stages;
@@ -185,7 +180,6 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   }
   if (bad) {
     if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, bad_value);
-    grid_dependency_wait();
     return;
   }
   const int first = __ldg(rec + 2);
@@ -413,7 +407,6 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
       mbar_wait_bounded(&full[s], (last / S) & 1);
     }
   }
-  grid_dependency_wait();
 }
 
 template <class Tag, int D>
@@ -431,7 +424,7 @@ cudaError_t ensure_shared_smem_attr(int device) {
 }
 
 template <class Tag, int D>
-int launch_t(const SharedParams& p, bool programmatic, cudaStream_t stream) {
+int launch_t(const SharedParams& p, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   if (ensure_shared_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
@@ -447,18 +440,11 @@ int launch_t(const SharedParams& p, bool programmatic, cudaStream_t stream) {
   if (!encode_tensor_map(&tk, bf16, p.k_cache, 2, dims, strides, box) ||
       !encode_tensor_map(&tv, bf16, p.v_cache, 2, dims, strides, box))
     return PA_ERR_CUDA;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(p.num_heads / p.heads_per_cta, p.num_records);
-  cfg.blockDim = dim3((p.heads_per_cta + 1) * 32);
-  cfg.dynamicSmemBytes = shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_attn_shared_kernel<Tag, D>, tk, tv, p) != cudaSuccess)
-    return PA_ERR_CUDA;
+  const dim3 grid(p.num_heads / p.heads_per_cta, p.num_records);
+  const dim3 block((p.heads_per_cta + 1) * 32);
+  paged_attn_shared_kernel<Tag, D><<<grid, block,
+                                     shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages),
+                                     stream>>>(tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -468,8 +454,7 @@ size_t shared_kernel_smem_bytes(int head_dim, int heads_per_cta, int stages) {
   return kHeader + kAlign + static_cast<size_t>(stages) * heads_per_cta * 2 * kChunk * head_dim * 2;
 }
 
-int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, bool programmatic,
-                             cudaStream_t stream) {
+int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, cudaStream_t stream) {
   if (p.num_records == 0) return PA_OK;
   if (p.num_records < 0 || p.num_records > 65535 || p.heads_per_cta < 1 ||
       p.heads_per_cta > kMaxG || p.num_heads % p.heads_per_cta != 0 || p.stages < 2 ||
@@ -480,14 +465,11 @@ int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, boo
   const bool bf16 = dtype == PA_BF16;
   switch (head_dim) {
     case 64:
-      return bf16 ? launch_t<BF16, 64>(p, programmatic, stream)
-                  : launch_t<F16, 64>(p, programmatic, stream);
+      return bf16 ? launch_t<BF16, 64>(p, stream) : launch_t<F16, 64>(p, stream);
     case 128:
-      return bf16 ? launch_t<BF16, 128>(p, programmatic, stream)
-                  : launch_t<F16, 128>(p, programmatic, stream);
+      return bf16 ? launch_t<BF16, 128>(p, stream) : launch_t<F16, 128>(p, stream);
     case 256:
-      return bf16 ? launch_t<BF16, 256>(p, programmatic, stream)
-                  : launch_t<F16, 256>(p, programmatic, stream);
+      return bf16 ? launch_t<BF16, 256>(p, stream) : launch_t<F16, 256>(p, stream);
     default: return PA_ERR_UNSUPPORTED;
   }
 }
