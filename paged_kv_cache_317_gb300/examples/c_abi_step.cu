@@ -1,7 +1,8 @@
 // A decode step driven through the C ABI alone (include/pagedkv.h and
 // libpagedkv.so; no Python): host allocator, KV append, copy-on-write block
-// copy, the host decode schedule and paged decode attention.  It checks two
-// exact properties:
+// copy, the host decode schedule (and a second plan that reads the blocks a
+// fork shares with its parent once for both) and paged decode attention.  It
+// checks two exact properties, on both decodes:
 //  * a sequence forked from another and given the same next token decodes to
 //    the same bits as its parent, although its last block is a private copy;
 //  * a one-token sequence returns its value row exactly (one weight of 1).
@@ -9,6 +10,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -181,15 +184,75 @@ int main() {
       return 1;
     }
   }
+
+  // The same decode with 16-token partitions, reading the two full blocks that
+  // sequence 0 and its fork share once for both (pa_decode_share_plan records).
+  const int pt2 = 16;
+  int32_t n_items2 = 0, n_recs = 0;
+  CHECK(pa_decode_share_plan(tables.data(), lens.data(), 3, kMaxBlocks, kBlock, pt2, 0, nullptr,
+                             nullptr, 0, &n_items2, nullptr, 0, &n_recs));
+  std::vector<int32_t> items2(n_items2), recs(static_cast<size_t>(n_recs) * PA_SHARE_RECORD_WORDS);
+  CHECK(pa_decode_share_plan(tables.data(), lens.data(), 3, kMaxBlocks, kBlock, pt2, 0, nullptr,
+                             items2.data(), n_items2, &n_items2, recs.data(), n_recs, &n_recs));
+  if (n_recs != 2 || recs[1] != 2) {
+    std::fprintf(stderr, "expected 2 shared records of 2 members, got %d\n", n_recs);
+    return 1;
+  }
+  int32_t *items2_d = nullptr, *recs_d = nullptr;
+  CUDA(cudaMalloc(&items2_d, items2.size() * sizeof(int32_t)));
+  CUDA(cudaMalloc(&recs_d, recs.size() * sizeof(int32_t)));
+  CUDA(cudaMemcpy(items2_d, items2.data(), items2.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(recs_d, recs.data(), recs.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  pa_decode_opts opts2{};
+  opts2.work_items = items2_d;
+  opts2.num_work_items = n_items2;
+  opts2.shared_records = recs_d;
+  opts2.num_shared = n_recs;
+  const size_t ws2 = paged_attn_workspace_size(3, kHeads, kDim, kBlock, kMaxBlocks, pt2);
+  void* workspace2 = nullptr;
+  float* out2 = nullptr;
+  if (ws2) CUDA(cudaMalloc(&workspace2, ws2));
+  CUDA(cudaMalloc(&out2, o.size() * sizeof(float)));
+  CHECK(paged_attn_decode_ex(q, kc, vc, tables_d, lens_d, 3, kHeads, kDim, kBlock, kMaxBlocks,
+                             kBlocks, 1.0f / 11.3137085f, PA_F16, out2, PA_F32, pt2, workspace2,
+                             ws2, rec, nullptr, &opts2));
+  CUDA(cudaDeviceSynchronize());
+  CHECK(pa_error_read(rec, err, nullptr));
+  if (err[0] != 0) {
+    std::fprintf(stderr, "device error record (shared): %d %d %d %d\n", err[0], err[1], err[2],
+                 err[3]);
+    return 1;
+  }
+  std::vector<float> o2(3 * row);
+  CUDA(cudaMemcpy(o2.data(), out2, o2.size() * sizeof(float), cudaMemcpyDeviceToHost));
+  if (std::memcmp(o2.data(), o2.data() + row, row * sizeof(float)) != 0) {
+    std::fprintf(stderr, "shared blocks: fork decodes differently from its parent\n");
+    return 1;
+  }
+  for (size_t i = 0; i < row; ++i) {
+    if (o2[2 * row + i] != o[2 * row + i]) {
+      std::fprintf(stderr, "shared blocks: one-token sequence changed at element %zu\n", i);
+      return 1;
+    }
+  }
+  float worst = 0.f;
+  for (size_t i = 0; i < o.size(); ++i) worst = std::max(worst, std::fabs(o2[i] - o[i]));
+  if (!(worst <= 2e-3f)) {
+    std::fprintf(stderr, "shared blocks: output moved by %g from the first decode\n", worst);
+    return 1;
+  }
+
   CHECK(pa_alloc_check(alloc));
   pa_alloc_destroy(alloc);
   for (void* p : {static_cast<void*>(kc), static_cast<void*>(vc), static_cast<void*>(k),
                   static_cast<void*>(v), static_cast<void*>(q), static_cast<void*>(slot_d),
                   static_cast<void*>(pair_d), static_cast<void*>(tables_d),
                   static_cast<void*>(lens_d), static_cast<void*>(out), static_cast<void*>(rec),
-                  static_cast<void*>(items_d), workspace})
+                  static_cast<void*>(items_d), workspace, static_cast<void*>(items2_d),
+                  static_cast<void*>(recs_d), workspace2, static_cast<void*>(out2)})
     if (p) cudaFree(p);
   std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact; "
-              "%d-token partitions, %d work items\n", pt, n_items);
+              "%d-token partitions, %d work items; shared blocks read once: %d records, fork "
+              "still exact, max change %.2e\n", pt, n_items, n_recs, worst);
   return 0;
 }

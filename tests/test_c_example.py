@@ -36,3 +36,4 @@ def test_c_example_runs(lib, tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     assert "ok:" in r.stdout
     assert "64-token partitions" in r.stdout        # the split path with a work list
+    assert "2 records" in r.stdout                  # the shared-partition pass ran
