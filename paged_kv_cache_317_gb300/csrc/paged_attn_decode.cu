@@ -43,26 +43,58 @@ __global__ void __launch_bounds__(256) paged_attn_merge_kernel(const MergeParams
   if (nparts <= 1) return;  // the partition pass wrote this row directly
   const size_t row0 = static_cast<size_t>(gw) * p.num_partitions;
 
-  float M = -INFINITY;
-  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[row0 + i].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
   float o[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-  float lt = 0.f;
-  if (M != -INFINITY) {
-    for (int i = lane; i < nparts; i += 32) {
-      const float2 ml = p.ws_ml[row0 + i];
-      lt = fmaf(exp2f(ml.x - M), ml.y, lt);
+  float M = -INFINITY, lt = 0.f;
+  if (nparts <= 32) {
+    // Lane i holds partition i's (m, l): one load for all of them, weights by
+    // shuffle, and the partials' rows loaded four at a time so that their
+    // latencies overlap.
+    const float2 ml = lane < nparts ? p.ws_ml[row0 + lane] : make_float2(-INFINITY, 0.f);
+    M = ml.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    if (M != -INFINITY) {
+      const float w = lane < nparts ? exp2f(ml.x - M) : 0.f;
+      lt = w * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
+      for (int i0 = 0; i0 < nparts; i0 += 4) {
+        float a[4][DPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = min(i0 + u, nparts - 1);  // repeats are weighted 0 below
+          const float* src = p.ws_acc + (row0 + i) * D + lane * DPL;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) a[u][j] = src[j];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float wu = __shfl_sync(kFullMask, w, min(i0 + u, 31));
+          const float wi = i0 + u < nparts ? wu : 0.f;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) o[j] = fmaf(wi, a[u][j], o[j]);
+        }
+      }
     }
+  } else {
+    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[row0 + i].x);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
-    for (int i = 0; i < nparts; ++i) {
-      const float w = exp2f(p.ws_ml[row0 + i].x - M);
-      const float* a = p.ws_acc + (row0 + i) * D + lane * DPL;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
+    if (M != -INFINITY) {
+      for (int i = lane; i < nparts; i += 32) {
+        const float2 ml = p.ws_ml[row0 + i];
+        lt = fmaf(exp2f(ml.x - M), ml.y, lt);
+      }
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) o[j] = fmaf(w, a[j], o[j]);
+      for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
+      for (int i = 0; i < nparts; ++i) {
+        const float w = exp2f(p.ws_ml[row0 + i].x - M);
+        const float* a = p.ws_acc + (row0 + i) * D + lane * DPL;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[j] = fmaf(w, a[j], o[j]);
+      }
     }
   }
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
