@@ -502,6 +502,51 @@ def _time_graph(fns, K, W, stream, calls_per_graph=32):
     return a.elapsed_time(b) / (reps * calls_per_graph)
 
 
+class _Staging:
+    """Per-step host inputs of a serving loop in one pinned int32 buffer per set
+    (copy-on-write pairs as int64, block tables, lengths, work list,
+    shared-partition records) and one device buffer, uploaded with one copy.
+    Two sets alternate; a set is refilled once the copy that read it is done."""
+
+    def __init__(self, n_seqs, max_blocks, n_items_max, record_words, dev):
+        import torch
+        self.sizes = {"pairs": 4 * n_seqs, "bt": n_seqs * max_blocks, "sl": n_seqs,
+                      "it": n_items_max, "rc": n_items_max * record_words}
+        self.off, at = {}, 0
+        for k, n in self.sizes.items():
+            self.off[k] = at
+            at += n + (-n) % 4           # keep every region 16-byte aligned
+        self.n_seqs, self.max_blocks, self.rw = n_seqs, max_blocks, record_words
+        self.host = [torch.empty(at, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.dev = [torch.empty(at, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+
+    def upload(self, step, stream, pairs, tables, lens, items, recs):
+        """Fill set step % 2 and enqueue its upload; returns device views
+        (pairs int64 [n, 2], tables, lengths, work list, records)."""
+        import numpy as np
+        import torch
+        j = step % 2
+        self.done[j].synchronize()               # the copy that read this set two steps back
+        h, o = self.host[j].numpy(), self.off
+        n_p, n_i, n_r = len(pairs), len(items), len(recs)
+        if n_p:
+            h[o["pairs"]:o["pairs"] + 4 * n_p].view(np.int64)[:] = pairs.ravel()
+        h[o["bt"]:o["bt"] + tables.size] = tables.ravel()
+        h[o["sl"]:o["sl"] + len(lens)] = lens
+        h[o["it"]:o["it"] + n_i] = items
+        h[o["rc"]:o["rc"] + n_r * self.rw] = recs.ravel()
+        used = o["rc"] + n_r * self.rw
+        d = self.dev[j]
+        d[:used].copy_(self.host[j][:used], non_blocking=True)
+        self.done[j].record(stream)
+        return (d[o["pairs"]:o["pairs"] + 4 * n_p].view(torch.int64).view(n_p, 2),
+                d[o["bt"]:o["bt"] + tables.size].view(self.n_seqs, self.max_blocks),
+                d[o["sl"]:o["sl"] + len(lens)],
+                d[o["it"]:o["it"] + n_i],
+                d[o["rc"]:o["rc"] + n_r * self.rw].view(n_r, self.rw) if n_r else None)
+
+
 def run_workload(args, rank, world, local_rank):
     """Device time of one step of the other seeded workloads (decode attention,
     plus the allocator, copies and appends where the workload has them)."""
@@ -702,22 +747,12 @@ def run_workload(args, rank, world, local_rank):
                                                      max_blocks, pt), dtype=torch.uint8,
                          device=dev)
         torch.cuda.synchronize()
-        # per-step host inputs staged in pinned memory (two sets, reused once the
-        # copy that read them two steps back has finished)
+        # per-step host inputs staged in one pinned buffer per set, one upload per step
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
-        pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
-                     "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
-                     "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
-                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32).pin_memory(),
-                     "done": torch.cuda.Event()} for _ in range(2)]
-        dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
-                     "sl": torch.empty(N, dtype=torch.int32, device=dev),
-                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev),
-                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32, device=dev)}
-                    for _ in range(2)]
+        staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         host_s, stage_s, plan_s, lens_seen, n_shared = 0.0, 0.0, 0.0, 0, 0
-        # per step: events before copies, before table uploads, before decode, after
+        # per step: events before the upload, before the copies, before decode, after
         # (created before the loop: creating events costs host time every step)
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                  for _ in range(plan.steps)]
@@ -737,13 +772,7 @@ def run_workload(args, rank, world, local_rank):
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
-            evs = split[s_]
-            evs[0].record(stream)
-            if len(pairs):
-                B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
-            evs[1].record(stream)
             q, k, v = tokens_all[s_]
-            hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
             h2 = time.perf_counter()
             if args.no_share:
                 items = B.partition_work_items(lens, pt, max_blocks, plan.block_size)
@@ -752,30 +781,37 @@ def run_workload(args, rank, world, local_rank):
                 items, recs = B.share_plan(tables, lens, pt, plan.block_size, fused_append=True)
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
-            hs["done"].synchronize()            # the copy that read this buffer set
+            evs = split[s_]
+            evs[0].record(stream)
             h1 = time.perf_counter()
-            hs["bt"].numpy()[:] = tables
-            hs["sl"].numpy()[:] = lens
-            hs["it"].numpy()[: len(items)] = items
-            hs["rc"].numpy()[: len(recs)] = recs
+            pairs_d, bt_d, sl_d, it_d, rc_d = staging.upload(s_, stream, pairs, tables, lens,
+                                                             items, recs)
             stage_s += time.perf_counter() - h1
-            ds["bt"].copy_(hs["bt"], non_blocking=True)
-            ds["sl"].copy_(hs["sl"], non_blocking=True)
-            ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
-            ds["rc"][: len(recs)].copy_(hs["rc"][: len(recs)], non_blocking=True)
-            hs["done"].record(stream)
-            bt_d, sl_d, it_d = ds["bt"], ds["sl"], ds["it"][: len(items)]
+            evs[1].record(stream)
+            if len(pairs):
+                B.block_copy([kc], [vc], pairs_d)
             evs[2].record(stream)
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=it_d,
-                                       shared_records=ds["rc"][: len(recs)] if len(recs) else None)
+                                       work_items=it_d, shared_records=rc_d)
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) / plan.steps
         ms = ev0.elapsed_time(ev1) / plan.steps
+        # the staged inputs of the last step gave the same output as direct uploads
+        # (the fused append rewrites the same rows: idempotent)
+        ref_out = torch.empty_like(out)
+        B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
+                                   torch.from_numpy(lens).to(dev), plan.scale, out=ref_out,
+                                   partition_tokens=pt, workspace=ws, error_record=rec,
+                                   work_items=torch.from_numpy(items).to(dev),
+                                   shared_records=(torch.from_numpy(recs).to(dev)
+                                                   if len(recs) else None))
+        torch.cuda.synchronize()
+        if not torch.equal(ref_out, out):
+            raise RuntimeError("staged and direct inputs gave different outputs")
         seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
         tokens = lens_seen / plan.steps
         total = tokens * plan.num_heads * plan.head_dim * 4
@@ -792,7 +828,7 @@ def run_workload(args, rank, world, local_rank):
                     host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     device_ms_per_step_split={
-                        "block_copy": seg(0, 1), "table_uploads": seg(1, 2),
+                        "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
                         "append_and_decode": seg(2, 3),
                         "note": "the append is fused into the decode launch"},
                     note="value counts K/V bytes only; device time includes copies, H2D "
@@ -832,16 +868,7 @@ def run_workload(args, rank, world, local_rank):
                          dtype=torch.uint8, device=dev)
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
-        pin_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32).pin_memory(),
-                     "sl": torch.empty(N, dtype=torch.int32).pin_memory(),
-                     "it": torch.empty(n_items_max, dtype=torch.int32).pin_memory(),
-                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32).pin_memory(),
-                     "done": torch.cuda.Event()} for _ in range(2)]
-        dev_sets = [{"bt": torch.empty((N, max_blocks), dtype=torch.int32, device=dev),
-                     "sl": torch.empty(N, dtype=torch.int32, device=dev),
-                     "it": torch.empty(n_items_max, dtype=torch.int32, device=dev),
-                     "rc": torch.empty((n_items_max, RW), dtype=torch.int32, device=dev)}
-                    for _ in range(2)]
+        staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -863,13 +890,7 @@ def run_workload(args, rank, world, local_rank):
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
             copies += len(pairs)
-            evs = split[s_]
-            evs[0].record(stream)
-            if len(pairs):
-                B.block_copy([kc], [vc], torch.from_numpy(pairs).to(dev, non_blocking=True))
-            evs[1].record(stream)
             q, k, v = tokens_all[s_]
-            hs, ds = pin_sets[s_ % 2], dev_sets[s_ % 2]
             h2 = time.perf_counter()
             if args.no_share:
                 items = B.partition_work_items(lens, pt, max_blocks, bs)
@@ -878,29 +899,37 @@ def run_workload(args, rank, world, local_rank):
                 items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
-            hs["done"].synchronize()            # the copy that read this buffer set
+            evs = split[s_]
+            evs[0].record(stream)
             h1 = time.perf_counter()
-            hs["bt"].numpy()[:] = tables
-            hs["sl"].numpy()[:] = lens
-            hs["it"].numpy()[: len(items)] = items
-            hs["rc"].numpy()[: len(recs)] = recs
+            pairs_d, bt_d, sl_d, it_d, rc_d = staging.upload(s_, stream, pairs, tables, lens,
+                                                             items, recs)
             stage_s += time.perf_counter() - h1
-            ds["bt"].copy_(hs["bt"], non_blocking=True)
-            ds["sl"].copy_(hs["sl"], non_blocking=True)
-            ds["it"][: len(items)].copy_(hs["it"][: len(items)], non_blocking=True)
-            ds["rc"][: len(recs)].copy_(hs["rc"][: len(recs)], non_blocking=True)
-            hs["done"].record(stream)
+            evs[1].record(stream)
+            if len(pairs):
+                B.block_copy([kc], [vc], pairs_d)
             evs[2].record(stream)
-            B.paged_attn_decode_append(q, k, v, kc, vc, ds["bt"], ds["sl"], plan.scale, out=out,
+            B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=ds["it"][: len(items)],
-                                       shared_records=ds["rc"][: len(recs)] if len(recs) else None)
+                                       work_items=it_d, shared_records=rc_d)
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) / plan.steps
         ms = ev0.elapsed_time(ev1) / plan.steps
+        # the staged inputs of the last step gave the same output as direct uploads
+        # (the fused append rewrites the same rows: idempotent)
+        ref_out = torch.empty_like(out)
+        B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
+                                   torch.from_numpy(lens).to(dev), plan.scale, out=ref_out,
+                                   partition_tokens=pt, workspace=ws, error_record=rec,
+                                   work_items=torch.from_numpy(items).to(dev),
+                                   shared_records=(torch.from_numpy(recs).to(dev)
+                                                   if len(recs) else None))
+        torch.cuda.synchronize()
+        if not torch.equal(ref_out, out):
+            raise RuntimeError("staged and direct inputs gave different outputs")
         seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
         tokens = lens_seen / plan.steps
         total = tokens * H * D * 4
@@ -921,7 +950,7 @@ def run_workload(args, rank, world, local_rank):
                     wall_ms_per_step=round(1e3 * wall, 4),
                     copies_per_step=round(copies / plan.steps, 2),
                     device_ms_per_step_split={
-                        "block_copy": seg(0, 1), "table_uploads": seg(1, 2),
+                        "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
                         "append_and_decode": seg(2, 3),
                         "note": "the append is fused into the decode launch"},
                     note="value counts logical K/V bytes (beams share prefix blocks, so part "
