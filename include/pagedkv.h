@@ -234,8 +234,9 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  *
  * The host holds every sequence's length (it builds the block tables), so it
  * can shape a decode launch to the batch: pick the split-K partition length and
- * list the (sequence, partition) work items.  Both functions are host code only:
- * they read host arrays, write host arrays and enqueue nothing.  Results feed
+ * list the (sequence, partition) work items, and find the partitions that
+ * several sequences share.  These functions are host code only: they read host
+ * arrays, write host arrays and enqueue nothing.  Results feed
  * paged_attn_workspace_size, partition_tokens and pa_decode_opts.work_items of
  * paged_attn_decode_ex / paged_attn_decode_append; the outputs of the decode are
  * the same whatever is chosen, up to fp32 rounding order across partitions.  The
@@ -293,7 +294,9 @@ int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int partition_to
  *   num_items, num_records  out: the counts
  * Returns PA_OK or PA_ERR_INVALID_ARG (as for pa_decode_work_items, or a
  * capacity below a count: the counts are still written, the arrays untouched).
- * Host work: one pass over the table entries of every shareable partition. */
+ * Host work: per partition, a sort of the sequences that hold it by its first
+ * block (blocks are shared only through forks), and an entry-by-entry comparison
+ * of the tables within runs of equal first block. */
 int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                          int max_blocks_per_seq, int block_size, int partition_tokens,
                          int fused_append, const int32_t* order, int32_t* work_items,
