@@ -142,7 +142,7 @@ def _records_as_set(recs):
 def test_share_plan_matches_its_definition():
     rng = np.random.default_rng(5)
     for trial in range(150):
-        bs = int(rng.choice([16, 32]))
+        bs = int(rng.choice([16, 32, 48]))        # 48: partitions cut across blocks
         pt = int(rng.choice([16, 32, 64, 128]))
         N = int(rng.integers(1, 40))
         MB = int(rng.integers(1, 24))
