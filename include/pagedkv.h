@@ -15,7 +15,12 @@
  * ---------------------------------------
  * - Memory: every buffer is owned by the caller.  Pointers marked "device" must
  *   point to memory of the current CUDA device; "host" pointers to host memory.
- *   The library never allocates device memory.
+ *   No call allocates device memory.  The library's device image holds one
+ *   fixed array of PA_NOALLOC_SCRATCH_BYTES, the scratch of
+ *   paged_attn_decode_noalloc; it is resident on a GPU from the moment the
+ *   library's device code is loaded there (at context creation under eager
+ *   module loading, else at the first call) until the process exits, whichever
+ *   entry points are used.
  * - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Kernel entry points are asynchronous on that stream: they return
  *   once the work is enqueued.
@@ -359,9 +364,11 @@ int paged_attn_prefill_ex(const void* q, const int32_t* query_start, int total_q
  *  - Limit: returns PA_ERR_INVALID_ARG, enqueuing nothing, when
  *    paged_attn_workspace_size(...) for these sizes exceeds PA_NOALLOC_SCRATCH_BYTES.
  *  - The array stays resident on every GPU that loads this code until exit.
- *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call before
- *    any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress, which allocates nothing), so the call stays correct
+ *    after cudaDeviceReset or under another driver-API context on the device.
+ *    The first call in a context may load the library's device code there:
+ *    make it before any stream capture.
  *  - All calls share the array and it keeps the last call's contents (nothing
  *    in it needs clearing: every partial is written before it is read).  Calls
  *    whose kernels overlap on the GPU race on it: serialise them.

@@ -10,13 +10,10 @@
 // this library's device image, so the call allocates nothing.
 //
 // The array is PA_NOALLOC_SCRATCH_BYTES (32 MiB) and, once this file's device
-// code is loaded on a GPU, stays resident there until the process exits.  Its
-// device address is looked up once per device, on the first call made with that
-// device current.  All calls share the one array: calls whose kernels overlap on
-// the GPU (different streams, or different host threads) race on it.
+// code is loaded on a GPU, stays resident there until the process exits.  All
+// calls share the one array: calls whose kernels overlap on the GPU (different
+// streams, or different host threads) race on it.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "pagedkv.h"
 
@@ -24,25 +21,17 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_decode_scratch on the current device.  In host code the
+// Device address of g_decode_scratch in the current context.  In host code the
 // array's name is only a host-side stand-in, so the address must come from the
-// runtime; it is cached per device.
+// runtime.  It belongs to the context the module is loaded in, not to the
+// device ordinal: after cudaDeviceReset, or under another driver-API context on
+// the same device, it changes.  So it is looked up on every call (a host-side
+// table lookup once the module is loaded; it allocates nothing).
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> guard(g_lock);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
-      return PA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+    return PA_ERR_CUDA;
+  *out = p;
   return PA_OK;
 }
 
