@@ -6,7 +6,6 @@
 // The partition kernel itself is in decode_partition.cuh.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -118,19 +117,19 @@ int resolve_partition(int partition_tokens) {
   return partition_tokens <= 0 ? kDefaultPartition : partition_tokens;
 }
 
-// Per-instantiation, per-device record of the opt-in shared memory attribute.
+// Opt-in shared memory above the 48 KB default.  The attribute belongs to the
+// module loaded in the current context and is lost with it (cudaDeviceReset,
+// another driver-API context), so it is set on every launch that needs it, to
+// the device's opt-in maximum (concurrent callers then never lower it for one
+// another); a launch within the default sets nothing.
 template <class Tag, int D>
-cudaError_t ensure_smem_attr(int device) {
-  static std::atomic<uint64_t> done{0};
-  const uint64_t bit = device < 64 ? (1ull << device) : 0;
-  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+cudaError_t ensure_smem_attr(int device, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(paged_attn_partition_kernel<Tag, D>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
+  return cudaFuncSetAttribute(paged_attn_partition_kernel<Tag, D>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 template <class Tag, int D>
@@ -150,7 +149,7 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
       const int st = launch_shared_partitions(*shared, dtype, D, stream);
       if (st != PA_OK) return st;
     }
-    if (ensure_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
+    if (ensure_smem_attr<Tag, D>(device, smem) != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(p.num_heads / p.heads_per_cta, p.num_partitions, num_seqs);
     if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
     dim3 block((p.heads_per_cta + 1) * 32);

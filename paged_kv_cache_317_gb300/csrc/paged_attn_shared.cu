@@ -35,7 +35,6 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <type_traits>
 
@@ -409,25 +408,24 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   }
 }
 
+// Opt-in shared memory above the 48 KB default, set on every launch that needs
+// it (the attribute is lost with the context, e.g. after cudaDeviceReset).
 template <class Tag, int D>
-cudaError_t ensure_shared_smem_attr(int device) {
-  static std::atomic<uint64_t> done{0};
-  const uint64_t bit = device < 64 ? (1ull << device) : 0;
-  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+cudaError_t ensure_shared_smem_attr(int device, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(paged_attn_shared_kernel<Tag, D>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
+  return cudaFuncSetAttribute(paged_attn_shared_kernel<Tag, D>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 template <class Tag, int D>
 int launch_t(const SharedParams& p, cudaStream_t stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
-  if (ensure_shared_smem_attr<Tag, D>(device) != cudaSuccess) return PA_ERR_CUDA;
+  const size_t smem = shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages);
+  if (ensure_shared_smem_attr<Tag, D>(device, smem) != cudaSuccess) return PA_ERR_CUDA;
   // the caches as [num_blocks * H * bs][D] row-major, boxes of 16 rows x 64 columns
   const unsigned long long rows =
       static_cast<unsigned long long>(p.num_blocks) * p.num_heads * p.block_size;
@@ -442,9 +440,7 @@ int launch_t(const SharedParams& p, cudaStream_t stream) {
     return PA_ERR_CUDA;
   const dim3 grid(p.num_heads / p.heads_per_cta, p.num_records);
   const dim3 block((p.heads_per_cta + 1) * 32);
-  paged_attn_shared_kernel<Tag, D><<<grid, block,
-                                     shared_kernel_smem_bytes(D, p.heads_per_cta, p.stages),
-                                     stream>>>(tk, tv, p);
+  paged_attn_shared_kernel<Tag, D><<<grid, block, smem, stream>>>(tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

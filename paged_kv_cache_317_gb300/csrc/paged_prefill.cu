@@ -39,7 +39,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -635,22 +634,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
 }
 
 // ------------------------------------------------------------------ host side
+// The kernel always needs opt-in shared memory.  The attribute belongs to the
+// module loaded in the current context and is lost with it (cudaDeviceReset,
+// another driver-API context), so it is set on every launch.
 template <bool BF16, int D>
-cudaError_t ensure_prefill_smem(int device) {
-  static std::atomic<uint64_t> done{0};
-  const uint64_t bit = device < 64 ? (1ull << device) : 0;
-  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(paged_prefill_kernel<BF16, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<D>::kSmemBytes);
-  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
+cudaError_t ensure_prefill_smem() {
+  return cudaFuncSetAttribute(paged_prefill_kernel<BF16, D>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
 }
 
 template <bool BF16, int D>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, dim3 grid, int device, cudaStream_t st) {
-  if (ensure_prefill_smem<BF16, D>(device) != cudaSuccess) return PA_ERR_CUDA;
+                   const PrefillParams& p, dim3 grid, cudaStream_t st) {
+  if (ensure_prefill_smem<BF16, D>() != cudaSuccess) return PA_ERR_CUDA;
   paged_prefill_kernel<BF16, D><<<grid, kThreads, Cfg<D>::kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -733,16 +729,14 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   p.total_queries = total_queries;
   p.qscale = scale * kLog2e;
 
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
   const dim3 grid((max_query_len + kQTile - 1) / kQTile, num_heads, num_seqs);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch ((bf16 ? 1 : 0) | (head_dim == 64 ? 0 : head_dim == 128 ? 2 : 4)) {
-    case 0: return launch_prefill<false, 64>(tq, tk, tv, p, grid, device, st);
-    case 1: return launch_prefill<true, 64>(tq, tk, tv, p, grid, device, st);
-    case 2: return launch_prefill<false, 128>(tq, tk, tv, p, grid, device, st);
-    case 3: return launch_prefill<true, 128>(tq, tk, tv, p, grid, device, st);
-    case 4: return launch_prefill<false, 256>(tq, tk, tv, p, grid, device, st);
-    default: return launch_prefill<true, 256>(tq, tk, tv, p, grid, device, st);
+    case 0: return launch_prefill<false, 64>(tq, tk, tv, p, grid, st);
+    case 1: return launch_prefill<true, 64>(tq, tk, tv, p, grid, st);
+    case 2: return launch_prefill<false, 128>(tq, tk, tv, p, grid, st);
+    case 3: return launch_prefill<true, 128>(tq, tk, tv, p, grid, st);
+    case 4: return launch_prefill<false, 256>(tq, tk, tv, p, grid, st);
+    default: return launch_prefill<true, 256>(tq, tk, tv, p, grid, st);
   }
 }
