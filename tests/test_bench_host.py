@@ -114,3 +114,56 @@ def test_oracle_sample_follows_the_block_size():
         want = OA.paged_decode_attention(bits(b.q), kc, vc, b.block_tables, b.context_lens,
                                          b.scale, bs, "bf16")[seqs]
         assert np.array_equal(got, want)
+
+
+def test_nvml_reason_bits_by_name():
+    assert bench.reasons_from_mask(0) == []
+    assert bench.reasons_from_mask(0x4 | 0x40) == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.reasons_from_mask(0x1 | 0x8 | 0x20) == ["hw_slowdown", "sw_thermal_slowdown"]
+    c = bench.summarize_clocks([2070.0, 1990.0, 2070.0], [2070.0], {"sw_power_cap"}, "nvml")
+    assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 3, "source": "nvml"}
+    assert bench.clocks_rejected(dict(c, reasons=["hw_power_brake_slowdown"]))
+
+
+def test_balance_groups_cover_every_sequence_once():
+    import numpy as np
+    lens = np.random.default_rng(0).integers(1, 2000, size=97)
+    groups = bench.balance_groups(lens, 8)
+    flat = sorted(i for g in groups for i in g)
+    assert flat == list(range(97))
+    loads = [int(lens[g].sum()) for g in groups]
+    assert max(loads) - min(loads) <= int(lens.max())       # greedy longest-first bound
+    assert bench.balance_groups([5, 3], 8) == [[0], [1]]     # no empty groups
+
+
+def test_host_oracle_processes_match_the_oracle_in_one_process():
+    """The spawned-process runner gives exactly what the oracle gives in this
+    process, sequence for sequence, on every pass."""
+    import numpy as np
+    from workloads import random_decode_batch
+    b = random_decode_batch(41, [1, 17, 200, 513, 40, 90, 1000], 3, 64, 16, dtype="bf16",
+                            device="cpu", with_append=True, poison=False)
+    want = bench._oracle_step(bench._oracle_sample(b, list(range(b.num_seqs))), b.scale)
+    host = bench.HostOracle(b, 3)
+    try:
+        assert host.workers == 3
+        for _ in range(2):
+            got, dt = host.run()
+            assert np.array_equal(got, want) and dt > 0
+    finally:
+        host.close()
+
+
+def test_parity_report_flags_an_element_out_of_bound():
+    import numpy as np
+    rng = np.random.default_rng(1)
+    ref = rng.standard_normal((4, 2, 8))
+    out = torch.from_numpy(ref).to(torch.bfloat16)
+    r = bench.parity_report(out, ref, True)
+    assert r["ok"] and r["elements_out_of_bound"] == 0 and r["seqs_checked"] == 4
+    assert not bench.parity_report(out, ref, False)["ok"]      # append not bit-exact
+    bad = out.clone()
+    bad[2, 1, 3] += 0.05
+    r = bench.parity_report(bad, ref, True)
+    assert not r["ok"] and r["elements_out_of_bound"] == 1
