@@ -74,15 +74,14 @@ def test_bench_step_configuration(B):
     """The step bench.py times, on the batch it times: 13B-shaped lengths (seed 2),
     fused append, (sequence, partition) work items longest first, 512-token
     partitions, bf16 output, partition pass then merge pass with a preallocated
-    workspace.  Sampled rows against the oracle; appended rows bit for bit."""
+    workspace.  Every sequence against the oracle; appended rows bit for bit."""
     import numpy as np
     from paged_kv_cache_317_gb300.binding import partition_work_items
     b = decode_13b(seed=2, device="cuda", poison=False)
     N, H, D, bs, MB, pt = b.num_seqs, b.num_heads, b.head_dim, b.block_size, \
         b.max_blocks_per_seq, 512
     lens = b.context_lens
-    seqs = sorted(set(range(0, N, 13)) | {int(np.argmax(lens)), int(np.argmin(lens))})
-    ref = oracle_decode(b, seqs)
+    ref = oracle_decode(b)
     bt = torch.from_numpy(b.block_tables).cuda()
     sl = torch.from_numpy(lens).cuda()
     items = torch.from_numpy(partition_work_items(
@@ -101,4 +100,4 @@ def test_bench_step_configuration(B):
     blk, row = slots // bs, slots % bs
     assert torch.equal(b.k_cache[blk, :, row, :].view(torch.int16), b.new_k.view(torch.int16))
     assert torch.equal(b.v_cache[blk, :, row, :].view(torch.int16), b.new_v.view(torch.int16))
-    assert_matches_oracle(out[seqs], ref, "bench step")
+    assert_matches_oracle(out, ref, "bench step, all 256 sequences")

@@ -38,9 +38,7 @@ def _sample(n, k, seed, always=()):
 # --------------------------------------------------------------- 13B-shaped
 def test_13b_decode_with_append(B):
     b = decode_13b(device="cuda")
-    lens = b.context_lens
-    seqs = _sample(b.num_seqs, 24, 0, always=(int(np.argmax(lens)), int(np.argmin(lens))))
-    ref = oracle_decode(b, seqs)                      # reads the generator's pool before the append
+    ref = oracle_decode(b)                            # reads the generator's pool before the append
     k0, v0 = b.k_cache.clone(), b.v_cache.clone()
     bt, sl = device_tables(b)
     slots = torch.from_numpy(b.slot_mapping).cuda()
@@ -57,7 +55,7 @@ def test_13b_decode_with_append(B):
     v0[blk, :, row, :] = b.new_v
     assert torch.equal(k0.view(torch.int16), b.k_cache.view(torch.int16))
     assert torch.equal(v0.view(torch.int16), b.v_cache.view(torch.int16))
-    assert_matches_oracle(out[seqs], ref, "13B")
+    assert_matches_oracle(out, ref, "13B, all 256 sequences")
 
 
 def test_13b_single_pass_and_split_agree_with_oracle(B):
@@ -81,7 +79,11 @@ def test_long_context_split_k(B, bs):
                               error_record=rec)
     assert B.pa_error_read(rec) == [0, 0, 0, 0]
     assert torch.isfinite(out).all()
-    seqs = [0, 31]
+    # the first and last sequence (the first and last blocks of the launch) and
+    # six more drawn at random: 8 of 32
+    inner = np.random.default_rng(40 + bs).choice(np.arange(1, b.num_seqs - 1), 6, replace=False)
+    seqs = sorted({0, b.num_seqs - 1, *(int(i) for i in inner)})
+    assert len(seqs) == 8
     assert_matches_oracle(out[seqs], oracle_decode(b, seqs), f"long bs{bs}")
 
 
