@@ -75,6 +75,7 @@ struct DecodeParams {
   int stages;          // S
   int out_dtype;
   float qscale;        // scale * log2(e): scores come out in log2 units
+  int wait_first;      // this pass is the call's first kernel (no shared pass before it)
 };
 
 // Reduce each of N = TPR/2 partial dot products over the TPR lanes of a row
@@ -98,9 +99,10 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[TPR / 2], int c) {
   return v[0] + __shfl_xor_sync(kFullMask, v[0], 1);
 }
 
-// Waits for the grid this pass may depend on programmatically (the pass over
-// shared partitions) to complete, so that the merge after this pass also
-// follows that one.  A no-op without such a prerequisite.
+// Waits for the grid this pass depends on programmatically (the pass over
+// shared partitions, or the kernel before the call) to complete and its writes
+// to be visible.  A no-op without such a prerequisite, and when it has already
+// been waited for.
 __device__ __forceinline__ void wait_prerequisite() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -126,9 +128,18 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   static_assert(TPL * 2 == TPR, "lane split");
 
   extern __shared__ __align__(128) uint8_t smem[];
-  // A pass over shared partitions may follow as a programmatic dependent (it
-  // reads nothing this kernel writes): let it start once every block here has.
+  // The merge after this pass is a programmatic dependent that waits for this
+  // grid to complete before reading: let it be placed once every block here has
+  // started.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // As the call's first kernel this pass is itself launched as a programmatic
+  // dependent of whatever precedes it on the stream (the merge of the previous
+  // decode call, typically), so that its blocks are resident when that kernel
+  // ends.  Nothing in memory is touched before that kernel has completed and
+  // its writes are visible.  Behind the shared-partition pass the wait stays at
+  // the end instead (that pass waited for the predecessor before it let this
+  // one start).
+  if (p.wait_first) wait_prerequisite();
   const int G = p.heads_per_cta;
   const int S = p.stages;
   const int hg = blockIdx.x;

@@ -28,10 +28,15 @@ struct MergeParams {
 template <int D>
 __global__ void __launch_bounds__(256) paged_attn_merge_kernel(const MergeParams p) {
   constexpr int DPL = D / 32;  // dims per lane
-  // Launched as a programmatic dependent of the partition pass (or of the pass
-  // over shared partitions, which itself completes only after the partition
-  // pass): wait until that grid has completed and its writes are visible.
+  // Launched as a programmatic dependent of the partition pass (which completes
+  // only after the pass over shared partitions, if any): wait until that grid
+  // has completed and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next decode call's first kernel waits for this one to complete before
+  // it touches memory: let it be placed while this grid runs.  Not before the
+  // wait above: blocks of later calls placed that early would sit on SM slots
+  // the partition pass still needs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int gw = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= p.num_seqs * p.num_heads) return;
@@ -154,22 +159,23 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
     if (p.work_items != nullptr) grid = dim3(p.num_heads / p.heads_per_cta, p.num_work_items, 1);
     dim3 block((p.heads_per_cta + 1) * 32);
     if (grid.y > 0) {
-      if (shared != nullptr) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = grid;
-        cfg.blockDim = block;
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, paged_attn_partition_kernel<Tag, D>, p) != cudaSuccess)
-          return PA_ERR_CUDA;
-      } else {
-        paged_attn_partition_kernel<Tag, D><<<grid, block, smem, stream>>>(p);
-      }
+      // A programmatic dependent of the kernel before it: the shared-partition
+      // pass, or (as the call's first kernel, which then waits for it before
+      // touching memory) whatever precedes the call on the stream.
+      DecodeParams q = p;
+      q.wait_first = shared == nullptr ? 1 : 0;
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = grid;
+      cfg.blockDim = block;
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, paged_attn_partition_kernel<Tag, D>, q) != cudaSuccess)
+        return PA_ERR_CUDA;
       if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
   }

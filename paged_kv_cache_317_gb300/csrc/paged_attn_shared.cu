@@ -140,10 +140,15 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
                              const __grid_constant__ CUtensorMap tm_v, const SharedParams p) {
   using Gm = Geo<D>;
   constexpr int kRowBytes = D * 2;
+  // This pass is the call's first kernel, launched as a programmatic dependent
+  // of whatever precedes the call on the stream (the previous decode call's
+  // merge, typically): nothing in memory is touched before that kernel has
+  // completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // The per-sequence partition pass follows as a programmatic dependent (it
-  // reads nothing this pass writes): let it start once every block here has.
-  // Its blocks wait for this pass to complete before they exit, so the merge
-  // after it follows both.
+  // reads nothing this pass writes): let it start once every block here has
+  // (and so only after the wait above).  Its blocks wait for this pass to
+  // complete before they exit, so the merge after it follows both.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
@@ -438,9 +443,18 @@ int launch_t(const SharedParams& p, cudaStream_t stream) {
   if (!encode_tensor_map(&tk, bf16, p.k_cache, 2, dims, strides, box) ||
       !encode_tensor_map(&tv, bf16, p.v_cache, 2, dims, strides, box))
     return PA_ERR_CUDA;
-  const dim3 grid(p.num_heads / p.heads_per_cta, p.num_records);
-  const dim3 block((p.heads_per_cta + 1) * 32);
-  paged_attn_shared_kernel<Tag, D><<<grid, block, smem, stream>>>(tk, tv, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.num_heads / p.heads_per_cta, p.num_records);
+  cfg.blockDim = dim3((p.heads_per_cta + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_attn_shared_kernel<Tag, D>, tk, tv, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
