@@ -19,6 +19,9 @@ The line checks itself: after timing, the step's output is compared with the
 fp64 CPU oracle on every sequence of the batch (the oracle runs as one spawned
 host process per core) and the appended rows with the new K/V bit for bit; the
 result goes into "parity" and a failure ends the run with a non-zero status.
+After the headline (one GPU), every other seeded workload is timed as
+`--workload <name>` would time it and summarised under "workloads"
+(`--no-workloads` skips them).
 """
 
 from __future__ import annotations
@@ -523,6 +526,11 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_hbm_peak()
     achieved = nbytes["decode_partition"] / (part_ms * 1e-3) / 1e9
 
+    # the other seeded workloads (configs of the survey), timed after the headline
+    others = None
+    if rank == 0 and world == 1 and not args.no_workloads:
+        others = workload_summaries(args, rank, world, local_rank)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -558,6 +566,8 @@ def run_ours(args, rank, world, local_rank):
             "clocks": clk,
             "cpu_baseline": cpu,
         }
+        if others is not None:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
     if failed > 0:
         raise SystemExit("parity check of the timed step failed: " + json.dumps(parity))
@@ -666,11 +676,12 @@ class _Staging:
                 d[o["rc"]:o["rc"] + n_r * self.rw].view(n_r, self.rw) if n_r else None)
 
 
-def run_workload(args, rank, world, local_rank):
+def run_workload(args, rank, world, local_rank, emit=True):
     """Device time of one step of the other seeded workloads (decode attention,
-    plus the allocator, copies and appends where the workload has them)."""
+    plus the allocator, copies and appends where the workload has them).
+    Prints the line (emit) and returns it."""
     if rank != 0:
-        return
+        return None
     import numpy as np
     import torch
 
@@ -1158,7 +1169,35 @@ def run_workload(args, rank, world, local_rank):
                 pct_of_hbm_peak=round(100 * value / peak, 2),
                 peak=f"{peak} GB/s ({peak_kind} hbm_gbs)",
                 seq_tokens_per_s=round(tokens / (ms * 1e-3), 1))
-    print(json.dumps(line), flush=True)
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+SUMMARY_WORKLOADS = ("tiny", "small", "long16", "long32", "sampling", "mixed", "beam",
+                     "prefill", "append", "copy")
+
+
+def workload_summaries(args, rank, world, local_rank) -> dict:
+    """The other workloads, each timed as `--workload <name>` would time it (same
+    steps and warm-up), summarised for the headline line."""
+    import copy
+    keep = ("unique_kv_gbs", "unique_kv_frac_of_peak", "without_sharing_ms", "block_copy_ms",
+            "fixed_partition_512", "device_ms_per_step_split", "dtype")
+    out = {}
+    for w in SUMMARY_WORKLOADS:
+        a = copy.copy(args)
+        a.workload = w
+        line = run_workload(a, rank, world, local_rank, emit=False)
+        entry = {"workload": line["config"]["workload"], "ms_per_step": line["ms_per_step"],
+                 "value": line["value"], "unit": line["unit"],
+                 "pct_of_hbm_peak": line["pct_of_hbm_peak"]}
+        entry.update({k: line[k] for k in keep if k in line})
+        if "roofline" in line:
+            r = line["roofline"]
+            entry["roofline"] = {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+        out[w] = entry
+    return out
 
 
 # --------------------------------------------------------------- oracle arms
@@ -1386,6 +1425,8 @@ def main(argv=None):
     ap.add_argument("--block-size", type=int, default=16, help="13B-shaped batch: tokens per block")
     ap.add_argument("--partition", type=int, default=512,
                     help="13B-shaped batch: split-K partition length in tokens")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="13b: skip the summaries of the other workloads in the headline line")
     ap.add_argument("--no-share", action="store_true",
                     help="sampling/beam/mixed: read shared partitions once per sequence "
                          "instead of once per group")
