@@ -198,21 +198,31 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
     const int h0 = hg * G;
+    // A 16-token chunk lies in one block when the block size is a multiple of
+    // 16; with 8-token blocks it spans two (sub = 2), each copied on its own.
+    const int sub = p.block_size >= kChunk ? 1 : 2;
+    const int per_round = 32 / sub;  // chunks whose blocks one round of table reads covers
     bool stop = false;
-    for (int c0 = 0; c0 < nchunks && !stop; c0 += 32) {
-      // Lane j fetches the physical block of chunk c0 + j.
+    for (int c0 = 0; c0 < nchunks && !stop; c0 += per_round) {
+      // Lane l fetches the physical block of chunk c0 + l (sub = 1), or of
+      // half l % 2 of chunk c0 + l / 2 (sub = 2); entries past the sequence's
+      // last token are not read.
       int blk = 0;
-      if (c0 + lane < nchunks) {
-        const int tok = tok_begin + (c0 + lane) * kChunk;
-        blk = __ldg(table + tok / p.block_size);
-        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-          report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
-          blk = 0;
+      {
+        const int chunk = c0 + lane / sub;
+        const int tok = tok_begin + chunk * kChunk + (lane % sub) * (kChunk / sub);
+        if (chunk < nchunks && tok < tok_end) {
+          blk = __ldg(table + tok / p.block_size);
+          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+            report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
+            blk = 0;
+          }
         }
       }
-      const int n = min(32, nchunks - c0);
+      const int n = min(per_round, nchunks - c0);
       for (int j = 0; j < n; ++j) {
-        const int b = __shfl_sync(kFullMask, blk, j);
+        const int b = __shfl_sync(kFullMask, blk, j * sub);
+        const int b_hi = sub == 2 ? __shfl_sync(kFullMask, blk, j * sub + 1) : 0;
         if (lane == 0) {
           const int chunk = c0 + j;
           const int s = chunk % S;
@@ -232,14 +242,25 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
             const int row0 = tok % p.block_size;
             mbar_arrive_expect_tx(&full[s], 2u * G * static_cast<uint32_t>(rows) * ROW_BYTES);
             uint8_t* dst = stages + s * stage_bytes;
+            // with 8-token blocks: rows 0-7 of the chunk from block b, rows 8-15 from b_hi
+            const int rows_lo = sub == 2 ? min(cache_rows, kChunk / 2) : cache_rows;
+            const int rows_hi = cache_rows - rows_lo;
+            const uint32_t bytes_lo = static_cast<uint32_t>(rows_lo) * ROW_BYTES;
             for (int w = 0; w < G; ++w) {
               uint8_t* kd = dst + w * 2 * CHUNK_BYTES;
-              if (cache_rows > 0) {
+              if (rows_lo > 0) {
                 const size_t off =
                     ((static_cast<size_t>(b) * p.num_heads + h0 + w) * p.block_size + row0) *
                     ROW_BYTES;
-                bulk_g2s(kd, kbase + off, bytes, &full[s], policy);
-                bulk_g2s(kd + CHUNK_BYTES, vbase + off, bytes, &full[s], policy);
+                bulk_g2s(kd, kbase + off, bytes_lo, &full[s], policy);
+                bulk_g2s(kd + CHUNK_BYTES, vbase + off, bytes_lo, &full[s], policy);
+              }
+              if (rows_hi > 0) {
+                const size_t off =
+                    (static_cast<size_t>(b_hi) * p.num_heads + h0 + w) * p.block_size * ROW_BYTES;
+                const uint32_t bytes_hi = static_cast<uint32_t>(rows_hi) * ROW_BYTES;
+                bulk_g2s(kd + bytes_lo, kbase + off, bytes_hi, &full[s], policy);
+                bulk_g2s(kd + CHUNK_BYTES + bytes_lo, vbase + off, bytes_hi, &full[s], policy);
               }
               if (new_here) {
                 const size_t off = (static_cast<size_t>(seq) * p.num_heads + h0 + w) * ROW_BYTES;

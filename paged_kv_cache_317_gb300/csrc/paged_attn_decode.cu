@@ -233,7 +233,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PA_ERR_UNSUPPORTED;
-  if (block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (block_size % 16 != 0 && block_size != 8) return PA_ERR_UNSUPPORTED;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32)
     return PA_ERR_UNSUPPORTED;
@@ -305,6 +305,8 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   if (opts && opts->shared_records && opts->num_shared != 0) {
     if (opts->num_shared < 0 || opts->num_shared > 65535 || !p.work_items)
       return PA_ERR_INVALID_ARG;
+    // the shared pass moves 16-row boxes, each inside one block
+    if (block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
     sp.q = q;
     sp.k_cache = k_cache;
     sp.v_cache = v_cache;

@@ -43,7 +43,7 @@ def test_tiny_config_append_then_decode(B):
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("bs", [8, 16, 32])
 def test_decode_sweep_ragged_lengths(B, dtype, D, bs):
     lens = [1, 2, 15, 16, 17, 31, 33, 100, 255, 511, 512, 513, 700, 1025, 0, 3]
     b = random_decode_batch(1000 + D + bs, lens, 4, D, bs, dtype=dtype, device="cuda")
@@ -68,8 +68,9 @@ def test_launch_shapes_agree(B, G, S):
     assert_matches_oracle(run_decode(B, b, heads_per_cta=G, stages=S), ref, f"G{G} S{S}")
 
 
-def test_permuted_placement_is_bit_identical(B):
-    b = random_decode_batch(9, [3, 64, 129, 800], 8, 128, 16, dtype="f16", device="cuda",
+@pytest.mark.parametrize("bs", [8, 16])
+def test_permuted_placement_is_bit_identical(B, bs):
+    b = random_decode_batch(9, [3, 64, 129, 800], 8, 128, bs, dtype="f16", device="cuda",
                             pool_factor=2.0)
     base = run_decode(B, b)
     perm = torch.from_numpy(np.random.default_rng(3).permutation(b.num_blocks)).cuda()
@@ -300,3 +301,29 @@ def test_host_schedule_matches_oracle(B, lens):
     torch.cuda.synchronize()
     assert B.pa_error_read(rec) == [0, 0, 0, 0]
     assert_matches_oracle(out, oracle_decode(b), f"host schedule pt {pt}")
+
+
+def test_bad_block_entry_in_the_second_half_of_a_chunk(B):
+    """8-token blocks: a 16-token chunk reads two table entries; a bad second one is
+    recorded and clamped too, and the other sequence is unaffected."""
+    b = random_decode_batch(15, [40, 20], 4, 64, 8, dtype="f16", device="cuda", poison=False)
+    bt, sl = device_tables(b)
+    bt[1, 1] = b.num_blocks + 7           # tokens 8-15 of sequence 1
+    rec = B.new_error_record()
+    out = B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, error_record=rec)
+    r = B.pa_error_read(rec)
+    assert r[0] == 4 and r[1] >= 1 and r[2] == 1 and r[3] == b.num_blocks + 7
+    assert torch.isfinite(out).all()
+    assert_matches_oracle(out[:1], oracle_decode(b, [0]), "unaffected sequence")
+
+
+def test_shared_records_need_blocks_of_16(B):
+    b = random_decode_batch(16, [600, 600], 4, 128, 8, dtype="bf16", device="cuda")
+    bt, sl = device_tables(b)
+    recs = torch.tensor([[0, 2, 0, 1] + [-1] * 6], dtype=torch.int32, device="cuda")
+    items = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+    with pytest.raises(B.PagedKVError) as e:
+        B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, partition_tokens=512,
+                            work_items=items, shared_records=recs)
+    assert e.value.name == "PA_ERR_UNSUPPORTED"
+

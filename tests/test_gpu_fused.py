@@ -46,7 +46,7 @@ def test_fused_tiny_matches_oracle_and_unfused(B, pt):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("D,bs", [(64, 16), (128, 32), (256, 16)])
+@pytest.mark.parametrize("D,bs", [(64, 16), (128, 32), (256, 16), (128, 8), (64, 8)])
 def test_fused_ragged_lengths(B, dtype, D, bs):
     lens = [1, 2, 16, 17, 32, 33, 511, 512, 513, 1000]
     b = random_decode_batch(300 + D + bs, lens, 4, D, bs, dtype=dtype, device="cuda",

@@ -21,10 +21,22 @@ def B(lib):
 
 @pytest.mark.parametrize("seed", range(48))
 def test_decode_random_configuration(B, seed):
+    _random_decode_case(B, seed)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_decode_random_configuration_8_token_blocks(B, seed):
+    """8-token blocks: every 16-token chunk spans two blocks."""
+    _random_decode_case(B, 500 + seed, block_size=8)
+
+
+def _random_decode_case(B, seed, block_size=None):
     from paged_kv_cache_317_gb300.binding import partition_work_items
     rng = np.random.default_rng(1000 + seed)
     D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32, 48]))
+    if block_size is not None:
+        bs = block_size
     H = int(rng.choice([1, 2, 3, 4, 8, 12]))
     N = int(rng.integers(1, 12))
     dtype = str(rng.choice(["f16", "bf16"]))
