@@ -71,7 +71,8 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
                                      a["out"], a["odt"], a["pt"], a["ws"], a["wsb"], None, None)
 
     assert call(D=96) == UNS
-    assert call(bs=8) == UNS
+    assert call(bs=24) == UNS                                # neither 8 nor a multiple of 16
+    assert call(bs=4) == UNS
     assert call(dt=2) == UNS
     assert call(odt=7) == UNS
     assert call(q=None) == INV
