@@ -328,7 +328,8 @@ int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, i
  *   query_start   device int32 [num_seqs + 1], nondecreasing, query_start[num_seqs]
  *                 <= total_queries
  *   max_query_len host: >= every Q_i (sizes the grid)
- *   head_dim      64, 128 or 256;  block_size: a multiple of 16
+ *   head_dim      64, 128 or 256;  block_size: a multiple of 16, or 8 (each 16-key
+ *                 chunk is then loaded as two 8-row boxes)
  *   out           device [total_queries][num_heads][head_dim] in `out_dtype`
  * Rows of out outside every sequence's query range are not written.  A sequence
  * whose range is inconsistent (Q_i > L, range outside q, Q_i > max_query_len) is

@@ -304,11 +304,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
   // Started before the block-wide barrier so that their latency overlaps the
   // set-up: the Q tile load (its barrier initialised by the issuing thread)
   // and the producers' first block-table entries.
-  int blk_first = 0;  // producers: physical block of 16-key chunk `lane`
+  // With 8-token blocks a 16-key chunk spans two blocks: rows 0-7 come from the
+  // block of its first key, rows 8-15 from the next one (boxes of 8 rows).
+  const bool half_blocks = p.block_size < 16;
+  int blk_first = 0, blk_first_hi = 0;  // producers: physical block(s) of chunk `lane`
   if (warp == kWarpK || warp == kWarpV) {
     if (lane * 16 < keys)
       blk_first = __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks +
                         lane * 16 / p.block_size);
+    if (half_blocks && lane * 16 + 8 < keys)
+      blk_first_hi = __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks +
+                           (lane * 16 + 8) / p.block_size);
     if (warp == kWarpK && lane == 0) {
       mbar_init(&bars->q_full, 1);
       fence_mbar_init();
@@ -356,12 +362,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     const int stages = is_v ? kVStages : kKStages;
     const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-    int blk = 0;
+    int blk = 0, blk_hi = 0;
     for (int j = 0; j < T; ++j) {
       if ((j & 7) == 0) {
         // lane l looks up the physical block of 16-key chunk 4*j + l (8 tiles' worth)
+        // (and, with 8-token blocks, that of its second half)
         const int key0 = (j * 4 + lane) * 16;
         blk = 0;
+        blk_hi = 0;
         if (key0 < keys) {
           blk = j == 0 ? blk_first : __ldg(table + key0 / p.block_size);
           if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
@@ -369,16 +377,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
             blk = 0;
           }
         }
+        if (half_blocks && key0 + 8 < keys) {
+          blk_hi = j == 0 ? blk_first_hi : __ldg(table + (key0 + 8) / p.block_size);
+          if (static_cast<unsigned>(blk_hi) >= static_cast<unsigned>(p.num_blocks)) {
+            if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk_hi);
+            blk_hi = 0;
+          }
+        }
       }
       const int s = j % stages, use = j / stages;
-      const int n = min(4, (keys - j * kKTile + 15) / 16);  // chunks holding visible keys
+      // rows loaded: 16 per chunk holding visible keys; with 8-token blocks a
+      // chunk whose second half holds none loads 8
+      const int kt0 = j * kKTile;
+      int rows_loaded = 16 * min(4, (keys - kt0 + 15) / 16);
+      if (half_blocks && keys - kt0 < kKTile && (keys - kt0) % 16 != 0 && (keys - kt0) % 16 <= 8)
+        rows_loaded -= 8;
       uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
       uint64_t* empty = is_v ? &bars->v_empty[s] : &bars->k_empty[s];
       uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
       int ok = 1;
       if (lane == 0) {
         if (use > 0) ok = mbar_wait_bounded(empty, (use - 1) & 1);
-        if (ok) mbar_arrive_expect_tx(full, static_cast<uint32_t>(n) * C::kGroups * 2048);
+        if (ok)
+          mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows_loaded) * C::kGroups * 128);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
       if (!ok) {
@@ -388,14 +409,32 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
         }
         break;
       }
-      for (int c = 0; c < 4; ++c) {
-        const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
-        const int k0 = j * kKTile + c * 16;
-        if (lane == 0 && k0 < keys) {
-          const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
+      if (!half_blocks) {
+        for (int c = 0; c < 4; ++c) {
+          const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
+          const int k0 = j * kKTile + c * 16;
+          if (lane == 0 && k0 < keys) {
+            const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
 #pragma unroll
-          for (int g = 0; g < C::kGroups; ++g)
-            tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
+            for (int g = 0; g < C::kGroups; ++g)
+              tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
+          }
+        }
+      } else {
+        for (int c = 0; c < 4; ++c) {
+          const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
+          const int b_hi = __shfl_sync(kFullMask, blk_hi, (j & 7) * 4 + c);
+          const int k0 = j * kKTile + c * 16;
+          if (lane == 0 && k0 < keys) {
+            const int row = (b * p.num_heads + h) * p.block_size;
+            const int row_hi = (b_hi * p.num_heads + h) * p.block_size;
+#pragma unroll
+            for (int g = 0; g < C::kGroups; ++g) {
+              tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
+              if (k0 + 8 < keys)
+                tma_load_2d(dst + g * kHalfBytes + c * 2048 + 1024, map, 64 * g, row_hi, full);
+            }
+          }
         }
       }
       kv_issued = j + 1;
@@ -681,7 +720,8 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
       block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || total_queries == 0 || max_query_len == 0) return PA_OK;
-  if ((head_dim != 64 && head_dim != 128 && head_dim != 256) || block_size % 16 != 0)
+  if ((head_dim != 64 && head_dim != 128 && head_dim != 256) ||
+      (block_size % 16 != 0 && block_size != 8))
     return PA_ERR_UNSUPPORTED;
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
   if (out_dtype != PA_F16 && out_dtype != PA_BF16 && out_dtype != PA_F32)
@@ -708,7 +748,8 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   const cuuint32_t qbox[3] = {64, 1, kQTile};
   const cuuint64_t cdims[2] = {static_cast<cuuint64_t>(head_dim), cache_rows};
   const cuuint64_t cstr[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  const cuuint32_t cbox[2] = {64, 16};
+  // a box is one 16-key chunk, or half of one with 8-token blocks
+  const cuuint32_t cbox[2] = {64, block_size >= 16 ? 16u : 8u};
   if (!encode_tensor_map(&tq, bf16, q, 3, qdims, qstr, qbox) ||
       !encode_tensor_map(&tk, bf16, k_cache, 2, cdims, cstr, cbox) ||
       !encode_tensor_map(&tv, bf16, v_cache, 2, cdims, cstr, cbox))

@@ -83,9 +83,21 @@ def _random_decode_case(B, seed, block_size=None):
 
 @pytest.mark.parametrize("seed", range(32))
 def test_prefill_random_configuration(B, seed):
+    _random_prefill_case(B, seed)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefill_random_configuration_8_token_blocks(B, seed):
+    """8-token blocks: every 16-key chunk is loaded as two 8-row boxes."""
+    _random_prefill_case(B, 500 + seed, block_size=8)
+
+
+def _random_prefill_case(B, seed, block_size=None):
     rng = np.random.default_rng(3000 + seed)
     D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32]))
+    if block_size is not None:
+        bs = block_size
     H = int(rng.integers(1, 5))
     N = int(rng.integers(1, 5))
     dtype = str(rng.choice(["f16", "bf16"]))

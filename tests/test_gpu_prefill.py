@@ -42,7 +42,7 @@ def _oracle(b, q, starts, seqs=None):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("bs", [8, 16, 32])
 def test_prefill_small_cases(B, dtype, bs):
     lens = [5, 300, 1000, 17, 129, 64]
     nq = [5, 64, 200, 1, 129, 3]            # whole-sequence prefill, chunks, one query
