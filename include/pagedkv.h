@@ -184,8 +184,7 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  (the pairs not covered by a record; when there are none, any
  *                  non-NULL pointer with num_work_items = 0); every pair that
  *                  holds tokens must appear exactly once across both.  At most
- *                  65535 records.  Needs a block_size that is a multiple of 16
- *                  (PA_ERR_UNSUPPORTED otherwise).
+ *                  65535 records.
  *                  pa_decode_share_plan builds both lists.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
@@ -299,9 +298,6 @@ int pa_decode_work_items(const int32_t* seq_lens, int num_seqs, int partition_to
  *   work_items     host int32 [items_capacity]; records: host int32
  *                  [records_capacity][PA_SHARE_RECORD_WORDS]; both NULL to count
  *   num_items, num_records  out: the counts
- * With a block_size that is not a multiple of 16 nothing is shared (the shared
- * pass reads 16-row boxes inside one block): *num_records = 0 and the work list
- * is that of pa_decode_work_items.
  * Returns PA_OK or PA_ERR_INVALID_ARG (as for pa_decode_work_items, or a
  * capacity below a count: the counts are still written, the arrays untouched).
  * Host work: per partition, a sort of the sequences that hold it by its first

@@ -153,14 +153,11 @@ extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* 
   std::vector<long long> first_part(static_cast<size_t>(num_seqs) + 1, 0);
   std::vector<int> shareable(static_cast<size_t>(num_seqs), 0);
   int most = 0;
-  // The shared pass reads 16-row boxes that must lie inside one block: with
-  // smaller blocks (8 tokens) nothing is shared and the plan is the work list.
-  const bool can_share = block_size % 16 == 0;
   for (int i = 0; i < num_seqs; ++i) {
     const int L = seq_lens[i];
     if (L < 0 || L > cap) return PA_ERR_INVALID_ARG;
     first_part[i + 1] = first_part[i] + std::max(1, (L + pt - 1) / pt);
-    shareable[i] = can_share ? std::max(0, (L - (fused_append ? 1 : 0)) / pt) : 0;
+    shareable[i] = std::max(0, (L - (fused_append ? 1 : 0)) / pt);
     most = std::max(most, shareable[i]);
   }
   const long long total = first_part[num_seqs];

@@ -305,8 +305,6 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   if (opts && opts->shared_records && opts->num_shared != 0) {
     if (opts->num_shared < 0 || opts->num_shared > 65535 || !p.work_items)
       return PA_ERR_INVALID_ARG;
-    // the shared pass moves 16-row boxes, each inside one block
-    if (block_size % 16 != 0) return PA_ERR_UNSUPPORTED;
     sp.q = q;
     sp.k_cache = k_cache;
     sp.v_cache = v_cache;

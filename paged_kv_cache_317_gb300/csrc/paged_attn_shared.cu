@@ -213,50 +213,106 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
     const int32_t* table = p.block_tables + static_cast<size_t>(first) * p.max_blocks;
     const int h0 = hg * G;
     bool stop = false;
-    for (int c0 = 0; c0 < nchunks && !stop; c0 += 32) {
-      int blk = 0;
-      if (c0 + lane < nchunks) {
-        const int tok = tok_begin + (c0 + lane) * kChunk;
-        blk = __ldg(table + tok / p.block_size);
-        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-          report_error(p.err, PA_ERR_BAD_BLOCK, first, blk);
-          blk = 0;
-        }
-      }
-      const int n = min(32, nchunks - c0);
-      for (int j = 0; j < n; ++j) {
-        const int b = __shfl_sync(kFullMask, blk, j);
-        const int chunk = c0 + j;
-        const int s = chunk % S;
-        if (lane == 0) {
-          bool ok = true;
-          if (chunk >= S) ok = mbar_wait_bounded(&empty[s], ((chunk / S) - 1) & 1);
-          if (!ok) {
-            *abort_flag = 1;
-            report_error(p.err, PA_ERR_TIMEOUT, first, chunk);
-          } else {
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
-            // the chunk's rows of (block b, head h) are rows y .. y + 15 of the
-            // cache viewed as [num_blocks * H * bs][D]
-            const int row0 = (tok_begin + chunk * kChunk) % p.block_size;
-            uint8_t* dst = ring + s * stage_bytes;
-            for (int w = 0; w < G; ++w) {
-              const int y = (b * p.num_heads + h0 + w) * p.block_size + row0;
-#pragma unroll
-              for (int cg = 0; cg < Gm::kGroups; ++cg) {
-                tma_load_2d(dst + (w * 2) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_k, cg * 64,
-                            y, &full[s]);
-                tma_load_2d(dst + (w * 2 + 1) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_v,
-                            cg * 64, y, &full[s]);
-              }
-            }
-            ++issued;
+    if (p.block_size >= kChunk) {
+      for (int c0 = 0; c0 < nchunks && !stop; c0 += 32) {
+        int blk = 0;
+        if (c0 + lane < nchunks) {
+          const int tok = tok_begin + (c0 + lane) * kChunk;
+          blk = __ldg(table + tok / p.block_size);
+          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+            report_error(p.err, PA_ERR_BAD_BLOCK, first, blk);
+            blk = 0;
           }
         }
-        __syncwarp();
-        if (__shfl_sync(kFullMask, *abort_flag, 0)) {
-          stop = true;
-          break;
+        const int n = min(32, nchunks - c0);
+        for (int j = 0; j < n; ++j) {
+          const int b = __shfl_sync(kFullMask, blk, j);
+          const int chunk = c0 + j;
+          const int s = chunk % S;
+          if (lane == 0) {
+            bool ok = true;
+            if (chunk >= S) ok = mbar_wait_bounded(&empty[s], ((chunk / S) - 1) & 1);
+            if (!ok) {
+              *abort_flag = 1;
+              report_error(p.err, PA_ERR_TIMEOUT, first, chunk);
+            } else {
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
+              // the chunk's rows of (block b, head h) are rows y .. y + 15 of the
+              // cache viewed as [num_blocks * H * bs][D]
+              const int row0 = (tok_begin + chunk * kChunk) % p.block_size;
+              uint8_t* dst = ring + s * stage_bytes;
+              for (int w = 0; w < G; ++w) {
+                const int y = (b * p.num_heads + h0 + w) * p.block_size + row0;
+  #pragma unroll
+                for (int cg = 0; cg < Gm::kGroups; ++cg) {
+                  tma_load_2d(dst + (w * 2) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_k, cg * 64,
+                              y, &full[s]);
+                  tma_load_2d(dst + (w * 2 + 1) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_v,
+                              cg * 64, y, &full[s]);
+                }
+              }
+              ++issued;
+            }
+          }
+          __syncwarp();
+          if (__shfl_sync(kFullMask, *abort_flag, 0)) {
+            stop = true;
+            break;
+          }
+        }
+      }
+    } else {
+      // 8-token blocks: rows 0-7 of a chunk come from the block of its first
+      // token, rows 8-15 from the next one (8-row boxes into the same tile);
+      // lane l looks up half l % 2 of chunk c0 + l / 2.  Records cover whole
+      // partitions, so both halves always hold tokens.
+      for (int c0 = 0; c0 < nchunks && !stop; c0 += 16) {
+        int blk = 0;
+        const int chunk_l = c0 + (lane >> 1);
+        if (chunk_l < nchunks) {
+          const int tok = tok_begin + chunk_l * kChunk + (lane & 1) * (kChunk / 2);
+          blk = __ldg(table + tok / p.block_size);
+          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+            report_error(p.err, PA_ERR_BAD_BLOCK, first, blk);
+            blk = 0;
+          }
+        }
+        const int n = min(16, nchunks - c0);
+        for (int j = 0; j < n; ++j) {
+          const int b = __shfl_sync(kFullMask, blk, 2 * j);
+          const int b_hi = __shfl_sync(kFullMask, blk, 2 * j + 1);
+          const int chunk = c0 + j;
+          const int s = chunk % S;
+          if (lane == 0) {
+            bool ok = true;
+            if (chunk >= S) ok = mbar_wait_bounded(&empty[s], ((chunk / S) - 1) & 1);
+            if (!ok) {
+              *abort_flag = 1;
+              report_error(p.err, PA_ERR_TIMEOUT, first, chunk);
+            } else {
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
+              uint8_t* dst = ring + s * stage_bytes;
+              for (int w = 0; w < G; ++w) {
+                const int y = (b * p.num_heads + h0 + w) * p.block_size;
+                const int y_hi = (b_hi * p.num_heads + h0 + w) * p.block_size;
+#pragma unroll
+                for (int cg = 0; cg < Gm::kGroups; ++cg) {
+                  uint8_t* kd = dst + (w * 2) * Gm::kTileBytes + cg * Gm::kGroupBytes;
+                  uint8_t* vd = dst + (w * 2 + 1) * Gm::kTileBytes + cg * Gm::kGroupBytes;
+                  tma_load_2d(kd, &tm_k, cg * 64, y, &full[s]);
+                  tma_load_2d(kd + Gm::kGroupBytes / 2, &tm_k, cg * 64, y_hi, &full[s]);
+                  tma_load_2d(vd, &tm_v, cg * 64, y, &full[s]);
+                  tma_load_2d(vd + Gm::kGroupBytes / 2, &tm_v, cg * 64, y_hi, &full[s]);
+                }
+              }
+              ++issued;
+            }
+          }
+          __syncwarp();
+          if (__shfl_sync(kFullMask, *abort_flag, 0)) {
+            stop = true;
+            break;
+          }
         }
       }
     }
@@ -437,7 +493,8 @@ int launch_t(const SharedParams& p, cudaStream_t stream) {
   if (rows >= (1ull << 31)) return PA_ERR_UNSUPPORTED;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, kChunk};
+  // a box is one 16-token chunk, or half of one with 8-token blocks
+  const cuuint32_t box[2] = {64, p.block_size >= kChunk ? 16u : 8u};
   CUtensorMap tk, tv;
   const bool bf16 = std::is_same<Tag, BF16>::value;
   if (!encode_tensor_map(&tk, bf16, p.k_cache, 2, dims, strides, box) ||
@@ -468,7 +525,8 @@ int launch_shared_partitions(const SharedParams& p, int dtype, int head_dim, cud
   if (p.num_records == 0) return PA_OK;
   if (p.num_records < 0 || p.num_records > 65535 || p.heads_per_cta < 1 ||
       p.heads_per_cta > kMaxG || p.num_heads % p.heads_per_cta != 0 || p.stages < 2 ||
-      p.stages > kMaxRing || p.partition_tokens % kChunk != 0 || p.block_size % kChunk != 0)
+      p.stages > kMaxRing || p.partition_tokens % kChunk != 0 ||
+      (p.block_size % kChunk != 0 && p.block_size != 8))
     return PA_ERR_INVALID_ARG;
   if (shared_kernel_smem_bytes(head_dim, p.heads_per_cta, p.stages) > 227 * 1024)
     return PA_ERR_INVALID_ARG;

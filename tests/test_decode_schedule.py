@@ -219,30 +219,24 @@ def test_share_plan_rejects_bad_arguments():
     assert list(items) == [0, 4] and recs.shape == (0, B.PA_SHARE_RECORD_WORDS)
 
 
-def test_share_plan_with_8_token_blocks_is_the_work_list():
-    """The shared pass reads 16-row boxes inside one block, so with 8-token blocks
-    the plan shares nothing: no records, and the work list of pa_decode_work_items."""
-    bs, pt = 8, 64
-    alloc = B.BlockAllocator(2000, bs)
-    ids = []
-    for k, prompt in enumerate((300, 700)):
-        alloc.add(100 * k, prompt)
-        for s in range(1, 4):
-            alloc.fork(100 * k, 100 * k + s)
-            ids.append(100 * k + s)
-        ids.append(100 * k)
-    alloc.batch_append(ids)
-    MB = 100
-    tables, lens = alloc.batch_block_tables(ids, MB)
-    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
-    assert recs.shape == (0, B.PA_SHARE_RECORD_WORDS)
-    assert list(items) == list(B.partition_work_items(lens, pt, MB, bs))
-    # the same tables at 16-token blocks do share (the rule is the block size)
-    alloc16 = B.BlockAllocator(2000, 16)
-    for k, prompt in enumerate((300, 700)):
-        alloc16.add(100 * k, prompt)
-        for s in range(1, 4):
-            alloc16.fork(100 * k, 100 * k + s)
-    alloc16.batch_append(ids)
-    t16, l16 = alloc16.batch_block_tables(ids, 50)
-    assert len(B.share_plan(t16, l16, pt, 16, fused_append=True)[1]) > 0
+def test_share_plan_with_8_token_blocks_matches_its_definition():
+    """8-token blocks: a 64-token partition spans 8 table entries; the plan still
+    groups exactly the sequences whose slices are identical."""
+    rng = np.random.default_rng(9)
+    for trial in range(60):
+        bs, pt = 8, int(rng.choice([16, 32, 64, 128]))
+        N, MB = int(rng.integers(1, 40)), int(rng.integers(1, 48))
+        prompts = rng.integers(0, 500, size=(4, MB)).astype(np.int32)
+        tables = rng.integers(0, 500, size=(N, MB)).astype(np.int32)
+        lens = rng.integers(0, MB * bs + 1, size=N)
+        for i in range(N):
+            if rng.random() < 0.7:
+                k = int(rng.integers(0, MB + 1))
+                tables[i, :k] = prompts[int(rng.integers(0, 4)), :k]
+        fused = bool(rng.integers(0, 2))
+        if fused:
+            lens = np.maximum(lens, 1)
+        items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused)
+        want_recs, want_items = _plan_by_definition(tables, lens, pt, bs, fused)
+        assert _records_as_set(recs) == want_recs, trial
+        assert np.array_equal(items, want_items), trial

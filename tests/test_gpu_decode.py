@@ -315,15 +315,3 @@ def test_bad_block_entry_in_the_second_half_of_a_chunk(B):
     assert r[0] == 4 and r[1] >= 1 and r[2] == 1 and r[3] == b.num_blocks + 7
     assert torch.isfinite(out).all()
     assert_matches_oracle(out[:1], oracle_decode(b, [0]), "unaffected sequence")
-
-
-def test_shared_records_need_blocks_of_16(B):
-    b = random_decode_batch(16, [600, 600], 4, 128, 8, dtype="bf16", device="cuda")
-    bt, sl = device_tables(b)
-    recs = torch.tensor([[0, 2, 0, 1] + [-1] * 6], dtype=torch.int32, device="cuda")
-    items = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
-    with pytest.raises(B.PagedKVError) as e:
-        B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, partition_tokens=512,
-                            work_items=items, shared_records=recs)
-    assert e.value.name == "PA_ERR_UNSUPPORTED"
-

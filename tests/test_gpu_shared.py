@@ -116,7 +116,7 @@ class Families:
 
 @pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("dtype,D,bs", [("bf16", 128, 16), ("f16", 128, 32), ("bf16", 64, 16),
-                                        ("f16", 256, 16)])
+                                        ("f16", 256, 16), ("bf16", 128, 8), ("f16", 64, 8)])
 def test_shared_partitions_match_oracle(B, fused, dtype, D, bs):
     fam = Families(B, 7 + D + bs, prompts=[700, 300, 1300], members=6, tail_max=150, H=4, D=D,
                    bs=bs, dtype=dtype, fused=fused)
@@ -231,9 +231,21 @@ def test_long_shared_pass_eager_and_in_a_cuda_graph(B):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_shared_random_configuration(B, seed):
+    _random_shared_case(B, seed)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_shared_random_configuration_8_token_blocks(B, seed):
+    """8-token blocks: each shared chunk is loaded as two 8-row boxes."""
+    _random_shared_case(B, 500 + seed, block_size=8)
+
+
+def _random_shared_case(B, seed, block_size=None):
     rng = np.random.default_rng(7000 + seed)
     D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32]))
+    if block_size is not None:
+        bs = block_size
     H = int(rng.choice([1, 2, 3, 4, 8]))
     dtype = str(rng.choice(["f16", "bf16"]))
     fused = bool(rng.integers(0, 2))
