@@ -243,7 +243,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
               uint8_t* dst = ring + s * stage_bytes;
               for (int w = 0; w < G; ++w) {
                 const int y = (b * p.num_heads + h0 + w) * p.block_size + row0;
-  #pragma unroll
+#pragma unroll
                 for (int cg = 0; cg < Gm::kGroups; ++cg) {
                   tma_load_2d(dst + (w * 2) * Gm::kTileBytes + cg * Gm::kGroupBytes, &tm_k, cg * 64,
                               y, &full[s]);

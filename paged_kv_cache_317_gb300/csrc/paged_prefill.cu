@@ -409,31 +409,25 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
         }
         break;
       }
-      if (!half_blocks) {
-        for (int c = 0; c < 4; ++c) {
-          const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
-          const int k0 = j * kKTile + c * 16;
-          if (lane == 0 && k0 < keys) {
-            const int row = (b * p.num_heads + h) * p.block_size + k0 % p.block_size;
+      // Lanes 4 (j % 8) .. 4 (j % 8) + 3 hold the blocks of this tile's four
+      // chunks (and, with 8-token blocks, of their second halves): each issues
+      // its own chunk's boxes, so a tile's loads go out in one warp instruction
+      // per column group rather than one thread's sequence of them (the
+      // producers sit on the critical path: 267 -> 235 us on the chunked-prefill
+      // batch).
+      {
+        const int c = lane - (j & 7) * 4;
+        const int k0 = j * kKTile + c * 16;
+        if (c >= 0 && c < 4 && k0 < keys) {
+          const int row = (blk * p.num_heads + h) * p.block_size + k0 % p.block_size;
+#pragma unroll
+          for (int g = 0; g < C::kGroups; ++g)
+            tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
+          if (half_blocks && k0 + 8 < keys) {
+            const int row_hi = (blk_hi * p.num_heads + h) * p.block_size;
 #pragma unroll
             for (int g = 0; g < C::kGroups; ++g)
-              tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
-          }
-        }
-      } else {
-        for (int c = 0; c < 4; ++c) {
-          const int b = __shfl_sync(kFullMask, blk, (j & 7) * 4 + c);
-          const int b_hi = __shfl_sync(kFullMask, blk_hi, (j & 7) * 4 + c);
-          const int k0 = j * kKTile + c * 16;
-          if (lane == 0 && k0 < keys) {
-            const int row = (b * p.num_heads + h) * p.block_size;
-            const int row_hi = (b_hi * p.num_heads + h) * p.block_size;
-#pragma unroll
-            for (int g = 0; g < C::kGroups; ++g) {
-              tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
-              if (k0 + 8 < keys)
-                tma_load_2d(dst + g * kHalfBytes + c * 2048 + 1024, map, 64 * g, row_hi, full);
-            }
+              tma_load_2d(dst + g * kHalfBytes + c * 2048 + 1024, map, 64 * g, row_hi, full);
           }
         }
       }
