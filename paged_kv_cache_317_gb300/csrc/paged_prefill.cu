@@ -51,7 +51,8 @@ constexpr int kQTile = 128;                       // query rows per block (MMA M
 constexpr int kKTile = 64;                        // keys per tile
 constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
 constexpr int kWarpK = 4, kWarpMma = 5, kWarpV = 6;
-constexpr int kKStages = 2;                       // K ring depth
+constexpr int kKStages = 2;                       // K ring depth (= the S buffers: a stage is freed by its S)
+static_assert(kKStages == 2, "K stage s is released through S buffer s's completion barrier");
 constexpr int kVStages = 3;                       // V ring depth: V(j+3) loads while P.V(j+1..j+2) run
 constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B: one 64-wide column group of a K/V tile
 constexpr int kQHalfBytes = kQTile * 128;         // 128 rows x 128 B: one 64-wide column group of Q
@@ -93,7 +94,7 @@ constexpr float kRescaleThreshold = 8.0f;
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t k_full[kKStages], v_full[kVStages], v_empty[kVStages];
   // s_free[b] completes when the P.V of buffer b's tile finishes (one phase
   // per two tiles), so it doubles as that P.V's completion signal.
   uint64_t s_full[2], s_free[2], p_full[2], drain;
@@ -325,10 +326,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     }
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
+    for (int s = 0; s < kKStages; ++s) mbar_init(&bars->k_full[s], 1);
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
@@ -393,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       if (half_blocks && keys - kt0 < kKTile && (keys - kt0) % 16 != 0 && (keys - kt0) % 16 <= 8)
         rows_loaded -= 8;
       uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
-      uint64_t* empty = is_v ? &bars->v_empty[s] : &bars->k_empty[s];
+      // a K stage is free once the S that read it has completed: with two K
+      // stages and two S buffers that is s_full[s] (S(j - 2) ends before S(j),
+      // which needs this load, can)
+      uint64_t* empty = is_v ? &bars->v_empty[s] : &bars->s_full[s];
       uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
       int ok = 1;
       if (lane == 0) {
@@ -456,8 +457,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
           const uint64_t bd = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
           mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
         }
-        mma_commit(&bars->s_full[b]);
-        mma_commit(&bars->k_empty[s]);
+        mma_commit(&bars->s_full[b]);  // also frees K stage s (= b: two stages)
         mma_started = 1;
         return true;
       };
