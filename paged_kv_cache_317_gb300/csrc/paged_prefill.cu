@@ -10,15 +10,16 @@
 //  * block = (128-query tile, head, sequence); 7 warps: one softmax warpgroup
 //    (one query row per thread = one TMEM lane), a K producer, an MMA issuer
 //    and a V producer.  head_dim 64, 128 or 256: tiles are stored as head_dim /
-//    64 column groups of 64 elements.  At 64 and 128, <= 113 KB of shared memory
+//    64 column groups of 64 elements.  At 64 and 128, <= 97 KB of shared memory
 //    and 256 TMEM columns, so two blocks share an SM and cover each other's
-//    start-up and tail; at 256, ~225 KB and 512 columns, one block per SM.
+//    start-up and tail; at 256, ~193 KB and 512 columns, one block per SM.
 //  * Q tile: two 3-D TMA loads (one per 64-wide half of head_dim, 128B
 //    swizzle), issued before the block-wide set-up barrier.  K/V: per 16-key
 //    chunk the producers follow the block table (32 entries at a time) and
-//    issue 2-D TMA loads of the rows (128B swizzle) into a 2-stage K ring and a
-//    3-stage V ring of 64-key tiles; a K tile is released when its S MMA
-//    completes, a V tile when its P.V completes.
+//    issue 2-D TMA loads of the rows (128B swizzle) into 2-stage K and V rings
+//    of 64-key tiles, each chunk's boxes by the lane holding its table entry; a
+//    K tile is released when its S MMA completes, a V tile when its P.V
+//    completes (the completion barriers of S/P buffer j & 1 serve for both).
 //  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16, fp32 accumulate) into one of
 //    two 64-column TMEM buffers.  Buffer j & 1 is reused for S(j+2) only after
 //    P.V(j), which reads the P stored there, has completed.
@@ -52,8 +53,9 @@ constexpr int kKTile = 64;                        // keys per tile
 constexpr int kThreads = 224;                     // 4 softmax, K producer, MMA, V producer
 constexpr int kWarpK = 4, kWarpMma = 5, kWarpV = 6;
 constexpr int kKStages = 2;                       // K ring depth (= the S buffers: a stage is freed by its S)
-static_assert(kKStages == 2, "K stage s is released through S buffer s's completion barrier");
-constexpr int kVStages = 3;                       // V ring depth: V(j+3) loads while P.V(j+1..j+2) run
+constexpr int kVStages = 2;                       // V ring depth (= the S/P buffers: a stage is freed by its P.V)
+static_assert(kKStages == 2 && kVStages == 2,
+              "K and V stage s are released through S/P buffer s's completion barriers");
 constexpr int kHalfBytes = kKTile * 128;          // 64 rows x 128 B: one 64-wide column group of a K/V tile
 constexpr int kQHalfBytes = kQTile * 128;         // 128 rows x 128 B: one 64-wide column group of Q
 // TMEM: two S/P buffers of 64 columns (S in fp32; after the softmax, P hi in the
@@ -71,15 +73,15 @@ struct Cfg {
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-  // At D = 128 two blocks must fit an SM (228 KB, less 1 KB reserved per block):
-  // 768 bytes are left for aligning the dynamic shared-memory base to 1 KB; the
-  // kernel checks it.  Otherwise a full 1 KB is left.
-  static constexpr int kAlignSlack = D == 128 ? 768 : 1024;
+  // 1 KB is left for aligning the dynamic shared-memory base to 1 KB (the
+  // kernel checks it); at D <= 128 two blocks still fit an SM (228 KB, less 1 KB
+  // reserved per block).
+  static constexpr int kAlignSlack = 1024;
   static constexpr int kSmemUsed = kOffBar + 256 + kAlignSlack;
   // Requested per block: at least 80 KB, so that no more than two blocks (two
   // 256-column TMEM allocations) ever share an SM, whatever the register count.
   static constexpr int kSmemBytes = kSmemUsed > 80 * 1024 ? kSmemUsed : 80 * 1024;
-  // D = 256 needs 384 TMEM columns (allocated as 512) and ~225 KB: one block per SM.
+  // D = 256 needs 384 TMEM columns (allocated as 512) and ~193 KB: one block per SM.
   static constexpr int kMinBlocks = D <= 128 ? 2 : 1;
   static constexpr uint32_t kTmemCols = kTmemO + D <= 256 ? 256 : 512;
   static_assert(D == 64 || D == 128 || D == 256, "head_dim");
@@ -94,7 +96,7 @@ constexpr float kRescaleThreshold = 8.0f;
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t k_full[kKStages], v_full[kVStages];
   // s_free[b] completes when the P.V of buffer b's tile finishes (one phase
   // per two tiles), so it doubles as that P.V's completion signal.
   uint64_t s_full[2], s_free[2], p_full[2], drain;
@@ -327,10 +329,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) mbar_init(&bars->k_full[s], 1);
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-    }
+    for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_full[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], 1);
@@ -391,10 +390,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       if (half_blocks && keys - kt0 < kKTile && (keys - kt0) % 16 != 0 && (keys - kt0) % 16 <= 8)
         rows_loaded -= 8;
       uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
-      // a K stage is free once the S that read it has completed: with two K
-      // stages and two S buffers that is s_full[s] (S(j - 2) ends before S(j),
-      // which needs this load, can)
-      uint64_t* empty = is_v ? &bars->v_empty[s] : &bars->s_full[s];
+      // A K stage is free once the S that read it has completed, a V stage once
+      // the P.V that read it has: with two stages of each and two S/P buffers,
+      // those are s_full[s] and s_free[s].  (The next completion on either
+      // barrier needs the load being waited for, so no phase can be skipped.)
+      uint64_t* empty = is_v ? &bars->s_free[s] : &bars->s_full[s];
       uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
       int ok = 1;
       if (lane == 0) {
@@ -482,8 +482,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
           mma_f16_ts(tmem + kTmemO, ph + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           mma_f16_ts(tmem + kTmemO, pl + kk * 8, bd, idesc_o, 1u);
         }
-        mma_commit(&bars->s_free[b]);
-        mma_commit(&bars->v_empty[s]);
+        mma_commit(&bars->s_free[b]);  // also frees V stage s (= b: two stages)
       }
       if (!ok) {
         *abort_flag = 1;
