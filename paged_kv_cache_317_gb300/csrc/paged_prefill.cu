@@ -444,17 +444,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       bool ok = mbar_wait_bounded(&bars->q_full, 0);
       // S_j goes to TMEM buffer j & 1, whose previous contents (P of tile j-2)
       // must have been consumed by P.V(j-2).
+      // descriptors of the tile bases; an offset within a tile is added to the
+      // start-address field (16-byte units, no carry: shared memory < 256 KB)
+      const uint64_t q_desc = smem_desc_sw128(Qs, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(k_tile(0), 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(v_tile(0), kHalfBytes, 1024);
       auto issue_s = [&](int j) -> bool {
         const int s = j % kKStages, b = j & 1;
         if (!mbar_wait_bounded(&bars->k_full[s], (j / kKStages) & 1)) return false;
         if (j >= 2 && !mbar_wait_bounded(&bars->s_free[b], ((j >> 1) - 1) & 1)) return false;
         tc_fence_after();
-        const uint8_t* ks = k_tile(s);
+        const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int half = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(Qs + half * kQHalfBytes + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(ks + half * kHalfBytes + off, 16, 1024);
+          const uint64_t a = q_desc + static_cast<uint64_t>((half * kQHalfBytes + off) >> 4);
+          const uint64_t bd = k_desc + static_cast<uint64_t>((half * kHalfBytes + off) >> 4);
           mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
         }
         mma_commit(&bars->s_full[b]);  // also frees K stage s (= b: two stages)
@@ -474,11 +479,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
           break;
         }
         tc_fence_after();
-        const uint8_t* vs = v_tile(s);
+        const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
         const uint32_t ph = tmem + b * kKTile, pl = ph + kKTile / 2;
 #pragma unroll
         for (int kk = 0; kk < kKTile / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(vs + kk * 2048, kHalfBytes, 1024);
+          const uint64_t bd = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
           mma_f16_ts(tmem + kTmemO, ph + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           mma_f16_ts(tmem + kTmemO, pl + kk * 8, bd, idesc_o, 1u);
         }
