@@ -7,19 +7,26 @@
 // physical scatter").  With >1 query per head the work is a dense contraction,
 // so it runs on tensor cores:
 //
-//  * block = (128-query tile, head, sequence); 7 warps: one softmax warpgroup
-//    (one query row per thread = one TMEM lane), a K producer, an MMA issuer
-//    and a V producer.  head_dim 64, 128 or 256: tiles are stored as head_dim /
-//    64 column groups of 64 elements.  At 64 and 128, <= 97 KB of shared memory
-//    and 256 TMEM columns, so two blocks share an SM and cover each other's
-//    start-up and tail; at 256, ~193 KB and 512 columns, one block per SM.
+//  * work item = (128-query tile, head, sequence).  The kernel is persistent:
+//    one block per resident slot (two per SM at head_dim <= 128), each taking
+//    items with a stride of the grid (sequences in the given dispatch order,
+//    a sequence's later query tiles first, heads innermost).  Key tiles are
+//    counted across a block's items, so the next item's Q and first K/V tiles
+//    load while the current one finishes.  7 warps: one softmax warpgroup (one
+//    query row per thread = one TMEM lane), a K producer (which also loads Q),
+//    an MMA issuer and a V producer.  head_dim 64, 128 or 256: tiles are stored
+//    as head_dim / 64 column groups of 64 elements.  At 64 and 128, <= 97 KB of
+//    shared memory and 256 TMEM columns, so two blocks share an SM and cover
+//    each other's hand-offs; at 256, ~193 KB and 512 columns, one block per SM.
 //  * Q tile: two 3-D TMA loads (one per 64-wide half of head_dim, 128B
-//    swizzle), issued before the block-wide set-up barrier.  K/V: per 16-key
-//    chunk the producers follow the block table (32 entries at a time) and
-//    issue 2-D TMA loads of the rows (128B swizzle) into 2-stage K and V rings
-//    of 64-key tiles, each chunk's boxes by the lane holding its table entry; a
-//    K tile is released when its S MMA completes, a V tile when its P.V
-//    completes (the completion barriers of S/P buffer j & 1 serve for both).
+//    swizzle), once every S of the block's previous item has completed.  K/V:
+//    per 16-key chunk the producers follow the block table (32 entries at a
+//    time) and issue 2-D TMA loads of the rows (128B swizzle) into 2-stage K
+//    and V rings of 64-key tiles, each chunk's boxes by the lane holding its
+//    table entry; a K tile is released when its S MMA completes, a V tile when
+//    its P.V completes (the completion barriers of S/P buffer j & 1 serve for
+//    both).  O is released to the next item's first P.V once the epilogue has
+//    read it.
 //  * S = Q K^T: 8 tcgen05.mma (M=128, N=64, K=16, fp32 accumulate) into one of
 //    two 64-column TMEM buffers.  Buffer j & 1 is reused for S(j+2) only after
 //    P.V(j), which reads the P stored there, has completed.
@@ -95,11 +102,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[kKStages], v_full[kVStages];
   // s_free[b] completes when the P.V of buffer b's tile finishes (one phase
   // per two tiles), so it doubles as that P.V's completion signal.
-  uint64_t s_full[2], s_free[2], p_full[2], drain;
+  uint64_t s_full[2], s_free[2], p_full[2];
+  uint64_t o_free;  // the epilogue has read O: the next tile's first P.V may overwrite it
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -252,49 +261,74 @@ __device__ __forceinline__ float half_to_float(uint32_t bits16) {
   }
 }
 
-template <bool BF16, int D>
-__global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
-    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using C = Cfg<D>;
-  const int qt = blockIdx.x, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int seq = blockIdx.z;
+// One work item: 128-query tile `q0 / kQTile` of sequence `seq`, head `h`.
+struct Tile {
+  int seq, h, q_begin, q0;
+  int rows;  // valid query rows
+  int pos0;  // position of the first query
+  int keys;  // keys any row of the tile sees
+  int T;     // 64-key tiles
+  bool valid;
+};
+
+// Item `it` of the launch: dispatch position z (through seq_order), then the
+// later (longer) query tiles of that sequence first, heads innermost.  Every
+// thread decodes the same items from the same device values, so all roles
+// agree on which items exist.
+__device__ __forceinline__ Tile decode_tile(const PrefillParams& p, int it, int num_seqs,
+                                            int num_qtiles, bool report) {
+  Tile w;
+  w.valid = false;
+  const int per_seq = p.num_heads * num_qtiles;
+  const int z = it / per_seq, rem = it % per_seq;
+  const int qt = num_qtiles - 1 - rem / p.num_heads;
+  w.h = rem % p.num_heads;
+  int seq = z;
   if (p.seq_order != nullptr) {
-    seq = __ldg(p.seq_order + blockIdx.z);
-    if (static_cast<unsigned>(seq) >= gridDim.z) {
-      if (threadIdx.x == 0 && qt == 0 && h == 0)
-        report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.z, seq);
-      return;
+    seq = __ldg(p.seq_order + z);
+    if (static_cast<unsigned>(seq) >= static_cast<unsigned>(num_seqs)) {
+      if (report && rem == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, z, seq);
+      return w;
     }
   }
-
-  int L = p.seq_lens[seq];
-  const int q_begin = p.query_start[seq];
-  int nq = p.query_start[seq + 1] - q_begin;
+  w.seq = seq;
+  int L = __ldg(p.seq_lens + seq);
+  w.q_begin = __ldg(p.query_start + seq);
+  const int nq = __ldg(p.query_start + seq + 1) - w.q_begin;
   const int cap = p.max_blocks * p.block_size;
   // Lengths and query ranges come from device memory: a bad one is recorded and
   // the sequence is clamped or skipped, never used to address memory.
   const bool bad_len = L < 0 || L > cap;
   L = L < 0 ? 0 : (L > cap ? cap : L);
-  const bool bad_q = nq < 0 || nq > L || q_begin < 0 || q_begin > p.total_queries - nq ||
-                     nq > static_cast<int>(gridDim.x) * kQTile;
+  const bool bad_q = nq < 0 || nq > L || w.q_begin < 0 || w.q_begin > p.total_queries - nq ||
+                     nq > num_qtiles * kQTile;
   if (bad_len || bad_q) {
-    if (threadIdx.x == 0 && qt == 0 && h == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, L);
-    if (bad_q) nq = 0;
+    if (report && rem == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, L);
+    if (bad_q) return w;
   }
-  const int q0 = qt * kQTile;
-  if (q0 >= nq) return;
-  const int rows = min(kQTile, nq - q0);   // query rows of this tile
-  const int pos0 = L - nq + q0;            // position of the tile's first query
-  const int keys = pos0 + rows;            // keys any row of the tile may see
-  const int T = (keys + kKTile - 1) / kKTile;
+  w.q0 = qt * kQTile;
+  if (w.q0 >= nq) return w;
+  w.rows = min(kQTile, nq - w.q0);
+  w.pos0 = L - nq + w.q0;
+  w.keys = w.pos0 + w.rows;
+  w.T = (w.keys + kKTile - 1) / kKTile;
+  w.valid = true;
+  return w;
+}
+
+template <bool BF16, int D>
+__global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const PrefillParams p,
+                         const int num_seqs, const int num_qtiles) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   if (pad > C::kAlignSlack) {  // never seen: the base is 1 KB aligned in practice
-    if (threadIdx.x == 0) report_error(p.err, PA_ERR_UNSUPPORTED, seq, static_cast<int>(pad));
+    if (threadIdx.x == 0) report_error(p.err, PA_ERR_UNSUPPORTED, -1, static_cast<int>(pad));
     return;
   }
   uint8_t* smem = smem_raw + pad;
@@ -303,31 +337,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
   volatile int* abort_flag = &bars->abort;
   auto k_tile = [&](int s) { return smem + C::kOffK + s * C::kTileBytes; };
   auto v_tile = [&](int s) { return smem + C::kOffV + s * C::kTileBytes; };
-
-  // Started before the block-wide barrier so that their latency overlaps the
-  // set-up: the Q tile load (its barrier initialised by the issuing thread)
-  // and the producers' first block-table entries.
   // With 8-token blocks a 16-key chunk spans two blocks: rows 0-7 come from the
   // block of its first key, rows 8-15 from the next one (boxes of 8 rows).
   const bool half_blocks = p.block_size < 16;
-  int blk_first = 0, blk_first_hi = 0;  // producers: physical block(s) of chunk `lane`
-  if (warp == kWarpK || warp == kWarpV) {
-    if (lane * 16 < keys)
-      blk_first = __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks +
-                        lane * 16 / p.block_size);
-    if (half_blocks && lane * 16 + 8 < keys)
-      blk_first_hi = __ldg(p.block_tables + static_cast<size_t>(seq) * p.max_blocks +
-                           (lane * 16 + 8) / p.block_size);
-    if (warp == kWarpK && lane == 0) {
-      mbar_init(&bars->q_full, 1);
-      fence_mbar_init();
-      mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
-#pragma unroll
-      for (int g = 0; g < C::kGroups; ++g)
-        tma_load_3d(Qs + g * kQHalfBytes, &tm_q, 64 * g, h, q_begin + q0, &bars->q_full);
-    }
-  }
+
   if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kKStages; ++s) mbar_init(&bars->k_full[s], 1);
     for (int s = 0; s < kVStages; ++s) mbar_init(&bars->v_full[s], 1);
     for (int b = 0; b < 2; ++b) {
@@ -335,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       mbar_init(&bars->s_free[b], 1);
       mbar_init(&bars->p_full[b], kQTile);
     }
+    mbar_init(&bars->o_free, kQTile);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -350,280 +367,342 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  const int n_items = num_seqs * p.num_heads * num_qtiles;
 
-  int kv_issued = 0;   // producer lane 0: tiles whose loads (K or V) were issued
-  int mma_started = 0; // MMA lane 0: whether any MMA was issued
+  // Key tiles are counted across the block's items: tile g of the block uses K
+  // and V stage g & 1 and S/P buffer g & 1, and its barriers' phases are g >> 1.
+  int kv_issued = 0;    // producers: tiles whose loads were issued (all lanes agree)
+  int q_issued = 0;     // K producer: Q tiles whose loads were issued
+  int mma_started = 0;  // MMA lane 0: whether any MMA was issued
   if (warp == kWarpK || warp == kWarpV) {
-    // ------------------------------------------------- producers: K and V
+    // ------------------------------------------------- producers: K (+Q) and V
     const bool is_v = (warp == kWarpV);
-    const int stages = is_v ? kVStages : kKStages;
-    const int32_t* table = p.block_tables + static_cast<size_t>(seq) * p.max_blocks;
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-    int blk = 0, blk_hi = 0;
-    for (int j = 0; j < T; ++j) {
-      if ((j & 7) == 0) {
-        // lane l looks up the physical block of 16-key chunk 4*j + l (8 tiles' worth)
-        // (and, with 8-token blocks, that of its second half)
-        const int key0 = (j * 4 + lane) * 16;
-        blk = 0;
-        blk_hi = 0;
-        if (key0 < keys) {
-          blk = j == 0 ? blk_first : __ldg(table + key0 / p.block_size);
-          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-            if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk);
-            blk = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const Tile w = decode_tile(p, it, num_seqs, num_qtiles, !is_v && lane == 0);
+      if (!w.valid) continue;
+      const int32_t* table = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks;
+      int blk = 0, blk_hi = 0;
+      for (int j = 0; j < w.T; ++j) {
+        if ((j & 7) == 0) {
+          // lane l looks up the physical block of 16-key chunk 4*j + l (8 tiles'
+          // worth) (and, with 8-token blocks, that of its second half)
+          const int key0 = (j * 4 + lane) * 16;
+          blk = 0;
+          blk_hi = 0;
+          if (key0 < w.keys) {
+            blk = __ldg(table + key0 / p.block_size);
+            if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+              if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, w.seq, blk);
+              blk = 0;
+            }
+          }
+          if (half_blocks && key0 + 8 < w.keys) {
+            blk_hi = __ldg(table + (key0 + 8) / p.block_size);
+            if (static_cast<unsigned>(blk_hi) >= static_cast<unsigned>(p.num_blocks)) {
+              if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, w.seq, blk_hi);
+              blk_hi = 0;
+            }
           }
         }
-        if (half_blocks && key0 + 8 < keys) {
-          blk_hi = j == 0 ? blk_first_hi : __ldg(table + (key0 + 8) / p.block_size);
-          if (static_cast<unsigned>(blk_hi) >= static_cast<unsigned>(p.num_blocks)) {
-            if (!is_v) report_error(p.err, PA_ERR_BAD_BLOCK, seq, blk_hi);
-            blk_hi = 0;
-          }
-        }
-      }
-      const int s = j % stages, use = j / stages;
-      // rows loaded: 16 per chunk holding visible keys; with 8-token blocks a
-      // chunk whose second half holds none loads 8
-      const int kt0 = j * kKTile;
-      int rows_loaded = 16 * min(4, (keys - kt0 + 15) / 16);
-      if (half_blocks && keys - kt0 < kKTile && (keys - kt0) % 16 != 0 && (keys - kt0) % 16 <= 8)
-        rows_loaded -= 8;
-      uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
-      // A K stage is free once the S that read it has completed, a V stage once
-      // the P.V that read it has: with two stages of each and two S/P buffers,
-      // those are s_full[s] and s_free[s].  (The next completion on either
-      // barrier needs the load being waited for, so no phase can be skipped.)
-      uint64_t* empty = is_v ? &bars->s_free[s] : &bars->s_full[s];
-      uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
-      int ok = 1;
-      if (lane == 0) {
-        if (use > 0) ok = mbar_wait_bounded(empty, (use - 1) & 1);
-        if (ok)
-          mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows_loaded) * C::kGroups * 128);
-      }
-      ok = __shfl_sync(kFullMask, ok, 0);
-      if (!ok) {
+        const int g = kv_issued, s = g & 1, use = g >> 1;
+        // rows loaded: 16 per chunk holding visible keys; with 8-token blocks a
+        // chunk whose second half holds none loads 8
+        const int kt0 = j * kKTile;
+        int rows_loaded = 16 * min(4, (w.keys - kt0 + 15) / 16);
+        if (half_blocks && w.keys - kt0 < kKTile && (w.keys - kt0) % 16 != 0 &&
+            (w.keys - kt0) % 16 <= 8)
+          rows_loaded -= 8;
+        uint64_t* full = is_v ? &bars->v_full[s] : &bars->k_full[s];
+        // A K stage is free once the S that read it has completed, a V stage once
+        // the P.V that read it has: with two stages of each and two S/P buffers,
+        // those are s_full[s] and s_free[s].  (The next completion on either
+        // barrier needs the load being waited for, so no phase can be skipped.)
+        uint64_t* empty = is_v ? &bars->s_free[s] : &bars->s_full[s];
+        uint8_t* dst = is_v ? v_tile(s) : k_tile(s);
+        int good = 1;
         if (lane == 0) {
-          *abort_flag = 1;
-          report_error(p.err, PA_ERR_TIMEOUT, seq, j);
+          if (use > 0) good = mbar_wait_bounded(empty, (use - 1) & 1);
+          if (good)
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows_loaded) * C::kGroups * 128);
         }
-        break;
-      }
-      // Lanes 4 (j % 8) .. 4 (j % 8) + 3 hold the blocks of this tile's four
-      // chunks (and, with 8-token blocks, of their second halves): each issues
-      // its own chunk's boxes, so a tile's loads go out in one warp instruction
-      // per column group rather than one thread's sequence of them (the
-      // producers sit on the critical path: 267 -> 235 us on the chunked-prefill
-      // batch).
-      {
-        const int c = lane - (j & 7) * 4;
-        const int k0 = j * kKTile + c * 16;
-        if (c >= 0 && c < 4 && k0 < keys) {
-          const int row = (blk * p.num_heads + h) * p.block_size + k0 % p.block_size;
+        good = __shfl_sync(kFullMask, good, 0);
+        if (!good) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report_error(p.err, PA_ERR_TIMEOUT, w.seq, j);
+          }
+          ok = false;
+          break;
+        }
+        // Lanes 4 (j % 8) .. 4 (j % 8) + 3 hold the blocks of this tile's four
+        // chunks (and, with 8-token blocks, of their second halves): each issues
+        // its own chunk's boxes, so a tile's loads go out in one warp instruction
+        // per column group rather than one thread's sequence of them (the
+        // producers sit on the critical path).
+        {
+          const int c = lane - (j & 7) * 4;
+          const int k0 = j * kKTile + c * 16;
+          if (c >= 0 && c < 4 && k0 < w.keys) {
+            const int row = (blk * p.num_heads + w.h) * p.block_size + k0 % p.block_size;
 #pragma unroll
-          for (int g = 0; g < C::kGroups; ++g)
-            tma_load_2d(dst + g * kHalfBytes + c * 2048, map, 64 * g, row, full);
-          if (half_blocks && k0 + 8 < keys) {
-            const int row_hi = (blk_hi * p.num_heads + h) * p.block_size;
+            for (int gr = 0; gr < C::kGroups; ++gr)
+              tma_load_2d(dst + gr * kHalfBytes + c * 2048, map, 64 * gr, row, full);
+            if (half_blocks && k0 + 8 < w.keys) {
+              const int row_hi = (blk_hi * p.num_heads + w.h) * p.block_size;
 #pragma unroll
-            for (int g = 0; g < C::kGroups; ++g)
-              tma_load_2d(dst + g * kHalfBytes + c * 2048 + 1024, map, 64 * g, row_hi, full);
+              for (int gr = 0; gr < C::kGroups; ++gr)
+                tma_load_2d(dst + gr * kHalfBytes + c * 2048 + 1024, map, 64 * gr, row_hi, full);
+            }
           }
         }
+        kv_issued = g + 1;
+        if (!is_v && j == 0) {
+          // This item's Q tile, once every S of the previous item has completed
+          // (issued after K(0) so that tile's latency overlaps the wait).
+          if (lane == 0) {
+            if (q_issued > 0) good = mbar_wait_bounded(&bars->q_empty, (q_issued - 1) & 1);
+            if (good) {
+              mbar_arrive_expect_tx(&bars->q_full, C::kQBytes);
+#pragma unroll
+              for (int gr = 0; gr < C::kGroups; ++gr)
+                tma_load_3d(Qs + gr * kQHalfBytes, &tm_q, 64 * gr, w.h, w.q_begin + w.q0,
+                            &bars->q_full);
+            }
+          }
+          good = __shfl_sync(kFullMask, good, 0);
+          if (!good) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              report_error(p.err, PA_ERR_TIMEOUT, w.seq, -3);
+            }
+            ok = false;
+            break;
+          }
+          ++q_issued;
+        }
+        __syncwarp();
+        if (__shfl_sync(kFullMask, *abort_flag, 0)) {
+          ok = false;
+          break;
+        }
       }
-      kv_issued = j + 1;
-      __syncwarp();
-      if (__shfl_sync(kFullMask, *abort_flag, 0)) break;
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(kQTile, kKTile, BF16, false);
       constexpr uint32_t idesc_o = make_idesc(kQTile, D, BF16, true);
-      bool ok = mbar_wait_bounded(&bars->q_full, 0);
-      // S_j goes to TMEM buffer j & 1, whose previous contents (P of tile j-2)
-      // must have been consumed by P.V(j-2).
       // descriptors of the tile bases; an offset within a tile is added to the
       // start-address field (16-byte units, no carry: shared memory < 256 KB)
       const uint64_t q_desc = smem_desc_sw128(Qs, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(k_tile(0), 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(v_tile(0), kHalfBytes, 1024);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kKStages, b = j & 1;
-        if (!mbar_wait_bounded(&bars->k_full[s], (j / kKStages) & 1)) return false;
-        if (j >= 2 && !mbar_wait_bounded(&bars->s_free[b], ((j >> 1) - 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int half = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t a = q_desc + static_cast<uint64_t>((half * kQHalfBytes + off) >> 4);
-          const uint64_t bd = k_desc + static_cast<uint64_t>((half * kHalfBytes + off) >> 4);
-          mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
-        }
-        mma_commit(&bars->s_full[b]);  // also frees K stage s (= b: two stages)
-        mma_started = 1;
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        const int s = j % kVStages, b = j & 1;
-        if (!mbar_wait_bounded(&bars->p_full[b], (j >> 1) & 1) ||
-            !mbar_wait_bounded(&bars->v_full[s], (j / kVStages) & 1)) {
+      int g = 0, items = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+        const Tile w = decode_tile(p, it, num_seqs, num_qtiles, false);
+        if (!w.valid) continue;
+        if (!mbar_wait_bounded(&bars->q_full, items & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
-        const uint32_t ph = tmem + b * kKTile, pl = ph + kKTile / 2;
+        const int g0 = g;
+        // S of the block's tile gg goes to TMEM buffer gg & 1, whose previous
+        // contents (P of tile gg - 2) must have been consumed by P.V(gg - 2).
+        // After the item's last S, Q is released for the next item.
+        auto issue_s = [&](int gg, bool last) -> bool {
+          const int b = gg & 1;
+          if (!mbar_wait_bounded(&bars->k_full[b], (gg >> 1) & 1)) return false;
+          if (gg >= 2 && !mbar_wait_bounded(&bars->s_free[b], ((gg >> 1) - 1) & 1)) return false;
+          tc_fence_after();
+          const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((b * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kKTile / 16; ++kk) {
-          const uint64_t bd = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
-          mma_f16_ts(tmem + kTmemO, ph + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_f16_ts(tmem + kTmemO, pl + kk * 8, bd, idesc_o, 1u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int half = kk >> 2, off = (kk & 3) * 32;
+            const uint64_t a = q_desc + static_cast<uint64_t>((half * kQHalfBytes + off) >> 4);
+            const uint64_t bd = k_desc + static_cast<uint64_t>((half * kHalfBytes + off) >> 4);
+            mma_f16(tmem + b * kKTile, a, bd, idesc_s, kk > 0);
+          }
+          mma_commit(&bars->s_full[b]);  // also frees K stage b (two stages)
+          if (last) mma_commit(&bars->q_empty);
+          mma_started = 1;
+          return true;
+        };
+        ok = issue_s(g0, w.T == 1);
+        for (int j = 0; ok && j < w.T; ++j) {
+          const int gg = g0 + j, b = gg & 1;
+          if (j + 1 < w.T && !issue_s(gg + 1, j + 2 == w.T)) {
+            ok = false;
+            break;
+          }
+          // the item's first P.V overwrites O: the previous item's epilogue must
+          // have read it
+          if (j == 0 && items > 0 && !mbar_wait_bounded(&bars->o_free, (items - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_bounded(&bars->p_full[b], (gg >> 1) & 1) ||
+              !mbar_wait_bounded(&bars->v_full[b], (gg >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((b * C::kTileBytes) >> 4);
+          const uint32_t ph = tmem + b * kKTile, pl = ph + kKTile / 2;
+#pragma unroll
+          for (int kk = 0; kk < kKTile / 16; ++kk) {
+            const uint64_t bd = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
+            mma_f16_ts(tmem + kTmemO, ph + kk * 8, bd, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(tmem + kTmemO, pl + kk * 8, bd, idesc_o, 1u);
+          }
+          mma_commit(&bars->s_free[b]);  // also frees V stage b (two stages)
         }
-        mma_commit(&bars->s_free[b]);  // also frees V stage s (= b: two stages)
+        g = g0 + w.T;
+        ++items;
       }
       if (!ok) {
         *abort_flag = 1;
-        report_error(p.err, PA_ERR_TIMEOUT, seq, -1);
+        report_error(p.err, PA_ERR_TIMEOUT, -1, -1);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int r = threadIdx.x;  // query row = TMEM lane
-    const bool row_valid = r < rows;
-    const int pos = row_valid ? pos0 + r : -1;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float m_ref = -INFINITY, l = 0.f;  // reference max (log2 units) and running sum
+    int g = 0;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[b], (j >> 1) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      float sv[kKTile];
-      {
-        float t[32];
-        tmem_ld32(tmem + lane_base + b * kKTile, t);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c] = t[c];
-        tmem_ld32(tmem + lane_base + b * kKTile + 32, t);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
-      }
-      // Raw scores; keys a row may not see become -inf.  Only tiles that
-      // cross some row's causal limit (the diagonal and the last tile) need it.
-      const int kbase = j * kKTile;
-      if (!__all_sync(kFullMask, kbase + kKTile - 1 <= pos)) {
-#pragma unroll
-        for (int c = 0; c < kKTile; ++c) sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
-      }
-      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-      for (int c = 4; c < kKTile; c += 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], sv[c + i]);
-      }
-      // scale > 0, so the max of the scaled scores is the scaled max (log2 units)
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.qscale;
-      // Move the reference only when the tile's max exceeds it by the threshold.
-      float alpha = 1.f;
-      if (mt > m_ref + kRescaleThreshold) {
-        alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
-        m_ref = mt;
-      }
-      // No visible key yet (or an unused row): a -inf offset makes every p zero.
-      const float neg_ref = (m_ref == -INFINITY) ? -INFINITY : -m_ref;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      // P as hi + lo halves, two 16-bit values per 32-bit TMEM column
-      float hi_f[32], lo_f[32];
-#pragma unroll
-      for (int c = 0; c < kKTile; c += 2) {
-        float x0, x1;
-        fma2(x0, x1, sv[c], sv[c + 1], p.qscale, neg_ref);
-        const float e0 = ex2_approx(x0);
-        const float e1 = ex2_approx(x1);
-        add2(sum4[c & 2], sum4[(c & 2) + 1], e0, e1);
-        if constexpr (BF16) {
-          // hi = the upper 16 bits of each fp32 p (a bf16 truncation), one byte
-          // permute for the pair; lo = RN(p - hi), where p - hi is exact in fp32
-          // and below one bf16 ulp of p, so hi + lo keeps ~16 significant bits
-          const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
-          float d0, d1;
-          sub2(d0, d1, e0, e1, __uint_as_float(b0 & 0xffff0000u),
-               __uint_as_float(b1 & 0xffff0000u));
-          hi_f[c / 2] = __uint_as_float(__byte_perm(b0, b1, 0x7632));
-          lo_f[c / 2] = __uint_as_float(pack_half2<true>(d0, d1));
-        } else {
-          const uint32_t hi = pack_half2<false>(e0, e1);
-          const float r0 = half_to_float<false>(hi & 0xffffu);
-          const float r1 = half_to_float<false>(hi >> 16);
-          hi_f[c / 2] = __uint_as_float(hi);
-          lo_f[c / 2] = __uint_as_float(pack_half2<false>(e0 - r0, e1 - r1));
-        }
-      }
-      const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      // O must not change under a running P.V: rescaling waits for P.V(j-1).
-      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
-        ok = __all_sync(kFullMask,
-                        mbar_wait_bounded(&bars->s_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const Tile w = decode_tile(p, it, num_seqs, num_qtiles, false);
+      if (!w.valid) continue;
+      const bool row_valid = r < w.rows;
+      const int pos = row_valid ? w.pos0 + r : -1;
+      float m_ref = -INFINITY, l = 0.f;  // reference max (log2 units) and running sum
+      for (int j = 0; j < w.T; ++j) {
+        const int gg = g + j, b = gg & 1;
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->s_full[b], (gg >> 1) & 1));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          float o[32];
-          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
+        float sv[kKTile];
+        {
+          float t[32];
+          tmem_ld32(tmem + lane_base + b * kKTile, t);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + lane_base + kTmemO + cc * 32, o);
+          for (int c = 0; c < 32; ++c) sv[c] = t[c];
+          tmem_ld32(tmem + lane_base + b * kKTile + 32, t);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 + c] = t[c];
+        }
+        // Raw scores; keys a row may not see become -inf.  Only tiles that
+        // cross some row's causal limit (the diagonal and the last tile) need it.
+        const int kbase = j * kKTile;
+        if (!__all_sync(kFullMask, kbase + kKTile - 1 <= pos)) {
+#pragma unroll
+          for (int c = 0; c < kKTile; ++c) sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
+        }
+        float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int c = 4; c < kKTile; c += 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], sv[c + i]);
+        }
+        // scale > 0, so the max of the scaled scores is the scaled max (log2 units)
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.qscale;
+        // Move the reference only when the tile's max exceeds it by the threshold.
+        float alpha = 1.f;
+        if (mt > m_ref + kRescaleThreshold) {
+          alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mt);
+          m_ref = mt;
+        }
+        // No visible key yet (or an unused row): a -inf offset makes every p zero.
+        const float neg_ref = (m_ref == -INFINITY) ? -INFINITY : -m_ref;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        // P as hi + lo halves, two 16-bit values per 32-bit TMEM column
+        float hi_f[32], lo_f[32];
+#pragma unroll
+        for (int c = 0; c < kKTile; c += 2) {
+          float x0, x1;
+          fma2(x0, x1, sv[c], sv[c + 1], p.qscale, neg_ref);
+          const float e0 = ex2_approx(x0);
+          const float e1 = ex2_approx(x1);
+          add2(sum4[c & 2], sum4[(c & 2) + 1], e0, e1);
+          if constexpr (BF16) {
+            // hi = the upper 16 bits of each fp32 p (a bf16 truncation), one byte
+            // permute for the pair; lo = RN(p - hi), where p - hi is exact in fp32
+            // and below one bf16 ulp of p, so hi + lo keeps ~16 significant bits
+            const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
+            float d0, d1;
+            sub2(d0, d1, e0, e1, __uint_as_float(b0 & 0xffff0000u),
+                 __uint_as_float(b1 & 0xffff0000u));
+            hi_f[c / 2] = __uint_as_float(__byte_perm(b0, b1, 0x7632));
+            lo_f[c / 2] = __uint_as_float(pack_half2<true>(d0, d1));
+          } else {
+            const uint32_t hi = pack_half2<false>(e0, e1);
+            const float r0 = half_to_float<false>(hi & 0xffffu);
+            const float r1 = half_to_float<false>(hi >> 16);
+            hi_f[c / 2] = __uint_as_float(hi);
+            lo_f[c / 2] = __uint_as_float(pack_half2<false>(e0 - r0, e1 - r1));
+          }
+        }
+        const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        // O must not change under a running P.V: rescaling waits for P.V(gg-1).
+        if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+          ok = __all_sync(kFullMask,
+                          mbar_wait_bounded(&bars->s_free[(gg - 1) & 1], ((gg - 1) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tmem + lane_base + kTmemO + cc * 32, o);
+          }
+        }
+        // P replaces S in this tile's buffer (S has been read into registers)
+        tmem_st32(tmem + lane_base + b * kKTile, hi_f);
+        tmem_st32(tmem + lane_base + b * kKTile + kKTile / 2, lo_f);
+        tmem_wait_st();
+        // keys past the last one any row may see: zero their V rows once the tile
+        // has landed (they may hold stale or unused-slot data; 0 * NaN is NaN)
+        if (j == w.T - 1 && w.keys < kbase + kKTile) {
+          ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->v_full[b], (gg >> 1) & 1));
+          if (!ok) break;
+          uint8_t* vs = v_tile(b);
+          const int first = w.keys - kbase;
+          constexpr int kPieces = C::kGroups * 8;  // 16-byte pieces per row
+          const int n16 = (kKTile - first) * kPieces;
+          for (int idx = r; idx < n16; idx += kQTile) {
+            const int row = first + idx / kPieces;
+            const int rest = idx % kPieces;
+            *reinterpret_cast<uint4*>(vs + (rest >> 3) * kHalfBytes + row * 128 +
+                                      (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        }
+        l = l * alpha + rowsum;
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[b]);
+        if (__shfl_sync(kFullMask, *abort_flag, 0)) {
+          ok = false;
+          break;
         }
       }
-      // P replaces S in this tile's buffer (S has been read into registers)
-      tmem_st32(tmem + lane_base + b * kKTile, hi_f);
-      tmem_st32(tmem + lane_base + b * kKTile + kKTile / 2, lo_f);
-      tmem_wait_st();
-      // keys past the last one any row may see: zero their V rows once the tile
-      // has landed (they may hold stale or unused-slot data; 0 * NaN is NaN)
-      if (j == T - 1 && keys < kbase + kKTile) {
-        const int s = j % kVStages;
-        ok = __all_sync(kFullMask, mbar_wait_bounded(&bars->v_full[s], (j / kVStages) & 1));
-        if (!ok) break;
-        uint8_t* vs = v_tile(s);
-        const int first = keys - kbase;
-        constexpr int kPieces = C::kGroups * 8;     // 16-byte pieces per row
-        const int n16 = (kKTile - first) * kPieces;
-        for (int idx = r; idx < n16; idx += kQTile) {
-          const int row = first + idx / kPieces;
-          const int rest = idx % kPieces;
-          *reinterpret_cast<uint4*>(vs + (rest >> 3) * kHalfBytes + row * 128 + (rest & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_async_smem();
-      }
-      l = l * alpha + rowsum;
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[b]);
-      if (__shfl_sync(kFullMask, *abort_flag, 0)) {
-        ok = false;
-        break;
-      }
-    }
-    // the last P.V (earlier ones finish first: the tensor pipe runs in order)
-    if (ok)
+      if (!ok) break;
+      // the item's last P.V (earlier ones finish first: they come from one thread
+      // into the same accumulator), then the epilogue; O is then free
+      const int g_last = g + w.T - 1;
       ok = __all_sync(kFullMask,
-                      mbar_wait_bounded(&bars->s_free[(T - 1) & 1], ((T - 1) >> 1) & 1));
-    if (ok) {
+                      mbar_wait_bounded(&bars->s_free[g_last & 1], (g_last >> 1) & 1));
+      if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t row_off =
-          (static_cast<size_t>(q_begin + q0 + r) * p.num_heads + h) * D;
+          (static_cast<size_t>(w.q_begin + w.q0 + r) * p.num_heads + w.h) * D;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
@@ -636,9 +715,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
             store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
         }
       }
-    } else if (lane == 0) {
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+      g += w.T;
+    }
+    if (!ok && lane == 0) {
       *abort_flag = 1;
-      report_error(p.err, PA_ERR_TIMEOUT, seq, -2);
+      report_error(p.err, PA_ERR_TIMEOUT, -2, warp);
     }
   }
 
@@ -649,12 +732,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     // memory and TMEM are released (bounded waits).
     if ((warp == kWarpK || warp == kWarpV) && lane == 0) {
       const bool is_v = (warp == kWarpV);
-      const int stages = is_v ? kVStages : kKStages;
-      for (int s = 0; s < stages && s < kv_issued; ++s) {
-        const int last = s + ((kv_issued - 1 - s) / stages) * stages;
-        mbar_wait_bounded(is_v ? &bars->v_full[s] : &bars->k_full[s], (last / stages) & 1);
+      for (int s = 0; s < 2 && s < kv_issued; ++s) {
+        const int last = s + ((kv_issued - 1 - s) / 2) * 2;  // last tile issued into stage s
+        mbar_wait_bounded(is_v ? &bars->v_full[s] : &bars->k_full[s], (last >> 1) & 1);
       }
-      if (!is_v) mbar_wait_bounded(&bars->q_full, 0);
+      if (!is_v && q_issued > 0) mbar_wait_bounded(&bars->q_full, (q_issued - 1) & 1);
     }
     if (warp == kWarpMma && lane == 0 && mma_started) {
       mma_commit(&bars->drain);
@@ -682,9 +764,19 @@ cudaError_t ensure_prefill_smem() {
 
 template <bool BF16, int D>
 int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                   const PrefillParams& p, dim3 grid, cudaStream_t st) {
+                   const PrefillParams& p, int num_seqs, int num_qtiles, cudaStream_t st) {
   if (ensure_prefill_smem<BF16, D>() != cudaSuccess) return PA_ERR_CUDA;
-  paged_prefill_kernel<BF16, D><<<grid, kThreads, Cfg<D>::kSmemBytes, st>>>(tq, tk, tv, p);
+  // Persistent: one block per resident slot (Cfg<D>::kMinBlocks per SM), each
+  // looping over the (sequence, query tile, head) items with a stride of the grid.
+  int device = 0, sms = 0;
+  if (cudaGetDevice(&device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const long long items = static_cast<long long>(num_seqs) * p.num_heads * num_qtiles;
+  const long long slots = static_cast<long long>(sms) * Cfg<D>::kMinBlocks;
+  const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
+  paged_prefill_kernel<BF16, D>
+      <<<grid, kThreads, Cfg<D>::kSmemBytes, st>>>(tq, tk, tv, p, num_seqs, num_qtiles);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -768,14 +860,17 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   p.total_queries = total_queries;
   p.qscale = scale * kLog2e;
 
-  const dim3 grid((max_query_len + kQTile - 1) / kQTile, num_heads, num_seqs);
+  const int qtiles = static_cast<int>((static_cast<long long>(max_query_len) + kQTile - 1) / kQTile);
+  // items are numbered in an int inside the kernel
+  if (static_cast<long long>(num_seqs) * num_heads * qtiles >= (1ll << 31))
+    return PA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch ((bf16 ? 1 : 0) | (head_dim == 64 ? 0 : head_dim == 128 ? 2 : 4)) {
-    case 0: return launch_prefill<false, 64>(tq, tk, tv, p, grid, st);
-    case 1: return launch_prefill<true, 64>(tq, tk, tv, p, grid, st);
-    case 2: return launch_prefill<false, 128>(tq, tk, tv, p, grid, st);
-    case 3: return launch_prefill<true, 128>(tq, tk, tv, p, grid, st);
-    case 4: return launch_prefill<false, 256>(tq, tk, tv, p, grid, st);
-    default: return launch_prefill<true, 256>(tq, tk, tv, p, grid, st);
+    case 0: return launch_prefill<false, 64>(tq, tk, tv, p, num_seqs, qtiles, st);
+    case 1: return launch_prefill<true, 64>(tq, tk, tv, p, num_seqs, qtiles, st);
+    case 2: return launch_prefill<false, 128>(tq, tk, tv, p, num_seqs, qtiles, st);
+    case 3: return launch_prefill<true, 128>(tq, tk, tv, p, num_seqs, qtiles, st);
+    case 4: return launch_prefill<false, 256>(tq, tk, tv, p, num_seqs, qtiles, st);
+    default: return launch_prefill<true, 256>(tq, tk, tv, p, num_seqs, qtiles, st);
   }
 }
