@@ -8,16 +8,18 @@
 // so it runs on tensor cores:
 //
 //  * work item = (128-query tile, head, sequence).  The kernel is persistent:
-//    one block per resident slot (two per SM at head_dim <= 128), each taking
-//    items with a stride of the grid (sequences in the given dispatch order,
-//    a sequence's later query tiles first, heads innermost).  Key tiles are
-//    counted across a block's items, so the next item's Q and first K/V tiles
-//    load while the current one finishes.  7 warps: one softmax warpgroup (one
-//    query row per thread = one TMEM lane), a K producer (which also loads Q),
-//    an MMA issuer and a V producer.  head_dim 64, 128 or 256: tiles are stored
-//    as head_dim / 64 column groups of 64 elements.  At 64 and 128, <= 97 KB of
-//    shared memory and 256 TMEM columns, so two blocks share an SM and cover
-//    each other's hand-offs; at 256, ~193 KB and 512 columns, one block per SM.
+//    one block per resident slot (two per SM at head_dim <= 128).  Items are
+//    numbered sequence by sequence in the given dispatch order, a sequence's
+//    later (longer) query tiles first, heads innermost, and block b takes
+//    items b, b + grid, b + 2 grid, ...  Key tiles are counted across a
+//    block's items, so the next item's Q and first K/V tiles load while the
+//    current one finishes.  7 warps: one softmax warpgroup (one query row per
+//    thread = one TMEM lane; it also writes the output), a K producer (which
+//    also loads Q), an MMA issuer and a V producer.  head_dim 64, 128 or 256:
+//    tiles are stored as head_dim / 64 column groups of 64 elements.  At 64
+//    and 128, <= 106 KB of shared memory and 256 TMEM columns, so two blocks
+//    share an SM and cover each other's hand-offs; at 256, ~202 KB and 512
+//    columns, one block per SM.
 //  * Q tile: two 3-D TMA loads (one per 64-wide half of head_dim, 128B
 //    swizzle), once every S of the block's previous item has completed.  K/V:
 //    per 16-key chunk the producers follow the block table (32 entries at a
@@ -41,6 +43,8 @@
 //    read from TMEM and V as an MN-major shared-memory operand, accumulating
 //    in TMEM.  The commit of buffer b's P.V is also the completion signal the
 //    softmax waits on before rescaling O or reading it in the epilogue.
+//  * Epilogue: O / l leaves through 2 KB of shared memory per warp, so that
+//    each store instruction writes whole 64-byte row segments.
 //  * Every mbarrier wait is bounded (one second); on a timeout the block
 //    records PA_ERR_TIMEOUT, waits (bounded) for its copies and MMAs, frees its
 //    TMEM and returns.  Nothing traps.
@@ -79,7 +83,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffStage = kOffV + kVStages * kTileBytes;  // 4 warps x 2 KB
+  static constexpr int kOffBar = kOffStage + 8192;
   // 1 KB is left for aligning the dynamic shared-memory base to 1 KB (the
   // kernel checks it); at D <= 128 two blocks still fit an SM (228 KB, less 1 KB
   // reserved per block).
@@ -316,6 +321,13 @@ __device__ __forceinline__ Tile decode_tile(const PrefillParams& p, int it, int 
   return w;
 }
 
+// The r-th item of this block: block b takes items b, b + gridDim.x, ...
+// (Dealing every other round in reverse, to even out long and short items per
+// block, measured 2 % slower: the two blocks sharing an SM already even out.)
+__device__ __forceinline__ int item_of(int r) {
+  return r * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+}
+
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -379,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     const bool is_v = (warp == kWarpV);
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+    for (int turn = 0, it = item_of(0); ok && it < n_items; it = item_of(++turn)) {
       const Tile w = decode_tile(p, it, num_seqs, num_qtiles, !is_v && lane == 0);
       if (!w.valid) continue;
       const int32_t* table = p.block_tables + static_cast<size_t>(w.seq) * p.max_blocks;
@@ -501,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       const uint64_t v_desc0 = smem_desc_sw128(v_tile(0), kHalfBytes, 1024);
       int g = 0, items = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      for (int turn = 0, it = item_of(0); ok && it < n_items; it = item_of(++turn)) {
         const Tile w = decode_tile(p, it, num_seqs, num_qtiles, false);
         if (!w.valid) continue;
         if (!mbar_wait_bounded(&bars->q_full, items & 1)) {
@@ -575,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     int g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+    for (int turn = 0, it = item_of(0); ok && it < n_items; it = item_of(++turn)) {
       const Tile w = decode_tile(p, it, num_seqs, num_qtiles, false);
       if (!w.valid) continue;
       const bool row_valid = r < w.rows;
@@ -701,22 +713,65 @@ __global__ void __launch_bounds__(kThreads, Cfg<D>::kMinBlocks)
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const size_t row_off =
-          (static_cast<size_t>(w.q_begin + w.q0 + r) * p.num_heads + w.h) * D;
+      // Rows leave through the warp's 2 KB of the staging buffer, 64 bytes of
+      // each at a time: each lane writes its row's piece, then the warp stores
+      // whole 64-byte row segments (8 rows per instruction) rather than 16
+      // bytes of 32 rows.  Pieces sit at an XOR of (row / 2) % 4 so that
+      // neither side has bank conflicts.
+      const int esz = p.out_dtype == PA_F32 ? 4 : 2;
+      const size_t row_bytes = static_cast<size_t>(p.num_heads) * D * esz;
+      char* out_warp = static_cast<char*>(p.out) +
+                       (static_cast<size_t>(w.q_begin + w.q0 + warp * 32) * p.num_heads + w.h) *
+                           D * esz;
+      const int warp_rows = w.rows - warp * 32;  // this warp's valid rows (may be <= 0)
+      uint8_t* stage = smem + C::kOffStage + warp * 2048;
+      auto put = [&](const uint4 (&v)[4], int col_byte) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(stage + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = v[k];
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int idx = lane + 32 * i, row = idx >> 2, k = idx & 3;
+          if (row < warp_rows)
+            *reinterpret_cast<uint4*>(out_warp + row * row_bytes + col_byte + k * 16) =
+                *reinterpret_cast<const uint4*>(stage + row * 64 + ((k ^ ((row >> 1) & 3)) << 4));
+        }
+        __syncwarp();
+      };
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         float o[32];
         tmem_ld32(tmem + lane_base + kTmemO + cc * 32, o);
+        if (cc == D / 32 - 1) {  // O read: the next item's first P.V may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] *= inv;
-        if (row_valid) {
+        if (esz == 4) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8)
-            store_out<8>(p.out, row_off + cc * 32 + i, o + i, p.out_dtype);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float* f = o + hh * 16 + k * 4;
+              v[k] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                __float_as_uint(f[2]), __float_as_uint(f[3]));
+            }
+            put(v, cc * 128 + hh * 64);
+          }
+        } else {
+          uint4 v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float* f = o + k * 8;
+            v[k] = make_uint4(pack2(f[0], f[1], p.out_dtype), pack2(f[2], f[3], p.out_dtype),
+                              pack2(f[4], f[5], p.out_dtype), pack2(f[6], f[7], p.out_dtype));
+          }
+          put(v, cc * 64);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
       g += w.T;
     }
     if (!ok && lane == 0) {
@@ -767,7 +822,7 @@ int launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const PrefillParams& p, int num_seqs, int num_qtiles, cudaStream_t st) {
   if (ensure_prefill_smem<BF16, D>() != cudaSuccess) return PA_ERR_CUDA;
   // Persistent: one block per resident slot (Cfg<D>::kMinBlocks per SM), each
-  // looping over the (sequence, query tile, head) items with a stride of the grid.
+  // looping over its share of the (sequence, query tile, head) items.
   int device = 0, sms = 0;
   if (cudaGetDevice(&device) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
@@ -861,8 +916,8 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   p.qscale = scale * kLog2e;
 
   const int qtiles = static_cast<int>((static_cast<long long>(max_query_len) + kQTile - 1) / kQTile);
-  // items are numbered in an int inside the kernel
-  if (static_cast<long long>(num_seqs) * num_heads * qtiles >= (1ll << 31))
+  // items are numbered in an int inside the kernel (with a grid's worth of headroom)
+  if (static_cast<long long>(num_seqs) * num_heads * qtiles >= (1ll << 30))
     return PA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch ((bf16 ? 1 : 0) | (head_dim == 64 ? 0 : head_dim == 128 ? 2 : 4)) {
