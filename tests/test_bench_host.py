@@ -167,3 +167,13 @@ def test_parity_report_flags_an_element_out_of_bound():
     bad[2, 1, 3] += 0.05
     r = bench.parity_report(bad, ref, True)
     assert not r["ok"] and r["elements_out_of_bound"] == 1
+
+
+def test_tensor_peak_for_long_regions_is_the_sustained_one(tmp_path, monkeypatch):
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    (tmp_path / "MEASURED_PEAKS.json").write_text(__import__("json").dumps(peaks))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_bf16_peak() == (1900.0, "measured bf16_tflops")
+    assert bench.measured_bf16_peak(True) == (1700.0, "measured bf16_tflops_sustained")
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    assert bench.measured_bf16_peak(True)[1] == "fallback"
