@@ -212,3 +212,53 @@ def test_prefill_seq_order_changes_nothing_but_the_schedule(B):
     assert B.pa_error_read(rec) == [6, 1, 4, 40]
     assert not out[starts[4]:starts[5]].any()                # sequence 4 was not dispatched
     assert torch.equal(out[: starts[4]], plain[: starts[4]])
+
+
+def test_prefill_many_items_per_block(B):
+    """Far more (sequence, query tile, head) items than resident blocks: each block
+    runs ~30 items in turn, many of them empty (query tiles past a short chunk),
+    so every barrier's phase is carried across items of different lengths."""
+    rng = np.random.default_rng(101)
+    n = 600
+    lens = rng.integers(20, 700, size=n)
+    nq = np.minimum(lens, rng.choice([1, 3, 64, 128, 129, 200, 256], size=n))
+    b, q, starts = _case(101, lens, nq, 8, 16, "bf16", poison=True)
+    rec = B.new_error_record()
+    out = _run(B, b, q, starts, rec=rec)
+    again = _run(B, b, q, starts)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    assert torch.equal(out, again)
+    seqs = sorted({0, 1, n - 1} | set(rng.choice(n, size=12, replace=False).tolist()))
+    ref = _oracle(b, q, starts, seqs=seqs)
+    rows = np.concatenate([np.arange(starts[i], starts[i + 1]) for i in seqs])
+    assert_matches_oracle(out[torch.from_numpy(rows).cuda()], ref, "many items per block")
+
+
+def test_prefill_bad_ranges_between_good_items(B):
+    """Sequences whose query range is invalid (more queries than tokens) are
+    recorded and skipped by every role of the block alike: the items around them,
+    in the same blocks, stay correct."""
+    rng = np.random.default_rng(103)
+    n = 400
+    lens = rng.integers(100, 600, size=n)
+    nq = np.minimum(lens, rng.integers(1, 200, size=n))
+    b, q, starts = _case(103, lens, nq, 4, 16, "bf16", poison=False)
+    bad = np.arange(5, n, 7)
+    seen = b.context_lens.copy()
+    seen[bad] = nq[bad] - 1                   # fewer tokens than queries: invalid
+    rec = B.new_error_record()
+    out = torch.zeros((q.shape[0], 4, 128), device="cuda")
+    B.paged_attn_prefill(q, torch.from_numpy(starts).cuda(), int(nq.max()), b.k_cache,
+                         b.v_cache, torch.from_numpy(b.block_tables).cuda(),
+                         torch.from_numpy(seen).cuda(), b.scale, out=out, error_record=rec)
+    torch.cuda.synchronize()
+    r = B.pa_error_read(rec)
+    assert r[0] == 6 and r[2] in set(bad.tolist())
+    for i in bad[:5]:
+        assert not out[starts[i]:starts[i + 1]].any()
+    good = [i for i in range(n) if i % 7 != 5]
+    seqs = sorted(set(rng.choice(good, size=14, replace=False).tolist()) | {good[0], good[-1]})
+    ref = _oracle(b, q, starts, seqs=seqs)
+    rows = np.concatenate([np.arange(starts[i], starts[i + 1]) for i in seqs])
+    assert_matches_oracle(out[torch.from_numpy(rows).cuda()], ref, "good items among bad")
