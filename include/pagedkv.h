@@ -323,7 +323,8 @@ int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, i
  *   q             device [total_queries][num_heads][head_dim] in `dtype`, 16-byte aligned
  *   query_start   device int32 [num_seqs + 1], nondecreasing, query_start[num_seqs]
  *                 <= total_queries
- *   max_query_len host: >= every Q_i (sizes the grid)
+ *   max_query_len host: >= every Q_i; the work is num_seqs x num_heads x
+ *                 ceil(max_query_len / 128) items, which must be < 2^30
  *   head_dim      64, 128 or 256;  block_size: a multiple of 16, or 8 (each 16-key
  *                 chunk is then loaded as two 8-row boxes)
  *   out           device [total_queries][num_heads][head_dim] in `out_dtype`
@@ -331,7 +332,9 @@ int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, i
  * whose range is inconsistent (Q_i > L, range outside q, Q_i > max_query_len) is
  * recorded as PA_ERR_BAD_SEQ_LEN and skipped.  scale must be > 0.  Other
  * arguments as for paged_attn_decode; num_blocks * num_heads * block_size must
- * be < 2^31. */
+ * be < 2^31.  Launch: one block per resident slot on the current device, each
+ * looping over its share of the items (it reads the device's SM count on every
+ * call). */
 int paged_attn_prefill(const void* q, const int32_t* query_start, int total_queries,
                        int max_query_len, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,

@@ -875,12 +875,16 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
     return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f) || num_seqs > 65535 || num_heads > 65535)
-    return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
   const unsigned long long cache_rows =
       static_cast<unsigned long long>(num_blocks) * num_heads * block_size;
   if (cache_rows >= (1ull << 31) || static_cast<long long>(max_blocks_per_seq) * block_size >
                                         (1ll << 30))
+    return PA_ERR_INVALID_ARG;
+
+  const int qtiles = static_cast<int>((static_cast<long long>(max_query_len) + kQTile - 1) / kQTile);
+  // items are numbered in an int inside the kernel (with a grid's worth of headroom)
+  if (static_cast<long long>(num_seqs) * num_heads * qtiles >= (1ll << 30))
     return PA_ERR_INVALID_ARG;
 
   const bool bf16 = dtype == PA_BF16;
@@ -915,10 +919,6 @@ extern "C" int paged_attn_prefill_ex(const void* q, const int32_t* query_start,
   p.total_queries = total_queries;
   p.qscale = scale * kLog2e;
 
-  const int qtiles = static_cast<int>((static_cast<long long>(max_query_len) + kQTile - 1) / kQTile);
-  // items are numbered in an int inside the kernel (with a grid's worth of headroom)
-  if (static_cast<long long>(num_seqs) * num_heads * qtiles >= (1ll << 30))
-    return PA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch ((bf16 ? 1 : 0) | (head_dim == 64 ? 0 : head_dim == 128 ? 2 : 4)) {
     case 0: return launch_prefill<false, 64>(tq, tk, tv, p, num_seqs, qtiles, st);

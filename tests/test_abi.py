@@ -377,3 +377,30 @@ def test_beam_churn_reuses_sequences_exactly(lib):
     assert {b: alloc.block_table(b) for b in beams} == before
     alloc.batch_free(beams)
     assert alloc.num_free() == 3000
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(lib):
+    from paged_kv_cache_317_gb300.binding import STATUS_CODE
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    INV, UNS = STATUS_CODE["PA_ERR_INVALID_ARG"], STATUS_CODE["PA_ERR_UNSUPPORTED"]
+
+    def call(**kw):
+        a = dict(q=p, qs=p, T=64, mq=64, k=p, v=p, bt=p, sl=p, N=4, H=8, D=128, bs=16, MB=4,
+                 B=64, scale=0.125, dt=1, out=p, odt=2)
+        a.update(kw)
+        return lib.paged_attn_prefill(a["q"], a["qs"], a["T"], a["mq"], a["k"], a["v"], a["bt"],
+                                      a["sl"], a["N"], a["H"], a["D"], a["bs"], a["MB"], a["B"],
+                                      a["scale"], a["dt"], a["out"], a["odt"], None, None)
+
+    assert call(D=96) == UNS
+    assert call(bs=24) == UNS
+    assert call(dt=2) == UNS
+    assert call(odt=7) == UNS
+    assert call(qs=None) == INV
+    assert call(out=ctypes.c_void_p((1 << 20) + 8)) == INV    # not 16-byte aligned
+    assert call(scale=0.0) == INV
+    assert call(scale=float("inf")) == INV
+    assert call(B=1 << 24, H=128) == INV                      # cache rows >= 2^31
+    # 2^20 sequences x 64 heads x 16 query tiles = 2^30 items: too many
+    assert call(N=1 << 20, H=64, mq=2048, B=8) == INV
+    assert call(N=0) == 0 and call(T=0) == 0 and call(mq=0) == 0   # nothing to do
