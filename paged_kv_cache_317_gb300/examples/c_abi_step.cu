@@ -1,11 +1,15 @@
 // A decode step driven through the C ABI alone (include/pagedkv.h and
 // libpagedkv.so; no Python): host allocator, KV append, copy-on-write block
 // copy, the host decode schedule (and a second plan that reads the blocks a
-// fork shares with its parent once for both) and paged decode attention.  It
-// checks two exact properties, on both decodes:
-//  * a sequence forked from another and given the same next token decodes to
-//    the same bits as its parent, although its last block is a private copy;
-//  * a one-token sequence returns its value row exactly (one weight of 1).
+// fork shares with its parent once for both), paged decode attention and a
+// chunked prefill over the same cache.  It checks two exact properties on both
+// decodes (the first also on the prefill):
+//  * a sequence forked from another and given the same next token (or the same
+//    queries) gives the same bits as its parent, although its last block is a
+//    private copy;
+//  * a one-token sequence decodes to its value row exactly (one weight of 1);
+// and that the prefill's queries that repeat the decode's match its output
+// within 2e-3.
 // Build: nvcc -std=c++17 -I include c_abi_step.cu -L<dir> -lpagedkv -o c_abi_step
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -242,6 +246,53 @@ int main() {
     return 1;
   }
 
+  // Chunked prefill on the tensor cores over the same cache: the last 5 tokens
+  // of sequence 0 and of its fork as causal queries (the same 5 query rows for
+  // both, the last one the decode's query), and sequence 2's one token with the
+  // decode's query.  The fork must give its parent's bits, and the queries that
+  // repeat a decode's query its output within 2e-3 (the one-token row is not
+  // exact here: the tile's reference max is the product s * scale rounded once,
+  // so the single weight is 2^(rounding error), not exactly 1).
+  const int nq = 5, total_q = 2 * nq + 1;
+  std::vector<__half> qp = random_rows(g, total_q);
+  std::memcpy(qp.data() + (nq - 1) * row, qh.data(), row * sizeof(__half));
+  std::memcpy(qp.data() + nq * row, qp.data(), nq * row * sizeof(__half));
+  std::memcpy(qp.data() + 2 * nq * row, qh.data() + 2 * row, row * sizeof(__half));
+  const int32_t qstart[4] = {0, nq, 2 * nq, total_q};
+  __half* qp_d = nullptr;
+  int32_t* qstart_d = nullptr;
+  float* outp = nullptr;
+  CUDA(cudaMalloc(&qp_d, qp.size() * sizeof(__half)));
+  CUDA(cudaMalloc(&qstart_d, sizeof(qstart)));
+  CUDA(cudaMalloc(&outp, static_cast<size_t>(total_q) * row * sizeof(float)));
+  CUDA(cudaMemcpy(qp_d, qp.data(), qp.size() * sizeof(__half), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(qstart_d, qstart, sizeof(qstart), cudaMemcpyHostToDevice));
+  CHECK(paged_attn_prefill(qp_d, qstart_d, total_q, nq, kc, vc, tables_d, lens_d, 3, kHeads, kDim,
+                           kBlock, kMaxBlocks, kBlocks, 1.0f / 11.3137085f, PA_F16, outp, PA_F32,
+                           rec, nullptr));
+  CUDA(cudaDeviceSynchronize());
+  CHECK(pa_error_read(rec, err, nullptr));
+  if (err[0] != 0) {
+    std::fprintf(stderr, "device error record (prefill): %d %d %d %d\n", err[0], err[1], err[2],
+                 err[3]);
+    return 1;
+  }
+  std::vector<float> op(static_cast<size_t>(total_q) * row);
+  CUDA(cudaMemcpy(op.data(), outp, op.size() * sizeof(float), cudaMemcpyDeviceToHost));
+  if (std::memcmp(op.data(), op.data() + nq * row, nq * row * sizeof(float)) != 0) {
+    std::fprintf(stderr, "prefill: fork differs from its parent\n");
+    return 1;
+  }
+  float worst_p = 0.f;
+  for (size_t i = 0; i < row; ++i) {
+    worst_p = std::max(worst_p, std::fabs(op[(nq - 1) * row + i] - o[i]));
+    worst_p = std::max(worst_p, std::fabs(op[2 * nq * row + i] - o[2 * row + i]));
+  }
+  if (!(worst_p <= 2e-3f)) {
+    std::fprintf(stderr, "prefill: differs from the decode by %g\n", worst_p);
+    return 1;
+  }
+
   CHECK(pa_alloc_check(alloc));
   pa_alloc_destroy(alloc);
   for (void* p : {static_cast<void*>(kc), static_cast<void*>(vc), static_cast<void*>(k),
@@ -249,10 +300,13 @@ int main() {
                   static_cast<void*>(pair_d), static_cast<void*>(tables_d),
                   static_cast<void*>(lens_d), static_cast<void*>(out), static_cast<void*>(rec),
                   static_cast<void*>(items_d), workspace, static_cast<void*>(items2_d),
-                  static_cast<void*>(recs_d), workspace2, static_cast<void*>(out2)})
+                  static_cast<void*>(recs_d), workspace2, static_cast<void*>(out2),
+                  static_cast<void*>(qp_d), static_cast<void*>(qstart_d),
+                  static_cast<void*>(outp)})
     if (p) cudaFree(p);
   std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact; "
               "%d-token partitions, %d work items; shared blocks read once: %d records, fork "
-              "still exact, max change %.2e\n", pt, n_items, n_recs, worst);
+              "still exact, max change %.2e; prefill: fork exact, within %.2e of the decode\n",
+              pt, n_items, n_recs, worst, worst_p);
   return 0;
 }

@@ -1,6 +1,6 @@
 """The C-ABI example (paged_kv_cache_317_gb300/examples/c_abi_step.cu) builds
 against include/pagedkv.h and libpagedkv.so alone, and on a GPU runs a decode step
-whose exact self-checks pass."""
+whose exact self-checks pass (decode, shared-partition decode and chunked prefill)."""
 
 import os
 import shutil
@@ -37,3 +37,4 @@ def test_c_example_runs(lib, tmp_path):
     assert "ok:" in r.stdout
     assert "64-token partitions" in r.stdout        # the split path with a work list
     assert "2 records" in r.stdout                  # the shared-partition pass ran
+    assert "prefill: fork exact" in r.stdout        # the tensor-core prefill ran
