@@ -54,9 +54,12 @@ def test_prefill_small_cases(B, dtype, bs):
     assert_matches_oracle(out, _oracle(b, q, starts), f"prefill {dtype} bs{bs}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
-def test_prefill_half_outputs(B, out_dtype):
-    b, q, starts = _case(50, [200, 90], [130, 90], 4, 16, "bf16")
+def test_prefill_half_outputs(B, out_dtype, D):
+    """16-bit outputs leave through the staging buffer as 32 columns per 64-byte
+    piece (fp32 ones as 16): every head_dim's column count."""
+    b, q, starts = _case(50, [200, 90], [130, 90], 4, 16, "bf16", D=D)
     assert_matches_oracle(_run(B, b, q, starts, out_dtype=out_dtype), _oracle(b, q, starts))
 
 
