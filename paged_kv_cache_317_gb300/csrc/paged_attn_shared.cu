@@ -157,7 +157,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* rec = p.records + static_cast<size_t>(blockIdx.y) * kRecord;
 
-  // Check the record (every thread reaches the same verdict): partition in
+  // Check the record (every thread reaches the same conclusion): partition in
   // range, 1..8 members, each a valid sequence whose length covers the whole
   // partition (and, with a fused append, the appended token lies past it).
   const int part = __ldg(rec);
