@@ -895,6 +895,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         host_s, stage_s, plan_s, lens_seen, n_shared = 0.0, 0.0, 0.0, 0, 0
+        unique_seen = 0
         # per step: events before the upload, before the copies, before decode, after
         # (created before the loop: creating events costs host time every step)
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -915,6 +916,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
+            unique_seen += alloc.stats()["slots_filled"]   # tokens stored once
             q, k, v = tokens_all[s_]
             h2 = time.perf_counter()
             if args.no_share:
@@ -959,6 +961,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         tokens = lens_seen / plan.steps
         total = tokens * plan.num_heads * plan.head_dim * 4
         value = total / (ms * 1e-3) / 1e9
+        unique_kv = unique_seen / plan.steps * plan.num_heads * plan.head_dim * 4
         line.update(config={"workload": "mixed serving: 512 seqs, 70% U[32,256] / 30% "
                                         "U[1024,4096], 26 forks/step, fused append+decode",
                             "steps_run": plan.steps, "partition_tokens": pt,
@@ -969,6 +972,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
                     host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
+                    unique_kv_bytes=round(unique_kv),
+                    unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
+                    unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     device_ms_per_step_split={
                         "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
@@ -1014,6 +1020,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
+        unique_seen = 0
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                  for _ in range(plan.steps)]
         t0 = time.perf_counter()
@@ -1032,6 +1039,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
             tables, lens = alloc.batch_block_tables(ids, max_blocks)
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
+            unique_seen += alloc.stats()["slots_filled"]   # tokens stored once
             copies += len(pairs)
             q, k, v = tokens_all[s_]
             h2 = time.perf_counter()
@@ -1077,6 +1085,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         tokens = lens_seen / plan.steps
         total = tokens * H * D * 4
         value = total / (ms * 1e-3) / 1e9
+        unique_kv = unique_seen / plan.steps * H * D * 4
         alloc.batch_free(beams.ravel())
         if alloc.num_free() != plan.num_blocks:
             raise RuntimeError("beam workload leaked blocks")
@@ -1090,6 +1099,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
                     host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
+                    unique_kv_bytes=round(unique_kv),
+                    unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
+                    unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     copies_per_step=round(copies / plan.steps, 2),
                     device_ms_per_step_split={
