@@ -186,6 +186,15 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  holds tokens must appear exactly once across both.  At most
  *                  65535 records.
  *                  pa_decode_share_plan builds both lists.
+ *   early_inputs   0, or nonzero to promise that the kernel preceding the call on
+ *                  the stream writes none of the call's read-only inputs (q, new_k,
+ *                  new_v, block_tables, seq_lens, seq_order, work_items,
+ *                  shared_records): they were written by copies, or by kernels that
+ *                  completed before that kernel began.  The call's first kernel,
+ *                  which is placed while the preceding kernel runs, may then read
+ *                  them (its work item, length, block-table entries and query)
+ *                  before that kernel has completed; the caches, the workspace and
+ *                  `out` are still touched only after it.  Results are identical.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -203,6 +212,7 @@ typedef struct pa_decode_opts {
   int num_work_items;
   const int32_t* shared_records;
   int num_shared;
+  int early_inputs;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,

@@ -39,14 +39,15 @@ class pa_prefill_opts(ctypes.Structure):
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
                 ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int),
-                ("shared_records", c_void_p), ("num_shared", c_int)]
+                ("shared_records", c_void_p), ("num_shared", c_int), ("early_inputs", c_int)]
 
 
 PA_SHARE_MAX_MEMBERS = 8
 PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
 
 
-def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_records=None):
+def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_records=None,
+                 early_inputs=False):
     if seq_order is not None:
         _need(seq_order, "seq_order", torch.int32)
     if work_items is not None:
@@ -63,7 +64,8 @@ def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_re
                           items_ptr,
                           0 if work_items is None else int(work_items.numel()),
                           None if shared_records is None else shared_records.data_ptr(),
-                          0 if shared_records is None else int(shared_records.shape[0]))
+                          0 if shared_records is None else int(shared_records.shape[0]),
+                          int(bool(early_inputs)))
 
 
 def _host_int32(values, name: str) -> "np.ndarray":
@@ -294,12 +296,13 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       stages: int = 0, phases: int = 0, seq_order: Optional[torch.Tensor] = None,
                       work_items: Optional[torch.Tensor] = None,
                       shared_records: Optional[torch.Tensor] = None,
-                      stream=None) -> torch.Tensor:
+                      early_inputs: bool = False, stream=None) -> torch.Tensor:
     """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
     seq_order: optional int32 [N] scheduling permutation on the device; work_items:
     optional int32 list of (sequence * P + partition) on the device; shared_records:
     optional int32 [r, PA_SHARE_RECORD_WORDS] shared partitions on the device
-    (share_plan builds both)."""
+    (share_plan builds both); early_inputs: the kernel before the call on the stream
+    writes none of the read-only inputs (pa_decode_opts.early_inputs)."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -315,7 +318,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records)
+                        shared_records, early_inputs)
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -334,7 +337,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              seq_order: Optional[torch.Tensor] = None,
                              work_items: Optional[torch.Tensor] = None,
                              shared_records: Optional[torch.Tensor] = None,
-                             stream=None) -> torch.Tensor:
+                             early_inputs: bool = False, stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
     N, H, D = q.shape
@@ -353,7 +356,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records)
+                        shared_records, early_inputs)
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),

@@ -76,6 +76,7 @@ struct DecodeParams {
   int out_dtype;
   float qscale;        // scale * log2(e): scores come out in log2 units
   int wait_first;      // this pass is the call's first kernel (no shared pass before it)
+  int early_inputs;    // the read-only inputs may be read before that wait
 };
 
 // Reduce each of N = TPR/2 partial dot products over the TPR lanes of a row
@@ -138,8 +139,13 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   // ends.  Nothing in memory is touched before that kernel has completed and
   // its writes are visible.  Behind the shared-partition pass the wait stays at
   // the end instead (that pass waited for the predecessor before it let this
-  // one start).
-  if (p.wait_first) wait_prerequisite();
+  // one start).  With early_inputs the caller promises that the predecessor
+  // writes none of the read-only inputs: the work item, length, block-table
+  // entries and query are then read first, and the wait comes just before the
+  // caches, the workspace or `out` are touched (in the producer before its first
+  // copy, in each consumer warp before its first chunk).
+  const bool early = p.wait_first && p.early_inputs;
+  if (p.wait_first && !early) wait_prerequisite();
   const int G = p.heads_per_cta;
   const int S = p.stages;
   const int hg = blockIdx.x;
@@ -219,6 +225,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
           }
         }
       }
+      if (early && c0 == 0) wait_prerequisite();
       const int n = min(per_round, nchunks - c0);
       for (int j = 0; j < n; ++j) {
         const int b = __shfl_sync(kFullMask, blk, j * sub);
@@ -294,6 +301,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
 #pragma unroll
       for (int j = 0; j < 8; ++j) qf[j] *= p.qscale;
     }
+    if (early) wait_prerequisite();
     float m = -INFINITY, lsum = 0.f;
     float acc[8];
 #pragma unroll

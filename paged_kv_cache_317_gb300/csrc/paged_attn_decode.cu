@@ -267,6 +267,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   DecodeParams p{};
   p.q = q;
   p.seq_order = opts ? opts->seq_order : nullptr;
+  p.early_inputs = (opts && opts->early_inputs) ? 1 : 0;
   p.work_items = opts ? opts->work_items : nullptr;
   p.num_work_items = p.work_items ? opts->num_work_items : 0;
   if (p.work_items && (p.num_work_items < 0 || p.num_work_items > 65535))

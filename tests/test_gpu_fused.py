@@ -101,3 +101,55 @@ def test_bench_step_configuration(B):
     assert torch.equal(b.k_cache[blk, :, row, :].view(torch.int16), b.new_k.view(torch.int16))
     assert torch.equal(b.v_cache[blk, :, row, :].view(torch.int16), b.new_v.view(torch.int16))
     assert_matches_oracle(out, ref, "bench step, all 256 sequences")
+
+
+def test_early_inputs_changes_nothing_eager_and_in_a_graph(B):
+    """early_inputs lets the call's first kernel read its work item, length, table
+    entries and query before the preceding kernel has completed; the caches, the
+    shared workspace and `out` are still touched only after it.  Back-to-back calls
+    on three batches that share one workspace (each call's partition pass writes
+    the partials the previous call's merge reads), eagerly and replayed from a
+    CUDA graph, give the same bits as without it."""
+    batches = [random_decode_batch(900 + j, [1, 40, 300, 700, 1500 + 100 * j, 17], 8, 128, 16,
+                                   dtype="bf16", device="cuda", with_append=True, poison=False)
+               for j in range(3)]
+    pt = 64
+    ws = torch.empty(max(B.paged_attn_workspace_size(6, 8, 128, 16, b.max_blocks_per_seq, pt)
+                         for b in batches), dtype=torch.uint8, device="cuda")
+    tabs = [device_tables(b) for b in batches]
+    items = [torch.from_numpy(B.partition_work_items(b.context_lens, pt, b.max_blocks_per_seq,
+                                                     16)).cuda() for b in batches]
+
+    def run(early, graph):
+        caches = [(b.k_cache.clone(), b.v_cache.clone()) for b in batches]
+        outs = [torch.empty(b.q.shape, dtype=torch.float32, device="cuda") for b in batches]
+
+        def step():
+            for _ in range(4):
+                for b, (kc, vc), (bt, sl), it, o in zip(batches, caches, tabs, items, outs):
+                    B.paged_attn_decode_append(b.q, b.new_k, b.new_v, kc, vc, bt, sl, b.scale,
+                                               out=o, partition_tokens=pt, workspace=ws,
+                                               work_items=it, early_inputs=early)
+        if graph:
+            step()                                   # warm-up outside the capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            for _ in range(3):
+                g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        return outs, caches
+
+    ref_outs, ref_caches = run(False, False)
+    for early, graph in ((True, False), (True, True), (False, True)):
+        outs, caches = run(early, graph)
+        for o, r in zip(outs, ref_outs):
+            assert torch.equal(o, r), (early, graph)
+        for (k, v), (rk, rv) in zip(caches, ref_caches):
+            assert torch.equal(k.view(torch.int16), rk.view(torch.int16))
+            assert torch.equal(v.view(torch.int16), rv.view(torch.int16))
+    for b, o in zip(batches, ref_outs):
+        assert_matches_oracle(o, oracle_decode(b), "early-input chain")
