@@ -539,7 +539,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_hbm_peak()
     achieved = nbytes["decode_partition"] / (part_ms * 1e-3) / 1e9
 
-    # the other seeded workloads (sampling, long context, mixed serving, ...), timed after the headline
+    # the other seeded workloads (sampling, long context, serving, ...), after the headline
     others = None
     if rank == 0 and world == 1 and not args.no_workloads:
         others = workload_summaries(args, rank, world, local_rank)
