@@ -647,46 +647,58 @@ def _time_graph(fns, K, W, stream, calls_per_graph=32):
 class _Staging:
     """Per-step host inputs of a serving loop in one pinned int32 buffer per set
     (copy-on-write pairs as int64, block tables, lengths, work list,
-    shared-partition records) and one device buffer, uploaded with one copy.
-    Two sets alternate; a set is refilled once the copy that read it is done."""
+    shared-partition records, tail starts) and one device buffer, uploaded with
+    one copy.  The allocator and the planner write their outputs straight into a
+    set's regions (views); two sets alternate, and a set is refilled once the copy
+    that read it is done."""
 
     def __init__(self, n_seqs, max_blocks, n_items_max, record_words, dev):
         import torch
         self.sizes = {"pairs": 4 * n_seqs, "bt": n_seqs * max_blocks, "sl": n_seqs,
-                      "it": n_items_max, "rc": n_items_max * record_words}
+                      "ts": n_seqs, "it": n_items_max, "rc": n_items_max * record_words}
         self.off, at = {}, 0
         for k, n in self.sizes.items():
             self.off[k] = at
             at += n + (-n) % 4           # keep every region 16-byte aligned
         self.n_seqs, self.max_blocks, self.rw = n_seqs, max_blocks, record_words
         self.host = [torch.empty(at, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.host_np = [h.numpy() for h in self.host]
         self.dev = [torch.empty(at, dtype=torch.int32, device=dev) for _ in range(2)]
         self.done = [torch.cuda.Event() for _ in range(2)]
 
-    def upload(self, step, stream, pairs, tables, lens, items, recs):
-        """Fill set step % 2 and enqueue its upload; returns device views
-        (pairs int64 [n, 2], tables, lengths, work list, records)."""
+    def views(self, step):
+        """Wait until set step % 2 may be refilled (the copy that read it two steps
+        back is done); returns its host regions: tables [n, max_blocks], lengths,
+        work list, records [cap, record words], tail starts."""
+        j = step % 2
+        self.done[j].synchronize()
+        h, o, n = self.host_np[j], self.off, self.n_seqs
+        return (h[o["bt"]:o["bt"] + n * self.max_blocks].reshape(n, self.max_blocks),
+                h[o["sl"]:o["sl"] + n], h[o["it"]:o["it"] + self.sizes["it"]],
+                h[o["rc"]:o["rc"] + self.sizes["rc"]].reshape(-1, self.rw),
+                h[o["ts"]:o["ts"] + n])
+
+    def upload(self, step, stream, pairs, n_items, n_recs, tails):
+        """Write the pairs into set step % 2 (its other regions filled through
+        views(step)) and enqueue its upload; returns device views (pairs int64
+        [n, 2], tables, lengths, work list, records, tail starts or None)."""
         import numpy as np
         import torch
         j = step % 2
-        self.done[j].synchronize()               # the copy that read this set two steps back
-        h, o = self.host[j].numpy(), self.off
-        n_p, n_i, n_r = len(pairs), len(items), len(recs)
+        h, o, n_p = self.host_np[j], self.off, len(pairs)
         if n_p:
             h[o["pairs"]:o["pairs"] + 4 * n_p].view(np.int64)[:] = pairs.ravel()
-        h[o["bt"]:o["bt"] + tables.size] = tables.ravel()
-        h[o["sl"]:o["sl"] + len(lens)] = lens
-        h[o["it"]:o["it"] + n_i] = items
-        h[o["rc"]:o["rc"] + n_r * self.rw] = recs.ravel()
-        used = o["rc"] + n_r * self.rw
+        used = o["rc"] + n_recs * self.rw
         d = self.dev[j]
         d[:used].copy_(self.host[j][:used], non_blocking=True)
         self.done[j].record(stream)
         return (d[o["pairs"]:o["pairs"] + 4 * n_p].view(torch.int64).view(n_p, 2),
-                d[o["bt"]:o["bt"] + tables.size].view(self.n_seqs, self.max_blocks),
-                d[o["sl"]:o["sl"] + len(lens)],
-                d[o["it"]:o["it"] + n_i],
-                d[o["rc"]:o["rc"] + n_r * self.rw].view(n_r, self.rw) if n_r else None)
+                d[o["bt"]:o["bt"] + self.n_seqs * self.max_blocks].view(self.n_seqs,
+                                                                      self.max_blocks),
+                d[o["sl"]:o["sl"] + self.n_seqs],
+                d[o["it"]:o["it"] + n_items],
+                d[o["rc"]:o["rc"] + n_recs * self.rw].view(n_recs, self.rw) if n_recs else None,
+                d[o["ts"]:o["ts"] + self.n_seqs] if tails else None)
 
 
 def run_workload(args, rank, world, local_rank, emit=True):
@@ -886,20 +898,21 @@ def run_workload(args, rank, world, local_rank, emit=True):
             slots0.append(alloc.slots(i, 0, e - a))
         B.kv_cache_append(plan.init_k, plan.init_v, torch.from_numpy(np.concatenate(slots0)).to(dev),
                           kc, vc)
-        ids, next_id = list(range(N)), N
+        ids, next_id = np.arange(N, dtype=np.int64), N     # slot -> live sequence id
         max_blocks = int(-(-(plan.init_lens.max() + plan.steps) // bs))
         tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
         out = torch.empty((N, plan.num_heads, plan.head_dim), dtype=plan.dtype, device=dev)
         pt = args.serving_partition or 512
+        prefix = not (args.no_share or args.no_prefix)
         ws = torch.empty(B.paged_attn_workspace_size(N, plan.num_heads, plan.head_dim, bs,
-                                                     max_blocks, pt), dtype=torch.uint8,
-                         device=dev)
+                                                     max_blocks, pt, tails=prefix),
+                         dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
         # per-step host inputs staged in one pinned buffer per set, one upload per step
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
-        host_s, stage_s, plan_s, lens_seen, n_shared = 0.0, 0.0, 0.0, 0, 0
+        host_s, stage_s, plan_s, lens_seen, n_shared, n_prefix = 0.0, 0.0, 0.0, 0, 0, 0
         unique_seen = 0
         # per step: events before the upload, before the copies, before decode, after
         # (created before the loop: creating events costs host time every step)
@@ -911,32 +924,45 @@ def run_workload(args, rank, world, local_rank, emit=True):
         for s_ in range(plan.steps):
             h0 = time.perf_counter()
             fp = plan.fork_pairs[s_]
-            if len(fp):
-                alloc.batch_free([ids[b_] for _, b_ in fp])
-                alloc.batch_fork([ids[a_] for a_, _ in fp], range(next_id, next_id + len(fp)))
-                for a_, b_ in fp:
-                    ids[b_] = next_id
-                    next_id += 1
+            if len(fp):   # slot b ends and continues as a fork of slot a (all distinct)
+                born = np.arange(next_id, next_id + len(fp), dtype=np.int64)
+                alloc.batch_free(ids[fp[:, 1]])
+                alloc.batch_fork(ids[fp[:, 0]], born)
+                ids[fp[:, 1]] = born
+                next_id += len(fp)
             slots, pairs = alloc.batch_append(ids)
-            tables, lens = alloc.batch_block_tables(ids, max_blocks)
+            host_s += time.perf_counter() - h0
+            h1 = time.perf_counter()
+            bt_h, sl_h, it_h, rc_h, ts_h = staging.views(s_)
+            stage_s += time.perf_counter() - h1
+            h0 = time.perf_counter()
+            tables, lens = alloc.batch_block_tables(ids, max_blocks, out=(bt_h, sl_h))
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
             if s_ % 10 == 0:   # tokens stored once (sampled: the call walks the pool)
                 unique_seen += alloc.stats()["slots_filled"]
             q, k, v = tokens_all[s_]
             h2 = time.perf_counter()
+            tails = None
             if args.no_share:
                 items = B.partition_work_items(lens, pt, max_blocks, plan.block_size)
-                recs = np.empty((0, RW), dtype=np.int32)
+                it_h[:len(items)] = items
+                recs = rc_h[:0]
+            elif prefix:   # and the first chunks they share of the partition they diverge in
+                items, recs, tails = B.share_plan_prefix(tables, lens, pt, plan.block_size,
+                                                         fused_append=True,
+                                                         out=(it_h, rc_h, ts_h))
             else:   # partitions that forked sequences still share are read once
-                items, recs = B.share_plan(tables, lens, pt, plan.block_size, fused_append=True)
+                items, recs = B.share_plan(tables, lens, pt, plan.block_size, fused_append=True,
+                                           out=(it_h, rc_h))
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
+            n_prefix += int((recs[:, 1] >> 8 > 0).sum())
             evs = split[s_]
             evs[0].record(stream)
             h1 = time.perf_counter()
-            pairs_d, bt_d, sl_d, it_d, rc_d = staging.upload(s_, stream, pairs, tables, lens,
-                                                             items, recs)
+            pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
+                s_, stream, pairs, len(items), len(recs), tails is not None)
             stage_s += time.perf_counter() - h1
             evs[1].record(stream)
             if len(pairs):
@@ -944,7 +970,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
             evs[2].record(stream)
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=it_d, shared_records=rc_d)
+                                       work_items=it_d, shared_records=rc_d, tail_start=ts_d)
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
@@ -959,7 +985,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
                                    partition_tokens=pt, workspace=ws, error_record=rec,
                                    work_items=torch.from_numpy(items).to(dev),
                                    shared_records=(torch.from_numpy(recs).to(dev)
-                                                   if len(recs) else None))
+                                                   if len(recs) else None),
+                                   tail_start=(torch.from_numpy(tails).to(dev)
+                                               if tails is not None else None))
         torch.cuda.synchronize()
         if not torch.equal(ref_out, out):
             raise RuntimeError("staged and direct inputs gave different outputs")
@@ -974,7 +1002,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
                             "steps_run": plan.steps, "partition_tokens": pt,
                             "schedule": ("work list only" if args.no_share else
                                          f"shared partitions ({n_shared / plan.steps:.1f} "
-                                         "records per step) + work list"),
+                                         f"records per step, {n_prefix / plan.steps:.1f} "
+                                         "of them prefix records) + work list"),
                             "l2": "inputs larger than L2"},
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
@@ -1020,13 +1049,15 @@ def run_workload(args, rank, world, local_rank, emit=True):
         tokens_all = [plan.step_tokens(s_) for s_ in range(plan.steps)]
         out = torch.empty((N, H, D), dtype=plan.dtype, device=dev)
         pt = args.serving_partition or 512
-        ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, max_blocks, pt),
+        prefix = not (args.no_share or args.no_prefix)
+        ws = torch.empty(B.paged_attn_workspace_size(N, H, D, bs, max_blocks, pt, tails=prefix),
                          dtype=torch.uint8, device=dev)
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
+        n_prefix = 0
         unique_seen = 0
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                  for _ in range(plan.steps)]
@@ -1043,7 +1074,12 @@ def run_workload(args, rank, world, local_rank, emit=True):
             beams = children.reshape(G_, Wd)
             ids = children
             slots, pairs = alloc.batch_append(ids)
-            tables, lens = alloc.batch_block_tables(ids, max_blocks)
+            host_s += time.perf_counter() - h0
+            h1 = time.perf_counter()
+            bt_h, sl_h, it_h, rc_h, ts_h = staging.views(s_)
+            stage_s += time.perf_counter() - h1
+            h0 = time.perf_counter()
+            tables, lens = alloc.batch_block_tables(ids, max_blocks, out=(bt_h, sl_h))
             host_s += time.perf_counter() - h0
             lens_seen += int(lens.sum())
             if s_ % 10 == 0:   # tokens stored once (sampled: the call walks the pool)
@@ -1051,18 +1087,25 @@ def run_workload(args, rank, world, local_rank, emit=True):
             copies += len(pairs)
             q, k, v = tokens_all[s_]
             h2 = time.perf_counter()
+            tails = None
             if args.no_share:
                 items = B.partition_work_items(lens, pt, max_blocks, bs)
-                recs = np.empty((0, RW), dtype=np.int32)
+                it_h[:len(items)] = items
+                recs = rc_h[:0]
+            elif prefix:   # and the first chunks they share of the partition they diverge in
+                items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=True,
+                                                         out=(it_h, rc_h, ts_h))
             else:   # the partitions a group's beams share are read once for the group
-                items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
+                items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True,
+                                           out=(it_h, rc_h))
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
+            n_prefix += int((recs[:, 1] >> 8 > 0).sum())
             evs = split[s_]
             evs[0].record(stream)
             h1 = time.perf_counter()
-            pairs_d, bt_d, sl_d, it_d, rc_d = staging.upload(s_, stream, pairs, tables, lens,
-                                                             items, recs)
+            pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
+                s_, stream, pairs, len(items), len(recs), tails is not None)
             stage_s += time.perf_counter() - h1
             evs[1].record(stream)
             if len(pairs):
@@ -1070,7 +1113,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
             evs[2].record(stream)
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=it_d, shared_records=rc_d)
+                                       work_items=it_d, shared_records=rc_d, tail_start=ts_d)
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
@@ -1085,7 +1128,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
                                    partition_tokens=pt, workspace=ws, error_record=rec,
                                    work_items=torch.from_numpy(items).to(dev),
                                    shared_records=(torch.from_numpy(recs).to(dev)
-                                                   if len(recs) else None))
+                                                   if len(recs) else None),
+                                   tail_start=(torch.from_numpy(tails).to(dev)
+                                               if tails is not None else None))
         torch.cuda.synchronize()
         if not torch.equal(ref_out, out):
             raise RuntimeError("staged and direct inputs gave different outputs")
@@ -1102,7 +1147,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
                             "steps_run": plan.steps, "partition_tokens": pt,
                             "schedule": ("work list only" if args.no_share else
                                          f"shared partitions ({n_shared / plan.steps:.1f} "
-                                         "records per step) + work list"),
+                                         f"records per step, {n_prefix / plan.steps:.1f} "
+                                         "of them prefix records) + work list"),
                             "l2": "inputs larger than L2"},
                     dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
@@ -1470,6 +1516,9 @@ def main(argv=None):
     ap.add_argument("--no-share", action="store_true",
                     help="sampling/beam/mixed: read shared partitions once per sequence "
                          "instead of once per group")
+    ap.add_argument("--no-prefix", action="store_true",
+                    help="beam/mixed: share whole partitions only, not the shared first "
+                         "chunks of a partition the group's members diverge in")
     ap.add_argument("--serving-partition", type=int, default=0,
                     help="sampling/beam/mixed: split-K partition length (0: the host rule "
                          "for sampling, 512 for beam and mixed)")

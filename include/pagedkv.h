@@ -138,6 +138,11 @@ int pa_selftest_bounded_wait(int32_t* error_record, int arrive, unsigned long lo
 /* Bytes of workspace paged_attn_decode needs for these sizes (0 if none). */
 size_t paged_attn_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size,
                                  int max_blocks_per_seq, int partition_tokens);
+/* The same with pa_decode_opts.tail_start given: max(P, 1) partial rows per
+ * (sequence, head) plus one tail row each (never 0). */
+size_t paged_attn_workspace_size_tails(int num_seqs, int num_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq,
+                                       int partition_tokens);
 
 int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
@@ -168,17 +173,22 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  (index = position, value = item) and skipped.  At most 65535.
  *   shared_records NULL, or device int32 [num_shared][PA_SHARE_RECORD_WORDS]:
  *                  partitions that several sequences share [P3d].  Record r =
- *                  {p, m, s_0, ..., s_{m-1}, unused...}: partition p of the m
+ *                  {p, m + 256 c, s_0, ..., s_{m-1}, unused...}: partition p of the m
  *                  (1..PA_SHARE_MAX_MEMBERS) member sequences s_j, whose block
- *                  tables name the same physical blocks over that partition.  One
+ *                  tables name the same physical blocks over that partition (c = 0),
+ *                  or over its first c 16-token chunks only (c > 0, a "prefix
+ *                  record", with tail_start below: the rest of the partition is
+ *                  each member's own work item).  One
  *                  thread block per (record, head pair) reads each K/V chunk once
  *                  for all members' queries (mma.sync, P as high + low half-
  *                  precision parts, fp32 accumulation) and writes every member's
  *                  partial for partition p, or its output row when p is its only
- *                  partition.  Blocks are looked up in s_0's table only.  Each
- *                  member must cover the whole partition: (p + 1) *
+ *                  partition (c = 0).  Blocks are looked up in s_0's table only.
+ *                  With c = 0 each member must cover the whole partition: (p + 1) *
  *                  partition_tokens <= L (<= L - 1 for paged_attn_decode_append,
- *                  whose appended token must lie past it).  A record that breaks
+ *                  whose appended token must lie past it); with c > 0, c <
+ *                  partition_tokens / 16 and tail_start[s_j] = p * partition_tokens
+ *                  + 16 c < L for every member.  A record that breaks
  *                  these rules is recorded as PA_ERR_BAD_SEQ_LEN (index = record,
  *                  value = the offending field) and skipped.  Requires work_items
  *                  (the pairs not covered by a record; when there are none, any
@@ -195,6 +205,16 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  them (its work item, length, block-table entries and query)
  *                  before that kernel has completed; the caches, the workspace and
  *                  `out` are still touched only after it.  Results are identical.
+ *   tail_start     NULL, or device int32 [num_seqs]: -1, or for a sequence whose
+ *                  partition p is split by a prefix record (see shared_records),
+ *                  the token t = p * partition_tokens + 16 c where its own part of
+ *                  that partition begins (a multiple of 16 below L).  Its work
+ *                  item (i, p) then covers tokens t .. min(L, (p + 1) *
+ *                  partition_tokens) - 1 and leaves its partial in a tail row of
+ *                  the workspace, which the merge adds to the sequence's others.
+ *                  The workspace must then hold paged_attn_workspace_size_tails
+ *                  bytes.  pa_decode_share_plan_ex builds the records and this
+ *                  array together.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -202,7 +222,9 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *   float2 ml[row] after all acc rows:   (m, l) with u_t = s_t * log2(e),
  *                                        m = max_t u_t, l = sum_t 2^(u_t - m)
  * over the tokens t of that partition.  Partitions at or past
- * ceil(L / partition_tokens) are not written. */
+ * ceil(L / partition_tokens) are not written.  With tail_start, max(P, 1) rows
+ * per (sequence, head) and then, after the ml rows, tail rows (i * num_heads + h):
+ * float acc_tail[num_seqs * num_heads][head_dim], float2 ml_tail[...]. */
 typedef struct pa_decode_opts {
   int heads_per_cta;
   int stages;
@@ -213,6 +235,7 @@ typedef struct pa_decode_opts {
   const int32_t* shared_records;
   int num_shared;
   int early_inputs;
+  const int32_t* tail_start;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -318,6 +341,28 @@ int pa_decode_share_plan(const int32_t* block_tables, const int32_t* seq_lens, i
                          int fused_append, const int32_t* order, int32_t* work_items,
                          int32_t items_capacity, int32_t* num_items, int32_t* records,
                          int32_t records_capacity, int32_t* num_records);
+
+/* pa_decode_share_plan_ex: the same, and (prefixes nonzero) prefix records for
+ * the partitions a group shares only in part, typically where forked samples or
+ * beams diverge.  After the whole-partition records, partition by partition, the
+ * sequences whose pair (i, p) is still in the work list, that no earlier prefix
+ * record took, and that hold at least 17 tokens of p are grouped by the first
+ * block of p; within a group, c = the largest number of leading 16-token chunks
+ * of p whose blocks all members' tables name alike, and whose tokens lie below
+ * L_i - 1 for every member (the last token stays in the member's own part).  A
+ * group of two or more (PA_SHARE_MAX_MEMBERS at most per record, members in
+ * index order) with c >= 1 becomes a record {p, m + 256 c, members}, and
+ * tail_start[s] = p * partition_tokens + 16 c for each member; the pair (s, p)
+ * stays in the work list for the rest.  c is also below partition_tokens / 16.
+ * Every other tail_start entry is -1.
+ *   tail_start     host int32 [num_seqs] (written only when prefixes is nonzero
+ *                  and the arrays are given; may be NULL otherwise) */
+int pa_decode_share_plan_ex(const int32_t* block_tables, const int32_t* seq_lens,
+                            int num_seqs, int max_blocks_per_seq, int block_size,
+                            int partition_tokens, int fused_append, const int32_t* order,
+                            int prefixes, int32_t* work_items, int32_t items_capacity,
+                            int32_t* num_items, int32_t* records, int32_t records_capacity,
+                            int32_t* num_records, int32_t* tail_start);
 
 /* Chunked prefill / multi-query attention through the block table  [P1], [P3c]
  *

@@ -39,7 +39,8 @@ class pa_prefill_opts(ctypes.Structure):
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
                 ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int),
-                ("shared_records", c_void_p), ("num_shared", c_int), ("early_inputs", c_int)]
+                ("shared_records", c_void_p), ("num_shared", c_int), ("early_inputs", c_int),
+                ("tail_start", c_void_p)]
 
 
 PA_SHARE_MAX_MEMBERS = 8
@@ -47,11 +48,13 @@ PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
 
 
 def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_records=None,
-                 early_inputs=False):
+                 early_inputs=False, tail_start=None):
     if seq_order is not None:
         _need(seq_order, "seq_order", torch.int32)
     if work_items is not None:
         _need(work_items, "work_items", torch.int32)
+    if tail_start is not None:
+        _need(tail_start, "tail_start", torch.int32)
     if shared_records is not None:
         _need(shared_records, "shared_records", torch.int32)
         if shared_records.dim() != 2 or shared_records.shape[1] != PA_SHARE_RECORD_WORDS:
@@ -65,7 +68,8 @@ def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_re
                           0 if work_items is None else int(work_items.numel()),
                           None if shared_records is None else shared_records.data_ptr(),
                           0 if shared_records is None else int(shared_records.shape[0]),
-                          int(bool(early_inputs)))
+                          int(bool(early_inputs)),
+                          None if tail_start is None else tail_start.data_ptr())
 
 
 def _host_int32(values, name: str) -> "np.ndarray":
@@ -116,10 +120,37 @@ def partition_work_items(seq_lens, partition_tokens: int, max_blocks_per_seq: in
 
 
 def share_plan(block_tables, seq_lens, partition_tokens: int, block_size: int,
-               fused_append: bool = True, order=None):
+               fused_append: bool = True, order=None, out=None):
     """Work list and shared-partition records (pa_decode_share_plan) for a decode
     over host tables [N, max_blocks] and lengths: (work_items int32 [n],
-    shared_records int32 [r, PA_SHARE_RECORD_WORDS])."""
+    shared_records int32 [r, PA_SHARE_RECORD_WORDS]).  out: optional int32
+    buffers (items [cap], records [cap, PA_SHARE_RECORD_WORDS]) to fill in place
+    (a pinned staging buffer, say); the results are then views of them."""
+    return _share_plan(block_tables, seq_lens, partition_tokens, block_size, fused_append,
+                       order, False, None if out is None else (*out[:2], None))[:2]
+
+
+def share_plan_prefix(block_tables, seq_lens, partition_tokens: int, block_size: int,
+                      fused_append: bool = True, order=None, out=None):
+    """The same plan with prefix records (pa_decode_share_plan_ex): partitions a
+    group shares only in part are read once up to where the members diverge.
+    Returns (work_items, shared_records, tail_start int32 [N]); pass tail_start to
+    the decode with the other two.  out: optional (items, records, tail_start)
+    buffers to fill in place."""
+    return _share_plan(block_tables, seq_lens, partition_tokens, block_size, fused_append,
+                       order, True, out)
+
+
+def _out_buffer(buf, name, shape_tail=()):
+    import numpy as np
+    if (not isinstance(buf, np.ndarray) or buf.dtype != np.int32 or
+            not buf.flags.c_contiguous or buf.shape[1:] != tuple(shape_tail)):
+        raise ValueError(f"{name} must be a C-contiguous int32 array of shape [n, *{shape_tail}]")
+    return buf
+
+
+def _share_plan(block_tables, seq_lens, partition_tokens, block_size, fused_append, order,
+                prefixes, out=None):
     import numpy as np
     tables = np.ascontiguousarray(block_tables, dtype=np.int32)
     if tables.ndim != 2:
@@ -139,12 +170,23 @@ def share_plan(block_tables, seq_lens, partition_tokens: int, block_size: int,
     # one call with room for every (sequence, partition) pair; records hold >= 2 each
     pt = partition_tokens or 512
     pairs = len(lens) * max(1, -(-tables.shape[1] * block_size // pt)) if pt > 0 else 0
-    items = np.empty(pairs, dtype=np.int32)
-    recs = np.empty((pairs // 2, PA_SHARE_RECORD_WORDS), dtype=np.int32)
-    _check(lib.pa_decode_share_plan(*args, items.ctypes.data, len(items),
-                                    ctypes.byref(ni), recs.ctypes.data, len(recs),
-                                    ctypes.byref(nr)), "pa_decode_share_plan")
-    return items[: ni.value], recs[: nr.value]
+    if out is None:
+        items = np.empty(pairs, dtype=np.int32)
+        recs = np.empty((pairs // 2, PA_SHARE_RECORD_WORDS), dtype=np.int32)
+        tails = np.empty(len(lens), dtype=np.int32)
+    else:
+        items = _out_buffer(out[0], "items")
+        recs = _out_buffer(out[1], "records", (PA_SHARE_RECORD_WORDS,))
+        tails = out[2]
+        if tails is None:
+            tails = np.empty(len(lens), dtype=np.int32)
+        elif _out_buffer(tails, "tail_start").shape[0] != len(lens):
+            raise ValueError("tail_start must hold one entry per sequence")
+    _check(lib.pa_decode_share_plan_ex(*args, int(bool(prefixes)), items.ctypes.data,
+                                       len(items), ctypes.byref(ni), recs.ctypes.data,
+                                       len(recs), ctypes.byref(nr), tails.ctypes.data),
+           "pa_decode_share_plan_ex")
+    return items[: ni.value], recs[: nr.value], tails
 
 
 # name -> (restype, argtypes); mirrors include/pagedkv.h
@@ -155,6 +197,7 @@ SIGNATURES = {
     "pa_error_read": (c_int, [c_void_p, P_int32, c_void_p]),
     "pa_selftest_bounded_wait": (c_int, [c_void_p, c_int, ctypes.c_ulonglong, c_void_p]),
     "paged_attn_workspace_size": (c_size_t, [c_int] * 6),
+    "paged_attn_workspace_size_tails": (c_size_t, [c_int] * 6),
     "paged_attn_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                   c_int, c_int, c_int, c_int, c_float, c_int, c_void_p, c_int,
                                   c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
@@ -186,6 +229,9 @@ SIGNATURES = {
     "pa_decode_share_plan": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                      c_void_p, c_void_p, c_int32, P_int32, c_void_p, c_int32,
                                      P_int32]),
+    "pa_decode_share_plan_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                        c_void_p, c_int, c_void_p, c_int32, P_int32, c_void_p,
+                                        c_int32, P_int32, c_void_p]),
     "pa_alloc_create": (c_void_p, [c_int32, c_int32, P_int32]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_seq_add": (c_int, [c_void_p, c_int64, c_int32]),
@@ -283,9 +329,12 @@ def pa_selftest_bounded_wait(record: torch.Tensor, arrive: bool, limit_ns: int,
 
 # ----------------------------------------------------------------- decode
 def paged_attn_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
-                              partition_tokens=0) -> int:
-    return int(load_library().paged_attn_workspace_size(num_seqs, num_heads, head_dim, block_size,
-                                                        max_blocks_per_seq, partition_tokens))
+                              partition_tokens=0, tails: bool = False) -> int:
+    """Workspace bytes of a decode; tails=True: with tail_start (prefix records)."""
+    fn = (load_library().paged_attn_workspace_size_tails if tails
+          else load_library().paged_attn_workspace_size)
+    return int(fn(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq,
+                  partition_tokens))
 
 
 def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -296,13 +345,15 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       stages: int = 0, phases: int = 0, seq_order: Optional[torch.Tensor] = None,
                       work_items: Optional[torch.Tensor] = None,
                       shared_records: Optional[torch.Tensor] = None,
-                      early_inputs: bool = False, stream=None) -> torch.Tensor:
+                      early_inputs: bool = False, tail_start: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
     """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
     seq_order: optional int32 [N] scheduling permutation on the device; work_items:
     optional int32 list of (sequence * P + partition) on the device; shared_records:
     optional int32 [r, PA_SHARE_RECORD_WORDS] shared partitions on the device
     (share_plan builds both); early_inputs: the kernel before the call on the stream
-    writes none of the read-only inputs (pa_decode_opts.early_inputs)."""
+    writes none of the read-only inputs (pa_decode_opts.early_inputs); tail_start:
+    optional int32 [N] on the device, with prefix records (share_plan_prefix)."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -313,12 +364,14 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if out is None:
         out = torch.empty((N, H, D), dtype=out_dtype, device=q.device)
     _need(out, "out")
-    need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:   # (a given one is checked against the size by the call)
+        need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens,
+                                         tails=tail_start is not None)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records, early_inputs)
+                        shared_records, early_inputs, tail_start)
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -337,7 +390,9 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              seq_order: Optional[torch.Tensor] = None,
                              work_items: Optional[torch.Tensor] = None,
                              shared_records: Optional[torch.Tensor] = None,
-                             early_inputs: bool = False, stream=None) -> torch.Tensor:
+                             early_inputs: bool = False,
+                             tail_start: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
     N, H, D = q.shape
@@ -351,12 +406,14 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if out is None:
         out = torch.empty((N, H, D), dtype=out_dtype, device=q.device)
     _need(out, "out")
-    need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:   # (a given one is checked against the size by the call)
+        need = paged_attn_workspace_size(N, H, D, bs, MB, partition_tokens,
+                                         tails=tail_start is not None)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records, early_inputs)
+                        shared_records, early_inputs, tail_start)
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),
@@ -550,12 +607,21 @@ class BlockAllocator:
         _check(self._lib.pa_batch_free(self._h, ids.ctypes.data, ids.shape[0]),
                "pa_batch_free")
 
-    def batch_block_tables(self, seqs, max_blocks: int):
+    def batch_block_tables(self, seqs, max_blocks: int, out=None):
+        """Block tables [n, max_blocks] (-1 past each sequence's blocks) and lengths
+        of the listed sequences; out: optional (tables, lengths) int32 arrays of
+        those shapes to fill in place (a pinned staging buffer, say)."""
         import numpy as np
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
         n = ids.shape[0]
-        tables = np.empty((n, max_blocks), dtype=np.int32)
-        lens = np.empty(n, dtype=np.int32)
+        if out is None:
+            tables = np.empty((n, max_blocks), dtype=np.int32)
+            lens = np.empty(n, dtype=np.int32)
+        else:
+            tables = _out_buffer(out[0], "tables", (max_blocks,))
+            lens = _out_buffer(out[1], "lengths")
+            if tables.shape[0] != n or lens.shape[0] != n:
+                raise ValueError("out must hold one row and one length per sequence")
         _check(self._lib.pa_batch_block_tables(self._h, ids.ctypes.data, n, max_blocks,
                                                tables.ctypes.data,
                                                lens.ctypes.data),

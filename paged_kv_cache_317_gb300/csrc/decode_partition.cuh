@@ -77,6 +77,9 @@ struct DecodeParams {
   float qscale;        // scale * log2(e): scores come out in log2 units
   int wait_first;      // this pass is the call's first kernel (no shared pass before it)
   int early_inputs;    // the read-only inputs may be read before that wait
+  const int32_t* tail_start;  // optional [N]: where a sequence's own part of a split partition begins
+  float* ws_tail_acc;         // [N * H][D] and [N * H]: the partials of those parts
+  float2* ws_tail_ml;
 };
 
 // Reduce each of N = TPR/2 partial dot products over the TPR lanes of a row
@@ -176,8 +179,24 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     wait_prerequisite();
     return;
   }
-  const int tok_begin = part * p.partition_tokens;
+  int tok_begin = part * p.partition_tokens;
   const int tok_end = min(L, tok_begin + p.partition_tokens);
+  // A partition whose first chunks a prefix record reads for several sequences:
+  // this item covers the sequence's own part, from tail_start on, and leaves its
+  // partial in the sequence's tail row, which the merge adds to the others.
+  bool tail = false;
+  if (p.tail_start != nullptr) {
+    const int ts = __ldg(p.tail_start + seq);
+    if (ts >= 0 && ts / p.partition_tokens == part) {
+      if (ts <= tok_begin || ts >= tok_end || ts % kChunk != 0) {
+        if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, ts);
+        wait_prerequisite();
+        return;
+      }
+      tok_begin = ts;
+      tail = true;
+    }
+  }
   const int nchunks = (max(0, tok_end - tok_begin) + kChunk - 1) / kChunk;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -377,7 +396,15 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(kFullMask, l, off);
 
-    if (nparts == 1) {
+    if (tail) {
+      const size_t row = static_cast<size_t>(seq) * p.num_heads + h;
+      if (r == 0) {
+        float* dst = p.ws_tail_acc + row * D + c * 8;
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      }
+      if (lane == 0) p.ws_tail_ml[row] = make_float2(m, l);
+    } else if (nparts == 1) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (r == 0) {
         float o[8];

@@ -52,13 +52,63 @@ bool launch_order(const int32_t* seq_lens, int num_seqs, const int32_t* order,
       seqs[k] = i;
     }
   } else {
-    // Long sequences start early and the short ones fill the launch's tail.
-    std::iota(seqs.begin(), seqs.end(), 0);
-    std::stable_sort(seqs.begin(), seqs.end(),
-                     [&](int32_t a, int32_t b) { return seq_lens[a] > seq_lens[b]; });
+    // Long sequences start early and the short ones fill the launch's tail:
+    // one sort of (longest first, then index) keys, all distinct.
+    std::vector<uint64_t> key(static_cast<size_t>(num_seqs));
+    for (int i = 0; i < num_seqs; ++i)
+      key[i] = (static_cast<uint64_t>(~static_cast<uint32_t>(seq_lens[i])) << 32) |
+               static_cast<uint32_t>(i);
+    std::sort(key.begin(), key.end());
+    for (int k = 0; k < num_seqs; ++k) seqs[k] = static_cast<int32_t>(key[k] & 0xffffffffu);
   }
   return true;
 }
+
+// How often each block id occurs among one partition's candidates, in an
+// open-addressing table, so that only the candidates whose first block occurs
+// more than once (the only ones a record can take) are sorted into runs.
+class BlockCounts {
+ public:
+  void reset(size_t n) {
+    size_t cap = 64;
+    while (cap < 2 * n) cap <<= 1;
+    if (key_.size() < cap) {
+      key_.assign(cap, 0);
+      count_.assign(cap, 0);
+      stamp_.assign(cap, 0);
+    }
+    mask_ = cap - 1;
+    if (++now_ == 0) {  // the generation counter wrapped: forget every stamp
+      std::fill(stamp_.begin(), stamp_.end(), 0u);
+      now_ = 1;
+    }
+  }
+  void add(int32_t block) {
+    const size_t h = find(block);
+    if (stamp_[h] != now_) {
+      stamp_[h] = now_;
+      key_[h] = block;
+      count_[h] = 0;
+    }
+    ++count_[h];
+  }
+  bool repeated(int32_t block) const {
+    const size_t h = find(block);
+    return stamp_[h] == now_ && count_[h] > 1;
+  }
+
+ private:
+  size_t find(int32_t block) const {
+    size_t h = (static_cast<uint32_t>(block) * 0x9E3779B1u) & mask_;
+    while (stamp_[h] == now_ && key_[h] != block) h = (h + 1) & mask_;
+    return h;
+  }
+  std::vector<int32_t> key_;
+  std::vector<int32_t> count_;
+  std::vector<uint32_t> stamp_;
+  size_t mask_ = 0;
+  uint32_t now_ = 0;
+};
 
 }  // namespace
 
@@ -135,6 +185,19 @@ extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* 
                                     int32_t* work_items, int32_t items_capacity,
                                     int32_t* num_items, int32_t* records,
                                     int32_t records_capacity, int32_t* num_records) {
+  return pa_decode_share_plan_ex(block_tables, seq_lens, num_seqs, max_blocks_per_seq,
+                                 block_size, partition_tokens, fused_append, order, 0,
+                                 work_items, items_capacity, num_items, records,
+                                 records_capacity, num_records, nullptr);
+}
+
+extern "C" int pa_decode_share_plan_ex(const int32_t* block_tables, const int32_t* seq_lens,
+                                       int num_seqs, int max_blocks_per_seq, int block_size,
+                                       int partition_tokens, int fused_append,
+                                       const int32_t* order, int prefixes, int32_t* work_items,
+                                       int32_t items_capacity, int32_t* num_items,
+                                       int32_t* records, int32_t records_capacity,
+                                       int32_t* num_records, int32_t* tail_start) {
   if (!num_items || !num_records || num_seqs < 0 ||
       (num_seqs > 0 && (!seq_lens || !block_tables)) || max_blocks_per_seq <= 0 ||
       block_size <= 0 || items_capacity < 0 || records_capacity < 0)
@@ -165,55 +228,112 @@ extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* 
 
   // Group, partition by partition, the sequences whose tables name the same
   // blocks over it.  Sequences share a physical block only through forks, so
-  // candidates are sorted by the partition's first block and only runs with an
-  // equal first block are compared entry by entry.
-  std::vector<int32_t> recs;
-  std::vector<std::pair<int32_t, int32_t>> keyed;  // (first block of the slice, sequence)
-  std::vector<int32_t> run, group;
-  for (int part = 0; part < most; ++part) {
-    const long long b0 = static_cast<long long>(part) * pt / block_size;
-    const long long b1 = (static_cast<long long>(part + 1) * pt - 1) / block_size;  // inclusive
-    const size_t n = static_cast<size_t>(b1 - b0 + 1);
-    keyed.clear();
+  // candidates are keyed by the partition's first block, and only the runs of
+  // an equal first block are compared entry by entry, in two ways:
+  //  - whole records: members whose tables agree over the whole partition;
+  //  - prefix records (if asked for): of the pairs still in the work list,
+  //    groups in run order that share the partition's first c whole 16-token
+  //    chunks (below every member's last token); each member keeps the rest of
+  //    the partition as its own item, from tail_start on.  One split per
+  //    sequence (its tail row in the workspace is single).
+  std::vector<int32_t> recs, prefix_recs;
+  std::vector<uint64_t> keyed;  // first block of the slice (high word), sequence
+  std::vector<int32_t> run, group, cand;
+  std::vector<int32_t> tails(static_cast<size_t>(num_seqs), -1);
+  BlockCounts counts;
+  const long long max_chunks = pt / 16 - 1;  // a prefix leaves at least one chunk's start
+  const bool split = prefixes && max_chunks >= 1 && max_chunks < (1ll << 22);
+  long long parts_to_scan = most;
+  if (split)
     for (int i = 0; i < num_seqs; ++i)
-      if (shareable[i] > part)
-        keyed.emplace_back(block_tables[static_cast<size_t>(i) * max_blocks_per_seq + b0], i);
+      parts_to_scan = std::max(parts_to_scan, first_part[i + 1] - first_part[i]);
+  const auto row = [&](int32_t i) {
+    return block_tables + static_cast<size_t>(i) * max_blocks_per_seq;
+  };
+  const auto key_seq = [](uint64_t k) { return static_cast<int32_t>(k & 0xffffffffu); };
+  const auto key_block = [](uint64_t k) { return static_cast<uint32_t>(k >> 32); };
+  for (long long part = 0; part < parts_to_scan; ++part) {
+    const long long start = part * pt;
+    const long long b0 = start / block_size;
+    const long long b1 = (start + pt - 1) / block_size;  // inclusive
+    const size_t n = static_cast<size_t>(b1 - b0 + 1);
+    const auto whole_ok = [&](int32_t i) { return shareable[i] > part; };
+    const auto prefix_ok = [&](int32_t i) {
+      return split && tails[i] < 0 && part < first_part[i + 1] - first_part[i] &&
+             seq_lens[i] - 1 - start >= 16;
+    };
+    cand.clear();
+    for (int i = 0; i < num_seqs; ++i)
+      if (whole_ok(i) || prefix_ok(i)) cand.push_back(i);
+    counts.reset(cand.size());
+    for (int32_t i : cand) counts.add(row(i)[b0]);
+    keyed.clear();
+    for (int32_t i : cand)
+      if (counts.repeated(row(i)[b0]))
+        keyed.push_back((static_cast<uint64_t>(static_cast<uint32_t>(row(i)[b0])) << 32) |
+                        static_cast<uint32_t>(i));
     std::sort(keyed.begin(), keyed.end());
     for (size_t a = 0; a < keyed.size();) {
       size_t e = a + 1;
-      while (e < keyed.size() && keyed[e].first == keyed[a].first) ++e;
-      if (e - a >= 2) {
-        run.clear();
-        for (size_t k = a; k < e; ++k) run.push_back(keyed[k].second);
-        // split the run into groups of identical slices (members in index order)
-        while (run.size() >= 2) {
-          const int32_t* ref =
-              block_tables + static_cast<size_t>(run[0]) * max_blocks_per_seq + b0;
-          group.clear();
-          size_t keep = 0;
-          for (size_t k = 0; k < run.size(); ++k) {
-            const int32_t* slice =
-                block_tables + static_cast<size_t>(run[k]) * max_blocks_per_seq + b0;
-            if (k == 0 || std::memcmp(slice, ref, n * sizeof(int32_t)) == 0)
-              group.push_back(run[k]);
-            else
-              run[keep++] = run[k];
-          }
-          run.resize(keep);
-          // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
-          for (size_t at = 0; at + 1 < group.size(); at += PA_SHARE_MAX_MEMBERS) {
-            const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, group.size() - at);
-            recs.push_back(part);
-            recs.push_back(static_cast<int32_t>(m));
-            for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
-              recs.push_back(j < m ? group[at + j] : -1);
-            for (size_t j = 0; j < m; ++j) covered[first_part[group[at + j]] + part] = 1;
-          }
+      while (e < keyed.size() && key_block(keyed[e]) == key_block(keyed[a])) ++e;
+      // whole records: split the run into groups of identical slices (members
+      // in index order)
+      run.clear();
+      for (size_t k = a; k < e; ++k)
+        if (whole_ok(key_seq(keyed[k]))) run.push_back(key_seq(keyed[k]));
+      while (run.size() >= 2) {
+        const int32_t* ref = row(run[0]) + b0;
+        group.clear();
+        size_t keep = 0;
+        for (size_t k = 0; k < run.size(); ++k) {
+          if (k == 0 || std::memcmp(row(run[k]) + b0, ref, n * sizeof(int32_t)) == 0)
+            group.push_back(run[k]);
+          else
+            run[keep++] = run[k];
         }
+        run.resize(keep);
+        // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
+        for (size_t at = 0; at + 1 < group.size(); at += PA_SHARE_MAX_MEMBERS) {
+          const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, group.size() - at);
+          recs.push_back(static_cast<int32_t>(part));
+          recs.push_back(static_cast<int32_t>(m));
+          for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
+            recs.push_back(j < m ? group[at + j] : -1);
+          for (size_t j = 0; j < m; ++j) covered[first_part[group[at + j]] + part] = 1;
+        }
+      }
+      // prefix records over the run's members still in the work list
+      group.clear();
+      if (split)
+        for (size_t k = a; k < e; ++k) {
+          const int32_t i = key_seq(keyed[k]);
+          if (prefix_ok(i) && !covered[first_part[i] + part]) group.push_back(i);
+        }
+      for (size_t at = 0; at + 1 < group.size(); at += PA_SHARE_MAX_MEMBERS) {
+        const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, group.size() - at);
+        const int32_t* ref = row(group[at]);
+        long long c = max_chunks;
+        for (size_t j = 0; j < m; ++j)
+          c = std::min<long long>(c, (seq_lens[group[at + j]] - 1 - start) / 16);
+        // d: the first block (of those the c chunks touch) where some member's
+        // table differs; a chunk is alike when it ends before block d
+        long long d = (start + 16 * c - 1) / block_size + 1;
+        for (size_t j = 1; j < m && d > b0; ++j)
+          d = std::mismatch(ref + b0, ref + d, row(group[at + j]) + b0).first - ref;
+        const long long same = std::min(c, (d * block_size - start) / 16);
+        if (same < 1) continue;
+        prefix_recs.push_back(static_cast<int32_t>(part));
+        prefix_recs.push_back(static_cast<int32_t>(m + 256 * same));
+        for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
+          prefix_recs.push_back(j < m ? group[at + j] : -1);
+        for (size_t j = 0; j < m; ++j)
+          tails[group[at + j]] = static_cast<int32_t>(start + 16 * same);
       }
       a = e;
     }
   }
+  // whole records first: the longer ones start early in the shared pass
+  recs.insert(recs.end(), prefix_recs.begin(), prefix_recs.end());
   const long long nrec = static_cast<long long>(recs.size()) / PA_SHARE_RECORD_WORDS;
   const long long nitems = total - std::count(covered.begin(), covered.end(), 1);
   if (nrec > INT32_MAX || nitems > INT32_MAX) return PA_ERR_INVALID_ARG;
@@ -228,5 +348,6 @@ extern "C" int pa_decode_share_plan(const int32_t* block_tables, const int32_t* 
       if (!covered[first_part[i] + part]) *w++ = static_cast<int32_t>(i * P + part);
   }
   if (!recs.empty()) std::memcpy(records, recs.data(), recs.size() * sizeof(int32_t));
+  if (tail_start) std::memcpy(tail_start, tails.data(), tails.size() * sizeof(int32_t));
   return PA_OK;
 }

@@ -15,6 +15,8 @@ struct SharedParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* records;    // [num_records][PA_SHARE_RECORD_WORDS]
+  const int32_t* tail_start; // [N] or null: where a member's own part of a prefix
+                             // record's partition begins
   int num_records;
   int num_seqs;
   int num_heads;

@@ -16,11 +16,17 @@
 namespace pagedkv {
 namespace {
 
-// One warp per (sequence, head): out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+// One warp per (sequence, head): out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p,
+// over the sequence's partitions and, for a sequence whose partition was split by
+// a prefix record, its tail row.
 struct MergeParams {
   const int32_t* seq_lens;
   const float* ws_acc;
   const float2* ws_ml;
+  const int32_t* tail_start;  // optional [N]
+  const float* ws_tail_acc;   // [N * H][D]
+  const float2* ws_tail_ml;   // [N * H]
+  int32_t* err;
   void* out;
   int num_seqs, num_heads, capacity, partition_tokens, num_partitions, out_dtype;
 };
@@ -44,58 +50,74 @@ __global__ void __launch_bounds__(256) paged_attn_merge_kernel(const MergeParams
   int L = p.seq_lens[seq];
   L = L < 0 ? 0 : (L > p.capacity ? p.capacity : L);
   const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
-  if (nparts <= 1) return;  // the partition pass wrote this row directly
+  // a tail row, when tail_start names a split inside the sequence (partition
+  // pass: the tokens from it to its partition's end)
+  bool tail = false;
+  if (p.tail_start != nullptr) {
+    const int ts = __ldg(p.tail_start + seq);
+    if (ts >= 0) {
+      tail = ts < L && ts % 16 == 0 && ts % p.partition_tokens != 0;
+      if (!tail && lane == 0 && gw % p.num_heads == 0)
+        report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, ts);
+    }
+  }
+  if (nparts <= 1 && !tail) return;  // the partition pass wrote this row directly
   const size_t row0 = static_cast<size_t>(gw) * p.num_partitions;
+  const int n = nparts + (tail ? 1 : 0);  // partials: the partitions, then the tail row
+  auto ml_of = [&](int i) { return i < nparts ? p.ws_ml[row0 + i] : p.ws_tail_ml[gw]; };
+  auto acc_of = [&](int i) {
+    return i < nparts ? p.ws_acc + (row0 + i) * D : p.ws_tail_acc + static_cast<size_t>(gw) * D;
+  };
 
   float o[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) o[j] = 0.f;
   float M = -INFINITY, lt = 0.f;
-  if (nparts <= 32) {
-    // Lane i holds partition i's (m, l): one load for all of them, weights by
+  if (n <= 32) {
+    // Lane i holds partial i's (m, l): one load for all of them, weights by
     // shuffle, and the partials' rows loaded four at a time so that their
     // latencies overlap.
-    const float2 ml = lane < nparts ? p.ws_ml[row0 + lane] : make_float2(-INFINITY, 0.f);
+    const float2 ml = lane < n ? ml_of(lane) : make_float2(-INFINITY, 0.f);
     M = ml.x;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
     if (M != -INFINITY) {
-      const float w = lane < nparts ? exp2f(ml.x - M) : 0.f;
+      const float w = lane < n ? exp2f(ml.x - M) : 0.f;
       lt = w * ml.y;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
-      for (int i0 = 0; i0 < nparts; i0 += 4) {
+      for (int i0 = 0; i0 < n; i0 += 4) {
         float a[4][DPL];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int i = min(i0 + u, nparts - 1);  // repeats are weighted 0 below
-          const float* src = p.ws_acc + (row0 + i) * D + lane * DPL;
+          const int i = min(i0 + u, n - 1);  // repeats are weighted 0 below
+          const float* src = acc_of(i) + lane * DPL;
 #pragma unroll
           for (int j = 0; j < DPL; ++j) a[u][j] = src[j];
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float wu = __shfl_sync(kFullMask, w, min(i0 + u, 31));
-          const float wi = i0 + u < nparts ? wu : 0.f;
+          const float wi = i0 + u < n ? wu : 0.f;
 #pragma unroll
           for (int j = 0; j < DPL; ++j) o[j] = fmaf(wi, a[u][j], o[j]);
         }
       }
     }
   } else {
-    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, p.ws_ml[row0 + i].x);
+    for (int i = lane; i < n; i += 32) M = fmaxf(M, ml_of(i).x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
     if (M != -INFINITY) {
-      for (int i = lane; i < nparts; i += 32) {
-        const float2 ml = p.ws_ml[row0 + i];
+      for (int i = lane; i < n; i += 32) {
+        const float2 ml = ml_of(i);
         lt = fmaf(exp2f(ml.x - M), ml.y, lt);
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
-      for (int i = 0; i < nparts; ++i) {
-        const float w = exp2f(p.ws_ml[row0 + i].x - M);
-        const float* a = p.ws_acc + (row0 + i) * D + lane * DPL;
+      for (int i = 0; i < n; ++i) {
+        const float w = exp2f(ml_of(i).x - M);
+        const float* a = acc_of(i) + lane * DPL;
 #pragma unroll
         for (int j = 0; j < DPL; ++j) o[j] = fmaf(w, a[j], o[j]);
       }
@@ -116,6 +138,20 @@ size_t workspace_bytes_for(int num_seqs, int num_heads, int head_dim, int P) {
   if (P <= 1) return 0;
   const size_t rows = static_cast<size_t>(num_seqs) * num_heads * P;
   return rows * head_dim * sizeof(float) + rows * sizeof(float2);
+}
+
+// With tail rows: max(P, 1) partition rows per (sequence, head), then (from a
+// 256-byte boundary, so that the tail partials keep the alignment of their
+// 16-byte stores) one tail row each.
+size_t tail_offset_for(int num_seqs, int num_heads, int head_dim, int P) {
+  const size_t rows = static_cast<size_t>(num_seqs) * num_heads * (P > 1 ? P : 1);
+  const size_t main = rows * head_dim * sizeof(float) + rows * sizeof(float2);
+  return (main + 255) / 256 * 256;
+}
+size_t workspace_bytes_tails(int num_seqs, int num_heads, int head_dim, int P) {
+  const size_t rows = static_cast<size_t>(num_seqs) * num_heads;
+  return tail_offset_for(num_seqs, num_heads, head_dim, P) + rows * head_dim * sizeof(float) +
+         rows * sizeof(float2);
 }
 
 int resolve_partition(int partition_tokens) {
@@ -179,10 +215,10 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
       if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
   }
-  if ((phases & 2) && p.num_partitions > 1) {
-    MergeParams mp{p.seq_lens, p.ws_acc, p.ws_ml, p.out, num_seqs, p.num_heads,
-                   p.max_blocks * p.block_size, p.partition_tokens, p.num_partitions,
-                   p.out_dtype};
+  if ((phases & 2) && (p.num_partitions > 1 || p.tail_start != nullptr)) {
+    MergeParams mp{p.seq_lens, p.ws_acc, p.ws_ml, p.tail_start, p.ws_tail_acc, p.ws_tail_ml,
+                   p.err, p.out, num_seqs, p.num_heads, p.max_blocks * p.block_size,
+                   p.partition_tokens, p.num_partitions, p.out_dtype};
     const long long warps = static_cast<long long>(num_seqs) * p.num_heads;
     // A programmatic dependent of the pass before it: its blocks are placed while
     // that pass drains and wait (griddepcontrol.wait) for it before reading.
@@ -205,6 +241,19 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
 }  // namespace pagedkv
 
 using namespace pagedkv;
+
+extern "C" size_t paged_attn_workspace_size_tails(int num_seqs, int num_heads, int head_dim,
+                                                  int block_size, int max_blocks_per_seq,
+                                                  int partition_tokens) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  const int pt = resolve_partition(partition_tokens);
+  const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+  if (cap > (1ll << 30)) return 0;
+  return workspace_bytes_tails(num_seqs, num_heads, head_dim,
+                               num_partitions_for(static_cast<int>(cap), pt));
+}
 
 extern "C" size_t paged_attn_workspace_size(int num_seqs, int num_heads, int head_dim,
                                             int block_size, int max_blocks_per_seq,
@@ -260,7 +309,9 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   const int pt = resolve_partition(partition_tokens);
   const int P = num_partitions_for(static_cast<int>(cap), pt);
   if (num_seqs > 65535 || P > 65535) return PA_ERR_INVALID_ARG;
-  const size_t need = workspace_bytes_for(num_seqs, num_heads, head_dim, P);
+  const int32_t* tail_start = opts ? opts->tail_start : nullptr;
+  const size_t need = tail_start ? workspace_bytes_tails(num_seqs, num_heads, head_dim, P)
+                                 : workspace_bytes_for(num_seqs, num_heads, head_dim, P);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return PA_ERR_INVALID_ARG;
 
@@ -284,9 +335,16 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   p.out = out;
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                             static_cast<size_t>(num_seqs) * num_heads * P *
-                                                 head_dim * sizeof(float))
+                                             static_cast<size_t>(num_seqs) * num_heads *
+                                                 (P > 1 ? P : 1) * head_dim * sizeof(float))
                  : nullptr;
+  p.tail_start = tail_start;
+  if (tail_start) {
+    char* t = static_cast<char*>(workspace) + tail_offset_for(num_seqs, num_heads, head_dim, P);
+    p.ws_tail_acc = reinterpret_cast<float*>(t);
+    p.ws_tail_ml = reinterpret_cast<float2*>(
+        t + static_cast<size_t>(num_seqs) * num_heads * head_dim * sizeof(float));
+  }
   p.err = error_record;
   p.num_heads = num_heads;
   p.block_size = block_size;
@@ -312,6 +370,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
     sp.block_tables = block_tables;
     sp.seq_lens = seq_lens;
     sp.records = opts->shared_records;
+    sp.tail_start = tail_start;
     sp.num_records = opts->num_shared;
     sp.num_seqs = num_seqs;
     sp.num_heads = num_heads;

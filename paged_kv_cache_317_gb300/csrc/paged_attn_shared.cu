@@ -159,15 +159,23 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
 
   // Check the record (every thread reaches the same conclusion): partition in
   // range, 1..8 members, each a valid sequence whose length covers the whole
-  // partition (and, with a fused append, the appended token lies past it).
+  // partition (and, with a fused append, the appended token lies past it); or,
+  // for a prefix record (word 1 = m + 256 c, c > 0), the first c chunks of the
+  // partition, with each member's own part starting right after them
+  // (tail_start) and holding at least its last token.
   const int part = __ldg(rec);
-  const int m = __ldg(rec + 1);
+  const int mw = __ldg(rec + 1);
+  const int m = mw & 255;
+  const int pc = mw >> 8;  // prefix chunks; 0: the whole partition
   const int cap = p.max_blocks * p.block_size;
-  bool bad = part < 0 || part >= p.num_partitions || m < 1 || m > kMembers;
-  int bad_value = part < 0 || part >= p.num_partitions ? part : m;
+  bool bad = part < 0 || part >= p.num_partitions || m < 1 || m > kMembers || pc < 0 ||
+             pc >= p.partition_tokens / kChunk || (pc > 0 && p.tail_start == nullptr);
+  int bad_value = part < 0 || part >= p.num_partitions ? part : mw;
+  const long long split = static_cast<long long>(part) * p.partition_tokens + pc * kChunk;
   if (!bad) {
-    const long long need = static_cast<long long>(part + 1) * p.partition_tokens +
-                           (p.fused_append ? 1 : 0);
+    const long long need = pc > 0 ? split + 1
+                                  : static_cast<long long>(part + 1) * p.partition_tokens +
+                                        (p.fused_append ? 1 : 0);
     for (int i = 0; i < m && !bad; ++i) {
       const int s = __ldg(rec + 2 + i);
       if (s < 0 || s >= p.num_seqs) {
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
         bad_value = s;
       } else {
         const int L = __ldg(p.seq_lens + s);
-        if (L < need || L > cap) {
+        if (L < need || L > cap || (pc > 0 && __ldg(p.tail_start + s) != split)) {
           bad = true;
           bad_value = s;
         }
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   }
   const int first = __ldg(rec + 2);
   const int tok_begin = part * p.partition_tokens;
-  const int nchunks = p.partition_tokens / kChunk;
+  const int nchunks = pc > 0 ? pc : p.partition_tokens / kChunk;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxRing;
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
         const int L = __ldg(p.seq_lens + seq);
         const int nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
         const size_t base = (static_cast<size_t>(seq) * p.num_heads + h) * D + g;
-        if (nparts == 1) {
+        if (nparts == 1 && pc == 0) {
           const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll
           for (int dd = 0; dd < D / 16; ++dd) {

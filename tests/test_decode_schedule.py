@@ -240,3 +240,167 @@ def test_share_plan_with_8_token_blocks_matches_its_definition():
         want_recs, want_items = _plan_by_definition(tables, lens, pt, bs, fused)
         assert _records_as_set(recs) == want_recs, trial
         assert np.array_equal(items, want_items), trial
+
+
+def _prefix_plan_by_definition(tables, lens, pt, bs, fused, order=None):
+    """The prefix step restated: (prefix records as a set of (p, m, c, members),
+    tail_start), on top of the whole-partition plan."""
+    N, MB = tables.shape
+    full, items = _plan_by_definition(tables, lens, pt, bs, fused, order)
+    covered = {(i, p) for p, mem in full for i in mem}
+    nparts = [max(1, -(-int(L) // pt)) for L in lens]
+    tails = np.full(N, -1, dtype=np.int32)
+    recs = set()
+    max_chunks = pt // 16 - 1
+    if max_chunks >= 1:
+        for p in range(max(nparts, default=0)):
+            start = p * pt
+            cand = [i for i in range(N) if tails[i] < 0 and p < nparts[i]
+                    and (i, p) not in covered and int(lens[i]) - 1 - start >= 16]
+            groups = {}
+            for i in sorted(cand, key=lambda i: (int(tables[i, start // bs]), i)):
+                groups.setdefault(int(tables[i, start // bs]), []).append(i)
+            for grp in groups.values():
+                for at in range(0, len(grp) - 1, B.PA_SHARE_MAX_MEMBERS):
+                    mem = grp[at:at + B.PA_SHARE_MAX_MEMBERS]
+                    c = min([max_chunks] + [(int(lens[i]) - 1 - start) // 16 for i in mem])
+                    same = 0
+                    while same < c:
+                        t0 = start + 16 * same
+                        blocks = range(t0 // bs, (t0 + 15) // bs + 1)
+                        if any(tables[i, b] != tables[mem[0], b] for i in mem for b in blocks):
+                            break
+                        same += 1
+                    if same < 1:
+                        continue
+                    recs.add((p, len(mem), same, tuple(mem)))
+                    for i in mem:
+                        tails[i] = start + 16 * same
+    return full, recs, items, tails
+
+
+def _random_family_tables(rng, bs):
+    pt = int(rng.choice([32, 64, 128, 256]))
+    N, MB = int(rng.integers(2, 40)), int(rng.integers(2, 24))
+    prompts = rng.integers(0, 500, size=(4, MB)).astype(np.int32)
+    tables = rng.integers(0, 500, size=(N, MB)).astype(np.int32)
+    lens = rng.integers(0, MB * bs + 1, size=N)
+    for i in range(N):
+        if rng.random() < 0.8:
+            k = int(rng.integers(0, MB + 1))
+            tables[i, :k] = prompts[int(rng.integers(0, 4)), :k]
+    return pt, tables, lens
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 48])
+def test_share_plan_prefix_matches_its_definition(bs):
+    rng = np.random.default_rng(11 + bs)
+    for trial in range(80):
+        pt, tables, lens = _random_family_tables(rng, bs)
+        fused = bool(rng.integers(0, 2))
+        if fused:
+            lens = np.maximum(lens, 1)
+        order = None if trial % 3 else list(rng.permutation(len(lens)))
+        items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=fused,
+                                                 order=order)
+        full, want_pre, want_items, want_tails = _prefix_plan_by_definition(
+            tables, lens, pt, bs, fused, order)
+        whole = {(int(r[0]), tuple(int(x) for x in r[2:2 + (r[1] & 255)])) for r in recs
+                 if r[1] >> 8 == 0}
+        pre = {(int(r[0]), int(r[1]) & 255, int(r[1]) >> 8,
+                tuple(int(x) for x in r[2:2 + (r[1] & 255)])) for r in recs if r[1] >> 8}
+        assert whole == full, trial
+        assert pre == want_pre, trial
+        assert np.array_equal(items, want_items), trial
+        assert np.array_equal(tails, want_tails), trial
+        # without prefixes the plan is the whole-partition one, tails all -1
+        items0, recs0 = B.share_plan(tables, lens, pt, bs, fused_append=fused, order=order)
+        assert np.array_equal(items0, items) and _records_as_set(recs0) == full
+
+
+def test_share_plan_prefix_covers_every_token_once_on_forked_sequences():
+    """Beams forked from prompts, diverging at different steps: every token of every
+    sequence is read exactly once, by a whole-partition record, a prefix record
+    (over blocks every member's table names alike) or the sequence's own item."""
+    bs, pt = 16, 128
+    alloc = B.BlockAllocator(6000, bs)
+    rng = np.random.default_rng(4)
+    ids = []
+    for k, prompt in enumerate((300, 700, 1000, 77)):
+        alloc.add(100 * k, prompt)
+        for s in range(1, 5):
+            alloc.fork(100 * k, 100 * k + s)
+            ids.append(100 * k + s)
+        ids.append(100 * k)
+    for step in range(30):                                 # fork / free churn per step
+        if step % 3 == 0:
+            for k in range(4):
+                par, child = 100 * k, 1000 + 10 * step + k
+                alloc.fork(par, child)
+                ids.append(child)
+        alloc.batch_append(ids)
+    MB = 90
+    tables, lens = alloc.batch_block_tables(ids, MB)
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=True)
+    assert (tails >= 0).sum() > 0 and any(r[1] >> 8 for r in recs)
+    P = -(-MB * bs // pt)
+    seen = [np.zeros(int(L), dtype=np.int32) for L in lens]
+    for x in items:
+        i, p = int(x) // P, int(x) % P
+        a = int(tails[i]) if tails[i] >= 0 and tails[i] // pt == p else p * pt
+        seen[i][a:min(int(lens[i]), (p + 1) * pt)] += 1
+    for r in recs:
+        p, m, c = int(r[0]), int(r[1]) & 255, int(r[1]) >> 8
+        mem = [int(x) for x in r[2:2 + m]]
+        end = (p + 1) * pt if c == 0 else p * pt + 16 * c
+        blocks = slice(p * pt // bs, (end - 1) // bs + 1)
+        assert all((tables[i, blocks] == tables[mem[0], blocks]).all() for i in mem)
+        for i in mem:
+            assert end <= int(lens[i]) - 1                 # the appended token stays private
+            if c:
+                assert tails[i] == end
+            seen[i][p * pt:end] += 1
+    assert all((s == 1).all() for s in seen)
+
+
+def test_plan_and_tables_fill_caller_buffers_in_place():
+    """out= buffers (a pinned staging buffer in a serving loop) get the same plan
+    and tables as fresh arrays; the results are views of them."""
+    bs, pt = 16, 128
+    alloc = B.BlockAllocator(800, bs)
+    ids = []
+    for k, n in enumerate((300, 520, 90)):
+        alloc.add(10 * k, n)
+        ids.append(10 * k)
+        for s in range(1, 4):
+            alloc.fork(10 * k, 10 * k + s)
+            ids.append(10 * k + s)
+    for _ in range(20):
+        alloc.batch_append(ids)
+    MB = 48
+    want_t, want_l = alloc.batch_block_tables(ids, MB)
+    buf = np.full(len(ids) * (MB + 1) + 8, 7, dtype=np.int32)
+    bt, sl = buf[:len(ids) * MB].reshape(len(ids), MB), buf[len(ids) * MB:len(ids) * (MB + 1)]
+    t, l = alloc.batch_block_tables(ids, MB, out=(bt, sl))
+    assert np.shares_memory(t, buf) and np.array_equal(t, want_t) and np.array_equal(l, want_l)
+    assert (buf[len(ids) * (MB + 1):] == 7).all()
+    with pytest.raises(ValueError):
+        alloc.batch_block_tables(ids, MB, out=(bt[:, :-1], sl))
+    with pytest.raises(ValueError):
+        alloc.batch_block_tables(ids, MB, out=(bt.astype(np.int64), sl))
+    P = -(-MB * bs // pt)
+    it = np.empty(len(ids) * P, np.int32)
+    rc = np.empty((len(ids) * P // 2, B.PA_SHARE_RECORD_WORDS), np.int32)
+    ts = np.empty(len(ids), np.int32)
+    for fn, out, n_out in ((B.share_plan_prefix, (it, rc, ts), 3), (B.share_plan, (it, rc), 2)):
+        want = fn(want_t, want_l, pt, bs)
+        got = fn(t, l, pt, bs, out=out)
+        assert len(got) == n_out
+        for g, w, o in zip(got, want, out):
+            assert np.shares_memory(g, o) and np.array_equal(g, w)
+    with pytest.raises(ValueError):
+        B.share_plan_prefix(t, l, pt, bs, out=(it, rc, ts[:-1]))
+    with pytest.raises(ValueError):
+        B.share_plan(t, l, pt, bs, out=(it, rc[:, :-1]))
+    with pytest.raises(B.PagedKVError):
+        B.share_plan(t, l, pt, bs, out=(it[:3], rc))        # too little room

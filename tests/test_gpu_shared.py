@@ -88,9 +88,12 @@ class Families:
         mb = max_blocks or max(len(self.alloc.block_table(i)) for i in self.ids)
         return self.alloc.batch_block_tables(self.ids, mb)
 
-    def decode(self, tables, lens, pt, items=None, recs=None, out_dtype=torch.float32):
+    def decode(self, tables, lens, pt, items=None, recs=None, out_dtype=torch.float32,
+               tails=None):
         B = self.B
         kw = dict(partition_tokens=pt, error_record=self.rec, out_dtype=out_dtype)
+        if tails is not None:
+            kw["tail_start"] = torch.from_numpy(tails).cuda()
         if items is not None:
             kw["work_items"] = torch.from_numpy(items).cuda()
         if recs is not None:
@@ -240,7 +243,7 @@ def test_shared_random_configuration_8_token_blocks(B, seed):
     _random_shared_case(B, 500 + seed, block_size=8)
 
 
-def _random_shared_case(B, seed, block_size=None):
+def _random_shared_case(B, seed, block_size=None, prefixes=False):
     rng = np.random.default_rng(7000 + seed)
     D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32]))
@@ -256,9 +259,14 @@ def _random_shared_case(B, seed, block_size=None):
                    tail_max=int(rng.integers(0, 200)), H=H, D=D, bs=bs, dtype=dtype, fused=fused)
     tables, lens = fam.tables()
     order = None if seed % 3 else rng.permutation(len(lens))
-    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused, order=order)
+    tails = None
+    if prefixes:
+        items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=fused,
+                                                 order=order)
+    else:
+        items, recs = B.share_plan(tables, lens, pt, bs, fused_append=fused, order=order)
     out_dtype = [torch.float32, torch.float16, torch.bfloat16][int(rng.integers(0, 3))]
-    out = fam.decode(tables, lens, pt, items, recs, out_dtype=out_dtype)
+    out = fam.decode(tables, lens, pt, items, recs, out_dtype=out_dtype, tails=tails)
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, f"seed {seed}: D{D} bs{bs} H{H} {dtype} pt{pt} fused={fused} "
                          f"{len(recs)} records")
@@ -286,3 +294,132 @@ def test_single_member_records_match_oracle(B):
     out = fam.decode(tables, lens, pt, np.array(keep, dtype=np.int32), np.stack(recs))
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, "single-member records")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("dtype,D,bs", [("bf16", 128, 16), ("f16", 64, 32), ("bf16", 256, 8),
+                                        ("f16", 128, 16)])
+def test_prefix_records_match_oracle(B, fused, dtype, D, bs):
+    """Prompts that end inside a partition: the chunks of that partition which the
+    whole family still shares are read once by a prefix record, each member's rest
+    by its own item from tail_start on, and the merge adds the two."""
+    fam = Families(B, 31 + D + bs, prompts=[700, 300, 1000, 1200], members=6, tail_max=150,
+                   H=4, D=D, bs=bs, dtype=dtype, fused=fused)
+    tables, lens = fam.tables()
+    pt = 128
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=fused)
+    assert (recs[:, 1] >> 8).max() >= 2 and (tails >= 0).sum() >= 12
+    out = fam.decode(tables, lens, pt, items, recs, tails=tails)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, f"prefix {dtype} D{D} bs{bs} fused={fused}")
+
+
+def test_prefix_records_single_partition_sequences(B):
+    """Sequences of one partition: the prefix record leaves its partial in the
+    workspace (not in the output), and the merge runs for them too."""
+    fam = Families(B, 77, prompts=[200, 90], members=5, tail_max=40, H=8, D=128, bs=16,
+                   dtype="bf16", fused=True)
+    tables, lens = fam.tables()
+    pt = 256
+    assert lens.max() <= pt
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, 16, fused_append=True)
+    assert len(recs) and (recs[:, 1] >> 8).min() >= 1
+    for out_dtype in (torch.float32, torch.bfloat16):
+        out = fam.decode(tables, lens, pt, items, recs, out_dtype=out_dtype, tails=tails)
+        assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+        fam.check(out, lens, f"one partition, out {out_dtype}")
+
+
+def test_prefix_and_whole_plans_agree(B):
+    fam = Families(B, 23, prompts=[1100, 900, 650], members=8, tail_max=300, H=8, D=128,
+                   bs=16, dtype="bf16", fused=False)
+    tables, lens = fam.tables()
+    items, recs = B.share_plan(tables, lens, 256, 16, fused_append=False)
+    items2, recs2, tails = B.share_plan_prefix(tables, lens, 256, 16, fused_append=False)
+    assert len(recs2) > len(recs)
+    a = fam.decode(tables, lens, 256, items, recs)
+    b = fam.decode(tables, lens, 256, items2, recs2, tails=tails)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    torch.testing.assert_close(a, b, rtol=2e-3, atol=2e-3)
+    fam.check(b, lens, "prefix plan")
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_prefix_random_configuration(B, seed):
+    _random_shared_case(B, 300 + seed, prefixes=True)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefix_random_configuration_8_token_blocks(B, seed):
+    _random_shared_case(B, 900 + seed, block_size=8, prefixes=True)
+
+
+def test_prefix_plan_replays_from_a_cuda_graph(B):
+    """The decode with prefix records captured once: new plans (other records,
+    other tails) written into the same device buffers give the oracle's output."""
+    fam = Families(B, 55, prompts=[800, 450], members=7, tail_max=120, H=4, D=128, bs=16,
+                   dtype="f16", fused=False)
+    tables, lens = fam.tables()
+    pt, N, RW = 128, len(lens), B.PA_SHARE_RECORD_WORDS
+    P = -(-tables.shape[1] * 16 // pt)
+    it_d = torch.zeros(N * P, dtype=torch.int32, device="cuda")
+    rc_d = torch.zeros((N * P, RW), dtype=torch.int32, device="cuda")
+    ts_d = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    bt, sl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    out = torch.empty((N, 4, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.paged_attn_workspace_size(N, 4, 128, 16, tables.shape[1], pt, tails=True),
+                     dtype=torch.uint8, device="cuda")
+
+    def load(items, recs, tails):
+        it_d.zero_()
+        it_d[:len(items)] = torch.from_numpy(items)
+        rc_d[:len(recs)] = torch.from_numpy(recs)
+        ts_d.copy_(torch.from_numpy(tails))
+        return it_d[:len(items)], rc_d[:len(recs)]
+
+    plans = [B.share_plan_prefix(tables, lens, pt, 16),
+             B.share_plan_prefix(tables, lens, pt, 16, order=list(range(N))[::-1])]
+    its, rcs = load(*plans[0])
+    step = lambda: B.paged_attn_decode(fam.q, fam.kc, fam.vc, bt, sl, fam.scale, out=out,
+                                       partition_tokens=pt, workspace=ws, work_items=its,
+                                       shared_records=rcs, tail_start=ts_d,
+                                       error_record=fam.rec)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for items, recs, tails in plans:
+        assert len(items) == len(its) and len(recs) == len(rcs)
+        load(items, recs, tails)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+        fam.check(out, lens, "graph replay")
+
+
+def test_prefix_record_and_tail_start_that_disagree_report_an_error(B):
+    """A tail_start that names another split than its prefix record, or that is not
+    a multiple of 16 tokens: an error in the record, no hang, no stray writes."""
+    fam = Families(B, 5, prompts=[700], members=4, tail_max=60, H=4, D=128, bs=16,
+                   dtype="bf16", fused=False)
+    tables, lens = fam.tables()
+    items, recs, tails = B.share_plan_prefix(tables, lens, 128, 16, fused_append=False)
+    s = int(np.flatnonzero(tails >= 0)[0])
+    for bad in (int(tails[s]) + 16, int(tails[s]) + 3):
+        if bad >= int(lens[s]):
+            continue
+        t = tails.copy()
+        t[s] = bad
+        B.pa_error_clear(fam.rec)
+        fam.decode(tables, lens, 128, items, recs, tails=t)
+        assert B.pa_error_read(fam.rec)[0] != 0
+    B.pa_error_clear(fam.rec)
+    out = fam.decode(tables, lens, 128, items, recs, tails=tails)
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, "after the bad calls")
