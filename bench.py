@@ -732,14 +732,22 @@ def run_workload(args, rank, world, local_rank, emit=True):
         bt = torch.from_numpy(b.block_tables).to(dev)
         sl = torch.from_numpy(b.context_lens).to(dev)
         out = torch.empty(b.q.shape, dtype=b.q.dtype, device=dev)
-        pt = 512
+        # the host schedule: partition length for the batch (512 for long context,
+        # 32 for the tiny batch) and the work list, longest first
+        pt = B.decode_partition_tokens(b.context_lens, b.num_heads)
+        items = torch.from_numpy(B.partition_work_items(b.context_lens, pt,
+                                                        b.max_blocks_per_seq,
+                                                        b.block_size)).to(dev)
+        ws = torch.empty(max(16, B.paged_attn_workspace_size(
+            b.num_seqs, b.num_heads, b.head_dim, b.block_size, b.max_blocks_per_seq, pt)),
+            dtype=torch.uint8, device=dev)
+        kw = dict(out=out, partition_tokens=pt, workspace=ws, work_items=items,
+                  error_record=rec)
         if b.has_append:
             fn = lambda: B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt,
-                                                    sl, b.scale, out=out, partition_tokens=pt,
-                                                    error_record=rec)
+                                                    sl, b.scale, **kw)
         else:
-            fn = lambda: B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, out=out,
-                                             partition_tokens=pt, error_record=rec)
+            fn = lambda: B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, **kw)
         flush = None
         if w == "tiny":
             scratch = torch.empty(2 * 132 * 2 ** 20, dtype=torch.uint8, device=dev)
@@ -751,6 +759,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
         line.update(config={"workload": b.name, "num_seqs": b.num_seqs, "num_heads": b.num_heads,
                             "head_dim": b.head_dim, "block_size": b.block_size,
                             "context_tokens": int(b.context_lens.sum()),
+                            "partition_tokens": pt,
+                            "schedule": "host-chosen partition length and work list",
                             "l2": "flushed between steps" if flush else "inputs larger than L2"},
                     dtype="f16" if b.dtype == torch.float16 else "bf16")
         tokens = int(b.context_lens.sum())

@@ -283,11 +283,13 @@ int paged_attn_decode_append(const void* q, const void* new_k, const void* new_v
  * (and one share plan) serves all the layers of a decode step.
  *
  * pa_decode_partition_tokens: writes to *partition_tokens the longest of 512,
- * 256 and 128 for which the heaviest block, min(partition, max_i L_i) tokens,
- * is at most 1/c of the average work per SM, sum_i L_i * num_heads /
- * heads_per_cta / num_sms, with c = 3.5 for 512 and 256 and c = 2 for 128; else
- * 64.  A batch with a lot of work per SM keeps 512; a few short sequences get
- * short partitions so that every SM has blocks.
+ * 256, 128 and 64 for which the heaviest block, min(partition, max_i L_i)
+ * tokens, is at most 1/c of the average work per SM, sum_i L_i * num_heads /
+ * heads_per_cta / num_sms, with c = 3.5 for 512 and 256, c = 2 for 128 and
+ * c = 1 for 64; else 32.  That length is then doubled, up to 512, while the
+ * longest sequence would take more than 32 partitions.  A batch with a lot of
+ * work per SM keeps 512; a few short sequences get short partitions so that
+ * every SM has blocks.
  *   seq_lens       host int32 [num_seqs], the lengths the decode will see (for
  *                  the fused append: including the appended token); each >= 0
  *   heads_per_cta  as in pa_decode_opts (0 = the automatic choice)

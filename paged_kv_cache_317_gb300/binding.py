@@ -87,7 +87,7 @@ def decode_partition_tokens(seq_lens, num_heads: int, heads_per_cta: int = 0,
                             num_sms: int = 0) -> int:
     """Split-K partition length for a decode over these (host) lengths, chosen by
     pa_decode_partition_tokens: 512 for batches with plenty of work per SM, down
-    to 64 for a few short sequences.  num_sms 0 asks the current device."""
+    to 32 for a few short sequences.  num_sms 0 asks the current device."""
     lens = _host_int32(seq_lens, "seq_lens")
     out = ctypes.c_int32()
     _check(load_library().pa_decode_partition_tokens(

@@ -24,17 +24,26 @@ namespace {
 // set the launch's length.  Shorter partitions add merge work and per-block
 // start-up cost, so the longest one that balances is best; a 128-token block
 // is cheap enough to start that it needs less balance (c = 2) than the longer
-// ones (c = 3.5).  Measured on GB300 with CUDA-graph replays over 39 batches
-// (1 to 512 sequences, medians of 30 to 30000 tokens, 40 heads x 128): on
-// average within 1.1 % of the best of 32..512 for each batch, at worst 13 %
-// (a 10 us call over 2 short sequences), where a fixed 512 is up to 2.4x slower
-// on batches of 1 to 24 sequences.
+// ones (c = 3.5), a 64-token one less still (c = 1).  Measured on GB300 with
+// CUDA-graph replays over 39 batches (1 to 512 sequences, medians of 30 to
+// 30000 tokens, 40 heads x 128): on average within 1.1 % of the best of
+// 32..512 for each batch, at worst 13 % (a 10 us call over 2 short sequences),
+// where a fixed 512 is up to 2.4x slower on batches of 1 to 24 sequences.
+// Calls with less work than one 64-token block per SM (a few sequences of a
+// few hundred tokens and few heads) take 32: 4 sequences of 95 to 191 tokens
+// with 8 heads x 64 ran in 12.9 us against 14.7 us at 64, with L2 flushed.
+// Whatever balances, the longest sequence is cut into at most kMaxPieces
+// partitions (the merge takes up to 32 partials in one load per lane; more go
+// through a slower loop): one sequence of 1500 tokens with 8 heads ran 23.4 us
+// at 32 (47 partitions) against 18.0 at 64, one of 4000 with 4 heads 36.3 us at
+// 32 and 27.3 at 64 against 21.9 at 128.
+constexpr int kMaxPieces = 32;
 struct Candidate {
   int tokens;
   long long num, den;  // c = num / den
 };
-constexpr Candidate kCandidates[] = {{512, 7, 2}, {256, 7, 2}, {128, 2, 1}};
-constexpr int kShortest = 64;
+constexpr Candidate kCandidates[] = {{512, 7, 2}, {256, 7, 2}, {128, 2, 1}, {64, 1, 1}};
+constexpr int kShortest = 32;
 
 bool valid_partition(int pt) { return pt > 0 && pt % 16 == 0; }
 
@@ -136,14 +145,20 @@ extern "C" int pa_decode_partition_tokens(const int32_t* seq_lens, int num_seqs,
     longest = std::max(longest, static_cast<int>(seq_lens[i]));
   }
   const long long work = tokens * (num_heads / G);
+  int pt = kShortest;
   for (const Candidate& c : kCandidates) {
     const long long heaviest = std::min(c.tokens, longest);
     if (c.num * heaviest * num_sms <= c.den * work) {
-      *partition_tokens = c.tokens;
-      return PA_OK;
+      pt = c.tokens;
+      break;
     }
   }
-  *partition_tokens = kShortest;
+  // no shorter than needed to keep the longest sequence within kMaxPieces
+  // partitions (512 at the most)
+  while (pt < kCandidates[0].tokens &&
+         (static_cast<long long>(longest) + pt - 1) / pt > kMaxPieces)
+    pt *= 2;
+  *partition_tokens = pt;
   return PA_OK;
 }
 

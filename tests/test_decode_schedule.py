@@ -14,10 +14,14 @@ def rule(lens, num_heads, heads_per_cta, num_sms):
     G = heads_per_cta or (2 if num_heads % 2 == 0 else 1)
     work = int(np.sum(lens)) * (num_heads // G)
     longest = int(np.max(lens)) if len(lens) else 0
-    for pt, c in ((512, 3.5), (256, 3.5), (128, 2.0)):
+    chosen = 32
+    for pt, c in ((512, 3.5), (256, 3.5), (128, 2.0), (64, 1.0)):
         if min(pt, longest) * num_sms * c <= work:
-            return pt
-    return 64
+            chosen = pt
+            break
+    while chosen < 512 and -(-longest // chosen) > 32:   # at most 32 pieces
+        chosen *= 2
+    return chosen
 
 
 def test_partition_choice_follows_the_balance_rule():
@@ -36,7 +40,8 @@ def test_partition_choice_follows_the_balance_rule():
 def test_partition_choice_at_the_ends():
     big = np.full(256, 350)
     assert B.decode_partition_tokens(big, 40, 0, 152) == 512      # plenty of work per SM
-    assert B.decode_partition_tokens([350], 40, 0, 152) == 64     # one short sequence
+    assert B.decode_partition_tokens([350], 40, 0, 152) == 32     # one short sequence
+    assert B.decode_partition_tokens([350] * 2, 40, 0, 152) == 64
     assert B.decode_partition_tokens([1024] * 4, 40, 0, 152) == 128
     assert B.decode_partition_tokens([], 40, 0, 152) == 512       # nothing to balance
     # a long batch keeps 512 even with one huge sequence, since the heaviest
@@ -49,6 +54,14 @@ def test_partition_choice_at_the_ends():
     # 128 needs only half the work per SM: 2 x 4 SMs x 128 = 1024 = 4 x 128 x 2 heads
     assert B.decode_partition_tokens([128] * 4, 2, 1, 4) == 128
     assert B.decode_partition_tokens([128] * 3, 2, 1, 4) == 64
+    # 64 with c = 1: 64 x 4 SMs = 256 = 2 x 64 x 2 heads; below that, 32
+    assert B.decode_partition_tokens([64] * 2, 2, 1, 4) == 64
+    assert B.decode_partition_tokens([64, 63], 2, 1, 4) == 32
+    # ... but the longest sequence takes at most 32 partitions
+    assert B.decode_partition_tokens([1024], 8, 0, 152) == 32
+    assert B.decode_partition_tokens([1025], 8, 0, 152) == 64
+    assert B.decode_partition_tokens([4000], 4, 0, 152) == 128
+    assert B.decode_partition_tokens([100000], 4, 0, 152) == 512
 
 
 def test_partition_choice_rejects_bad_arguments():

@@ -283,7 +283,7 @@ def test_bad_work_item_is_recorded_and_skipped(B):
     assert not out[1].any()
 
 
-@pytest.mark.parametrize("lens", [[1500], [900, 3, 2048, 40], [1, 17, 64, 65, 300] * 8,
+@pytest.mark.parametrize("lens", [[1500], [900, 3, 2048, 40], [1, 17, 64, 65, 300] * 8, [95, 3, 191],
                                   [700] * 40 + [5, 2000]])
 def test_host_schedule_matches_oracle(B, lens):
     """The partition length and work list the host schedule picks (short partitions
@@ -291,7 +291,7 @@ def test_host_schedule_matches_oracle(B, lens):
     b = random_decode_batch(31 + len(lens), lens, 8, 128, 16, dtype="bf16", device="cuda",
                             with_append=True)
     pt = B.decode_partition_tokens(b.context_lens, 8)
-    assert pt in (64, 128, 256, 512)
+    assert pt in (32, 64, 128, 256, 512)
     items = B.partition_work_items(b.context_lens, pt, b.max_blocks_per_seq, 16)
     bt, sl = device_tables(b)
     rec = B.new_error_record()
