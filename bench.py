@@ -648,14 +648,16 @@ class _Staging:
     """Per-step host inputs of a serving loop in one pinned int32 buffer per set
     (copy-on-write pairs as int64, block tables, lengths, work list,
     shared-partition records, tail starts) and one device buffer, uploaded with
-    one copy.  The allocator and the planner write their outputs straight into a
-    set's regions (views); two sets alternate, and a set is refilled once the copy
-    that read it is done."""
+    one copy, with the numbers of work items and records (device-side counts, for
+    a step replayed from a CUDA graph over the lists' capacities).  The allocator
+    and the planner write their outputs straight into a set's regions (views);
+    two sets alternate, and a set is refilled once the copy that read it is done."""
 
     def __init__(self, n_seqs, max_blocks, n_items_max, record_words, dev):
         import torch
         self.sizes = {"pairs": 4 * n_seqs, "bt": n_seqs * max_blocks, "sl": n_seqs,
-                      "ts": n_seqs, "it": n_items_max, "rc": n_items_max * record_words}
+                      "ts": n_seqs, "cnt": 2, "it": n_items_max,
+                      "rc": n_items_max * record_words}
         self.off, at = {}, 0
         for k, n in self.sizes.items():
             self.off[k] = at
@@ -663,7 +665,10 @@ class _Staging:
         self.n_seqs, self.max_blocks, self.rw = n_seqs, max_blocks, record_words
         self.host = [torch.empty(at, dtype=torch.int32).pin_memory() for _ in range(2)]
         self.host_np = [h.numpy() for h in self.host]
-        self.dev = [torch.empty(at, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.dev = [torch.zeros(at, dtype=torch.int32, device=dev) for _ in range(2)]
+        for d in self.dev:   # no copy-on-write pairs and no split partitions before an upload
+            d[self.off["pairs"]:self.off["pairs"] + self.sizes["pairs"]] = -1
+            d[self.off["ts"]:self.off["ts"] + self.sizes["ts"]] = -1
         self.done = [torch.cuda.Event() for _ in range(2)]
 
     def views(self, step):
@@ -678,16 +683,21 @@ class _Staging:
                 h[o["rc"]:o["rc"] + self.sizes["rc"]].reshape(-1, self.rw),
                 h[o["ts"]:o["ts"] + n])
 
-    def upload(self, step, stream, pairs, n_items, n_recs, tails):
-        """Write the pairs into set step % 2 (its other regions filled through
-        views(step)) and enqueue its upload; returns device views (pairs int64
-        [n, 2], tables, lengths, work list, records, tail starts or None)."""
+    def upload(self, step, stream, pairs, n_items, n_recs, tails, pad=False):
+        """Write the pairs (pad: and -1 pairs up to the capacity) and the counts
+        into set step % 2 (its other regions filled through views(step)) and
+        enqueue its upload; returns device views (pairs int64 [n, 2], tables,
+        lengths, work list, records, tail starts or None)."""
         import numpy as np
         import torch
         j = step % 2
         h, o, n_p = self.host_np[j], self.off, len(pairs)
         if n_p:
             h[o["pairs"]:o["pairs"] + 4 * n_p].view(np.int64)[:] = pairs.ravel()
+        if pad:
+            h[o["pairs"] + 4 * n_p:o["pairs"] + self.sizes["pairs"]] = -1
+        h[o["cnt"]] = n_items
+        h[o["cnt"] + 1] = n_recs
         used = o["rc"] + n_recs * self.rw
         d = self.dev[j]
         d[:used].copy_(self.host[j][:used], non_blocking=True)
@@ -699,6 +709,20 @@ class _Staging:
                 d[o["it"]:o["it"] + n_items],
                 d[o["rc"]:o["rc"] + n_recs * self.rw].view(n_recs, self.rw) if n_recs else None,
                 d[o["ts"]:o["ts"] + self.n_seqs] if tails else None)
+
+    def capacity_views(self, j):
+        """Device views of set j over the lists' capacities, for a captured step:
+        pairs int64 [n_seqs, 2], tables, lengths, work list, records (half the
+        work list's capacity: a record holds at least two pairs), tail starts,
+        counts."""
+        import torch
+        d, o, n = self.dev[j], self.off, self.n_seqs
+        n_it = self.sizes["it"]
+        return (d[o["pairs"]:o["pairs"] + 4 * n].view(torch.int64).view(n, 2),
+                d[o["bt"]:o["bt"] + n * self.max_blocks].view(n, self.max_blocks),
+                d[o["sl"]:o["sl"] + n], d[o["it"]:o["it"] + n_it],
+                d[o["rc"]:o["rc"] + (n_it // 2) * self.rw].view(n_it // 2, self.rw),
+                d[o["ts"]:o["ts"] + n], d[o["cnt"]:o["cnt"] + 2])
 
 
 def run_workload(args, rank, world, local_rank, emit=True):
@@ -923,6 +947,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
         host_s, stage_s, plan_s, lens_seen, n_shared, n_prefix = 0.0, 0.0, 0.0, 0, 0, 0
+        launch_s = 0.0
         unique_seen = 0
         # per step: events before the upload, before the copies, before decode, after
         # (created before the loop: creating events costs host time every step)
@@ -975,12 +1000,16 @@ def run_workload(args, rank, world, local_rank, emit=True):
                 s_, stream, pairs, len(items), len(recs), tails is not None)
             stage_s += time.perf_counter() - h1
             evs[1].record(stream)
+            h3 = time.perf_counter()
             if len(pairs):
                 B.block_copy([kc], [vc], pairs_d)
+            h4 = time.perf_counter()
             evs[2].record(stream)
+            h5 = time.perf_counter()
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
                                        work_items=it_d, shared_records=rc_d, tail_start=ts_d)
+            launch_s += time.perf_counter() - h5 + h4 - h3
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
@@ -1018,6 +1047,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
                     host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
+                    host_launch_ms_per_step=round(1e3 * launch_s / plan.steps, 4),
                     unique_kv_bytes=round(unique_kv),
                     unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
                     unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4),
@@ -1065,9 +1095,37 @@ def run_workload(args, rank, world, local_rank, emit=True):
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
-        torch.cuda.synchronize()
+        graphs = None
+        if not args.no_graph:
+            # the device step (copy-on-write copies, fused append + decode) captured
+            # once per staging set over the lists' capacities; each step writes its
+            # lists and their counts into the set and replays the set's graph
+            qkv = torch.empty((3, N, H, D), dtype=plan.dtype, device=dev)
+            tok_stack = torch.stack([torch.stack(t) for t in tokens_all])
+            graphs = []
+            for j in range(2):
+                pc, btj, slj, itj, rcj, tsj, cj = staging.capacity_views(j)
+
+                def device_step(pc=pc, btj=btj, slj=slj, itj=itj, rcj=rcj, tsj=tsj, cj=cj):
+                    B.block_copy([kc], [vc], pc)
+                    B.paged_attn_decode_append(qkv[0], qkv[1], qkv[2], kc, vc, btj, slj,
+                                               plan.scale, out=out, partition_tokens=pt,
+                                               workspace=ws, error_record=rec, work_items=itj,
+                                               shared_records=rcj,
+                                               tail_start=tsj if prefix else None, counts=cj)
+                side = torch.cuda.Stream(dev)
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    device_step()                 # counts 0, no pairs: nothing but the merge
+                stream.wait_stream(side)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    device_step()
+                graphs.append(g)
+            torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
-        n_prefix = 0
+        n_prefix, launch_s = 0, 0.0
         unique_seen = 0
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                  for _ in range(plan.steps)]
@@ -1115,15 +1173,26 @@ def run_workload(args, rank, world, local_rank, emit=True):
             evs[0].record(stream)
             h1 = time.perf_counter()
             pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
-                s_, stream, pairs, len(items), len(recs), tails is not None)
+                s_, stream, pairs, len(items), len(recs), tails is not None,
+                pad=graphs is not None)
             stage_s += time.perf_counter() - h1
             evs[1].record(stream)
-            if len(pairs):
-                B.block_copy([kc], [vc], pairs_d)
-            evs[2].record(stream)
-            B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
-                                       partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=it_d, shared_records=rc_d, tail_start=ts_d)
+            h3 = time.perf_counter()
+            if graphs is not None:
+                qkv.copy_(tok_stack[s_])
+                graphs[s_ % 2].replay()
+                h4 = h5 = time.perf_counter()
+            else:
+                if len(pairs):
+                    B.block_copy([kc], [vc], pairs_d)
+                h4 = time.perf_counter()
+                evs[2].record(stream)
+                h5 = time.perf_counter()
+                B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
+                                           partition_tokens=pt, workspace=ws, error_record=rec,
+                                           work_items=it_d, shared_records=rc_d,
+                                           tail_start=ts_d)
+            launch_s += time.perf_counter() - h5 + h4 - h3
             evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
@@ -1133,6 +1202,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
         # the staged inputs of the last step gave the same output as direct uploads
         # (the fused append rewrites the same rows: idempotent)
         ref_out = torch.empty_like(out)
+        if B.pa_error_read(rec) != [0, 0, 0, 0]:
+            raise RuntimeError(f"device error record {B.pa_error_read(rec)}")
         B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
                                    torch.from_numpy(lens).to(dev), plan.scale, out=ref_out,
                                    partition_tokens=pt, workspace=ws, error_record=rec,
@@ -1159,19 +1230,26 @@ def run_workload(args, rank, world, local_rank, emit=True):
                                          f"shared partitions ({n_shared / plan.steps:.1f} "
                                          f"records per step, {n_prefix / plan.steps:.1f} "
                                          "of them prefix records) + work list"),
+                            "device_step": ("copies + fused append and decode replayed from "
+                                            "a CUDA graph (lists sized by device-side counts)"
+                                            if graphs is not None else "eager launches"),
                             "l2": "inputs larger than L2"},
                     dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
                     host_plan_ms_per_step=round(1e3 * plan_s / plan.steps, 4),
+                    host_launch_ms_per_step=round(1e3 * launch_s / plan.steps, 4),
                     unique_kv_bytes=round(unique_kv),
                     unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
                     unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
                     copies_per_step=round(copies / plan.steps, 2),
-                    device_ms_per_step_split={
-                        "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
-                        "append_and_decode": seg(2, 3),
-                        "note": "the append is fused into the decode launch"},
+                    device_ms_per_step_split=(
+                        {"table_uploads": seg(0, 1), "copies_append_and_decode": seg(1, 3),
+                         "note": "one graph: copies, then the append fused into the decode"}
+                        if graphs is not None else
+                        {"table_uploads": seg(0, 1), "block_copy": seg(1, 2),
+                         "append_and_decode": seg(2, 3),
+                         "note": "the append is fused into the decode launch"}),
                     note="value counts logical K/V bytes (beams share prefix blocks, so part "
                          "of them is served from L2)")
     elif w in ("append", "copy"):
@@ -1526,6 +1604,9 @@ def main(argv=None):
     ap.add_argument("--no-share", action="store_true",
                     help="sampling/beam/mixed: read shared partitions once per sequence "
                          "instead of once per group")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="beam: launch each step's copies and decode eagerly instead of "
+                         "replaying them from a CUDA graph")
     ap.add_argument("--no-prefix", action="store_true",
                     help="beam/mixed: share whole partitions only, not the shared first "
                          "chunks of a partition the group's members diverge in")

@@ -215,6 +215,15 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  The workspace must then hold paged_attn_workspace_size_tails
  *                  bytes.  pa_decode_share_plan_ex builds the records and this
  *                  array together.
+ *   counts         NULL, or device int32 [2]: how many of the work_items and of
+ *                  the shared_records to run, read by the kernels on the device.
+ *                  num_work_items and num_shared are then capacities (the sizes
+ *                  of the launches), and the entries past the counts are never
+ *                  read.  A call captured once in a CUDA graph can so be replayed
+ *                  with lists of other lengths written into the same buffers
+ *                  (with the counts).  A count outside [0, capacity] is recorded
+ *                  as PA_ERR_BAD_SEQ_LEN (index -1 for the items, -2 for the
+ *                  records; value = the count) and that launch computes nothing.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
@@ -236,6 +245,7 @@ typedef struct pa_decode_opts {
   int num_shared;
   int early_inputs;
   const int32_t* tail_start;
+  const int32_t* counts;
 } pa_decode_opts;
 
 int paged_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache,

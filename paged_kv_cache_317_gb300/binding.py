@@ -40,7 +40,7 @@ class pa_decode_opts(ctypes.Structure):
     _fields_ = [("heads_per_cta", c_int), ("stages", c_int), ("phases", c_int),
                 ("seq_order", c_void_p), ("work_items", c_void_p), ("num_work_items", c_int),
                 ("shared_records", c_void_p), ("num_shared", c_int), ("early_inputs", c_int),
-                ("tail_start", c_void_p)]
+                ("tail_start", c_void_p), ("counts", c_void_p)]
 
 
 PA_SHARE_MAX_MEMBERS = 8
@@ -48,13 +48,17 @@ PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
 
 
 def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_records=None,
-                 early_inputs=False, tail_start=None):
+                 early_inputs=False, tail_start=None, counts=None):
     if seq_order is not None:
         _need(seq_order, "seq_order", torch.int32)
     if work_items is not None:
         _need(work_items, "work_items", torch.int32)
     if tail_start is not None:
         _need(tail_start, "tail_start", torch.int32)
+    if counts is not None:
+        _need(counts, "counts", torch.int32)
+        if counts.numel() < 2:
+            raise ValueError("counts must hold two entries (work items, records)")
     if shared_records is not None:
         _need(shared_records, "shared_records", torch.int32)
         if shared_records.dim() != 2 or shared_records.shape[1] != PA_SHARE_RECORD_WORDS:
@@ -69,7 +73,8 @@ def _decode_opts(heads_per_cta, stages, phases, seq_order, work_items, shared_re
                           None if shared_records is None else shared_records.data_ptr(),
                           0 if shared_records is None else int(shared_records.shape[0]),
                           int(bool(early_inputs)),
-                          None if tail_start is None else tail_start.data_ptr())
+                          None if tail_start is None else tail_start.data_ptr(),
+                          None if counts is None else counts.data_ptr())
 
 
 def _host_int32(values, name: str) -> "np.ndarray":
@@ -346,6 +351,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                       work_items: Optional[torch.Tensor] = None,
                       shared_records: Optional[torch.Tensor] = None,
                       early_inputs: bool = False, tail_start: Optional[torch.Tensor] = None,
+                      counts: Optional[torch.Tensor] = None,
                       stream=None) -> torch.Tensor:
     """q [N,H,D]; caches [B,H,bs,D]; block_tables int32 [N,MB]; seq_lens int32 [N];
     seq_order: optional int32 [N] scheduling permutation on the device; work_items:
@@ -353,7 +359,10 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     optional int32 [r, PA_SHARE_RECORD_WORDS] shared partitions on the device
     (share_plan builds both); early_inputs: the kernel before the call on the stream
     writes none of the read-only inputs (pa_decode_opts.early_inputs); tail_start:
-    optional int32 [N] on the device, with prefix records (share_plan_prefix)."""
+    optional int32 [N] on the device, with prefix records (share_plan_prefix);
+    counts: optional int32 [2] on the device, the numbers of work items and records
+    to run out of the lists given (then capacities), for CUDA-graph replays with
+    lists of varying length."""
     N, H, D = q.shape
     B, _, bs, _ = k_cache.shape
     MB = block_tables.shape[1]
@@ -371,7 +380,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records, early_inputs, tail_start)
+                        shared_records, early_inputs, tail_start, counts)
     st = load_library().paged_attn_decode_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens), N, H, D, bs,
         MB, B, float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], partition_tokens,
@@ -392,6 +401,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
                              shared_records: Optional[torch.Tensor] = None,
                              early_inputs: bool = False,
                              tail_start: Optional[torch.Tensor] = None,
+                             counts: Optional[torch.Tensor] = None,
                              stream=None) -> torch.Tensor:
     """Append each sequence's last token (new_k/new_v [N,H,D]) into its slot and
     decode over all seq_lens[i] tokens, in one pass."""
@@ -413,7 +423,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     opts = _decode_opts(heads_per_cta, stages, phases, seq_order, work_items,
-                        shared_records, early_inputs, tail_start)
+                        shared_records, early_inputs, tail_start, counts)
     st = load_library().paged_attn_decode_append(
         _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         _ptr(seq_lens), N, H, D, bs, MB, B, float(scale), _DTYPE[q.dtype], _ptr(out),

@@ -80,6 +80,7 @@ struct DecodeParams {
   const int32_t* tail_start;  // optional [N]: where a sequence's own part of a split partition begins
   float* ws_tail_acc;         // [N * H][D] and [N * H]: the partials of those parts
   float2* ws_tail_ml;
+  const int32_t* item_count;  // optional: the work items to run (num_work_items: capacity)
 };
 
 // Reduce each of N = TPR/2 partial dot products over the TPR lanes of a row
@@ -155,6 +156,19 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int part = blockIdx.y, seq = blockIdx.z;
   if (p.work_items != nullptr) {
+    if (p.item_count != nullptr) {  // a launch sized for the list's capacity
+      const int n = __ldg(p.item_count);
+      if (n < 0 || n > p.num_work_items) {
+        if (threadIdx.x == 0 && hg == 0 && blockIdx.y == 0)
+          report_error(p.err, PA_ERR_BAD_SEQ_LEN, -1, n);
+        wait_prerequisite();
+        return;
+      }
+      if (static_cast<int>(blockIdx.y) >= n) {
+        wait_prerequisite();
+        return;
+      }
+    }
     const int item = __ldg(p.work_items + blockIdx.y);
     if (item < 0 || item / p.num_partitions >= p.num_seqs) {
       if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, item);

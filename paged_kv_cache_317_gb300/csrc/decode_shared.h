@@ -17,6 +17,7 @@ struct SharedParams {
   const int32_t* records;    // [num_records][PA_SHARE_RECORD_WORDS]
   const int32_t* tail_start; // [N] or null: where a member's own part of a prefix
                              // record's partition begins
+  const int32_t* record_count;  // optional: the records to run (num_records: capacity)
   int num_records;
   int num_seqs;
   int num_heads;

@@ -319,6 +319,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
   p.q = q;
   p.seq_order = opts ? opts->seq_order : nullptr;
   p.early_inputs = (opts && opts->early_inputs) ? 1 : 0;
+  p.item_count = opts ? opts->counts : nullptr;
   p.work_items = opts ? opts->work_items : nullptr;
   p.num_work_items = p.work_items ? opts->num_work_items : 0;
   if (p.work_items && (p.num_work_items < 0 || p.num_work_items > 65535))
@@ -371,6 +372,7 @@ int decode_common(const void* q, const void* new_k, const void* new_v, const voi
     sp.seq_lens = seq_lens;
     sp.records = opts->shared_records;
     sp.tail_start = tail_start;
+    sp.record_count = opts->counts ? opts->counts + 1 : nullptr;
     sp.num_records = opts->num_shared;
     sp.num_seqs = num_seqs;
     sp.num_heads = num_heads;

@@ -155,6 +155,15 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   const int S = p.stages;
   const int hg = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.record_count != nullptr) {  // a launch sized for the list's capacity
+    const int n = __ldg(p.record_count);
+    if (n < 0 || n > p.num_records) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+        report_error(p.err, PA_ERR_BAD_SEQ_LEN, -2, n);
+      return;
+    }
+    if (static_cast<int>(blockIdx.y) >= n) return;
+  }
   const int32_t* rec = p.records + static_cast<size_t>(blockIdx.y) * kRecord;
 
   // Check the record (every thread reaches the same conclusion): partition in

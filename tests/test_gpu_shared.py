@@ -423,3 +423,79 @@ def test_prefix_record_and_tail_start_that_disagree_report_an_error(B):
     out = fam.decode(tables, lens, 128, items, recs, tails=tails)
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, "after the bad calls")
+
+
+def test_device_counts_let_one_graph_run_plans_of_any_length(B):
+    """counts (device int32 [2]) with capacity-sized lists: one captured decode
+    replays plans with different numbers of work items and records (prefix plan,
+    whole-partition plan, plain work list), each matching the oracle."""
+    fam = Families(B, 57, prompts=[800, 450, 1200], members=6, tail_max=120, H=4, D=128,
+                   bs=16, dtype="bf16", fused=False)
+    tables, lens = fam.tables()
+    pt, N, RW = 128, len(lens), B.PA_SHARE_RECORD_WORDS
+    P = -(-tables.shape[1] * 16 // pt)
+    it_d = torch.full((N * P,), -7, dtype=torch.int32, device="cuda")    # junk past the count
+    rc_d = torch.full((N * P // 2, RW), -7, dtype=torch.int32, device="cuda")
+    ts_d = torch.full((N,), -1, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(2, dtype=torch.int32, device="cuda")
+    bt, sl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    out = torch.empty((N, 4, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.paged_attn_workspace_size(N, 4, 128, 16, tables.shape[1], pt, tails=True),
+                     dtype=torch.uint8, device="cuda")
+    plain = B.partition_work_items(lens, pt, tables.shape[1], 16)
+    plans = [B.share_plan_prefix(tables, lens, pt, 16, fused_append=False),
+             (*B.share_plan(tables, lens, pt, 16, fused_append=False), np.full(N, -1, np.int32)),
+             (plain, np.empty((0, RW), np.int32), np.full(N, -1, np.int32))]
+    assert len({len(p[0]) for p in plans}) == 2 and len({len(p[1]) for p in plans}) == 3
+
+    def load(items, recs, tails):
+        it_d[:len(items)] = torch.from_numpy(items)
+        if len(recs):
+            rc_d[:len(recs)] = torch.from_numpy(recs)
+        ts_d.copy_(torch.from_numpy(tails))
+        cnt.copy_(torch.tensor([len(items), len(recs)], dtype=torch.int32))
+
+    step = lambda: B.paged_attn_decode(fam.q, fam.kc, fam.vc, bt, sl, fam.scale, out=out,
+                                       partition_tokens=pt, workspace=ws, work_items=it_d,
+                                       shared_records=rc_d, tail_start=ts_d, counts=cnt,
+                                       error_record=fam.rec)
+    load(*plans[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for k, plan in enumerate(plans + plans[::-1]):
+        load(*plan)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert B.pa_error_read(fam.rec) == [0, 0, 0, 0], k
+        fam.check(out, lens, f"graph replay, plan {k}")
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_device_count_above_capacity_is_recorded(B, which):
+    fam = Families(B, 58, prompts=[600], members=3, tail_max=50, H=4, D=128, bs=16,
+                   dtype="f16", fused=False)
+    tables, lens = fam.tables()
+    items, recs = B.share_plan(tables, lens, 128, 16, fused_append=False)
+    assert len(recs) >= 1
+    n = [len(items), len(recs)]
+    n[which] += 1
+    B.pa_error_clear(fam.rec)
+    B.paged_attn_decode(fam.q, fam.kc, fam.vc, torch.from_numpy(tables).cuda(),
+                        torch.from_numpy(lens).cuda(), fam.scale, partition_tokens=128,
+                        work_items=torch.from_numpy(items).cuda(),
+                        shared_records=torch.from_numpy(recs).cuda(),
+                        counts=torch.tensor(n, dtype=torch.int32, device="cuda"),
+                        error_record=fam.rec)
+    torch.cuda.synchronize()
+    code, _, index, value = B.pa_error_read(fam.rec)
+    assert B.STATUS[code] == "PA_ERR_BAD_SEQ_LEN" and index == -1 - which
+    assert value == n[which]
+    B.pa_error_clear(fam.rec)
