@@ -55,7 +55,9 @@
 extern "C" {
 #endif
 
-#define PAGEDKV_VERSION 2
+/* 3: pa_decode_opts gained early_inputs, tail_start and counts (appended), so a
+ * caller built against version 2 passes a shorter struct and must be rebuilt. */
+#define PAGEDKV_VERSION 3
 #define PA_ERROR_RECORD_WORDS 4
 #define PA_SHARE_MAX_MEMBERS 8
 #define PA_SHARE_RECORD_WORDS (2 + PA_SHARE_MAX_MEMBERS)

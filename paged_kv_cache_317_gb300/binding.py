@@ -43,6 +43,7 @@ class pa_decode_opts(ctypes.Structure):
                 ("tail_start", c_void_p), ("counts", c_void_p)]
 
 
+ABI_VERSION = 3             # PAGEDKV_VERSION of include/pagedkv.h
 PA_SHARE_MAX_MEMBERS = 8
 PA_SHARE_RECORD_WORDS = 2 + PA_SHARE_MAX_MEMBERS
 
@@ -286,6 +287,9 @@ def load_library() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
+        if lib.pa_version() != ABI_VERSION:   # the option structs below match this version
+            raise RuntimeError(f"{_build.LIB_PATH} is version {lib.pa_version()}, the "
+                               f"binding expects {ABI_VERSION}: rebuild it")
         _LIB = lib
     return _LIB
 

@@ -63,6 +63,10 @@ std::vector<__half> random_rows(Lcg& g, int rows) {
 
 int main() {
   std::printf("libpagedkv version %d\n", pa_version());
+  if (pa_version() != PAGEDKV_VERSION) {   // the option structs differ between versions
+    std::fprintf(stderr, "built against version %d\n", PAGEDKV_VERSION);
+    return 1;
+  }
   pa_allocator* alloc = pa_alloc_create(kBlocks, kBlock, nullptr);
   if (!alloc) return 1;
 
@@ -246,6 +250,74 @@ int main() {
     return 1;
   }
 
+  // Prefix records with 64-token partitions (pa_decode_share_plan_ex): the first
+  // two 16-token chunks of the partition, which sequence 0 and its fork share,
+  // are read once for both; each reads its own tokens from tail_start on, and the
+  // merge adds the two parts.  The lists' lengths are given on the device
+  // (pa_decode_opts.counts), as a call replayed from a CUDA graph would.
+  const int pt3 = 64;
+  int32_t n_items3 = 0, n_recs3 = 0;
+  std::vector<int32_t> tails(3, 0);
+  CHECK(pa_decode_share_plan_ex(tables.data(), lens.data(), 3, kMaxBlocks, kBlock, pt3, 0,
+                                nullptr, 1, nullptr, 0, &n_items3, nullptr, 0, &n_recs3,
+                                nullptr));
+  std::vector<int32_t> items3(n_items3),
+      recs3(static_cast<size_t>(n_recs3) * PA_SHARE_RECORD_WORDS);
+  CHECK(pa_decode_share_plan_ex(tables.data(), lens.data(), 3, kMaxBlocks, kBlock, pt3, 0,
+                                nullptr, 1, items3.data(), n_items3, &n_items3, recs3.data(),
+                                n_recs3, &n_recs3, tails.data()));
+  if (n_recs3 != 1 || recs3[1] != 2 + 256 * 2 || tails[0] != 32 || tails[1] != 32 ||
+      tails[2] != -1) {
+    std::fprintf(stderr, "expected one prefix record of 2 members over 2 chunks, got %d\n",
+                 n_recs3);
+    return 1;
+  }
+  const int32_t counts3[2] = {n_items3, n_recs3};
+  int32_t *items3_d = nullptr, *recs3_d = nullptr, *tails_d = nullptr, *counts3_d = nullptr;
+  CUDA(cudaMalloc(&items3_d, items3.size() * sizeof(int32_t)));
+  CUDA(cudaMalloc(&recs3_d, recs3.size() * sizeof(int32_t)));
+  CUDA(cudaMalloc(&tails_d, tails.size() * sizeof(int32_t)));
+  CUDA(cudaMalloc(&counts3_d, sizeof(counts3)));
+  CUDA(cudaMemcpy(items3_d, items3.data(), items3.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(recs3_d, recs3.data(), recs3.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(tails_d, tails.data(), tails.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
+  CUDA(cudaMemcpy(counts3_d, counts3, sizeof(counts3), cudaMemcpyHostToDevice));
+  pa_decode_opts opts3{};
+  opts3.work_items = items3_d;
+  opts3.num_work_items = n_items3;
+  opts3.shared_records = recs3_d;
+  opts3.num_shared = n_recs3;
+  opts3.tail_start = tails_d;
+  opts3.counts = counts3_d;
+  const size_t ws3 = paged_attn_workspace_size_tails(3, kHeads, kDim, kBlock, kMaxBlocks, pt3);
+  void* workspace3 = nullptr;
+  float* out3 = nullptr;
+  CUDA(cudaMalloc(&workspace3, ws3));
+  CUDA(cudaMalloc(&out3, o.size() * sizeof(float)));
+  CHECK(paged_attn_decode_ex(q, kc, vc, tables_d, lens_d, 3, kHeads, kDim, kBlock, kMaxBlocks,
+                             kBlocks, 1.0f / 11.3137085f, PA_F16, out3, PA_F32, pt3, workspace3,
+                             ws3, rec, nullptr, &opts3));
+  CUDA(cudaDeviceSynchronize());
+  CHECK(pa_error_read(rec, err, nullptr));
+  if (err[0] != 0) {
+    std::fprintf(stderr, "device error record (prefix records): %d %d %d %d\n", err[0], err[1],
+                 err[2], err[3]);
+    return 1;
+  }
+  std::vector<float> o3(3 * row);
+  CUDA(cudaMemcpy(o3.data(), out3, o3.size() * sizeof(float), cudaMemcpyDeviceToHost));
+  if (std::memcmp(o3.data(), o3.data() + row, row * sizeof(float)) != 0 ||
+      std::memcmp(o3.data() + 2 * row, o.data() + 2 * row, row * sizeof(float)) != 0) {
+    std::fprintf(stderr, "prefix records: fork or one-token sequence changed\n");
+    return 1;
+  }
+  float worst3 = 0.f;
+  for (size_t i = 0; i < o.size(); ++i) worst3 = std::max(worst3, std::fabs(o3[i] - o[i]));
+  if (!(worst3 <= 2e-3f)) {
+    std::fprintf(stderr, "prefix records: output moved by %g from the first decode\n", worst3);
+    return 1;
+  }
+
   // Chunked prefill on the tensor cores over the same cache: the last 5 tokens
   // of sequence 0 and of its fork as causal queries (the same 5 query rows for
   // both, the last one the decode's query), and sequence 2's one token with the
@@ -302,11 +374,14 @@ int main() {
                   static_cast<void*>(items_d), workspace, static_cast<void*>(items2_d),
                   static_cast<void*>(recs_d), workspace2, static_cast<void*>(out2),
                   static_cast<void*>(qp_d), static_cast<void*>(qstart_d),
-                  static_cast<void*>(outp)})
+                  static_cast<void*>(outp), static_cast<void*>(items3_d),
+                  static_cast<void*>(recs3_d), static_cast<void*>(tails_d),
+                  static_cast<void*>(counts3_d), workspace3, static_cast<void*>(out3)})
     if (p) cudaFree(p);
   std::printf("ok: fork decodes like its parent (one copy-on-write), one-token sequence exact; "
               "%d-token partitions, %d work items; shared blocks read once: %d records, fork "
-              "still exact, max change %.2e; prefill: fork exact, within %.2e of the decode\n",
-              pt, n_items, n_recs, worst, worst_p);
+              "still exact, max change %.2e; prefix records: %d record over 2 chunks, fork "
+              "exact, max change %.2e; prefill: fork exact, within %.2e of the decode\n",
+              pt, n_items, n_recs, worst, n_recs3, worst3, worst_p);
   return 0;
 }

@@ -42,7 +42,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     from paged_kv_cache_317_gb300.binding import STATUS
-    assert lib.pa_version() == 2
+    assert lib.pa_version() == 3
+    import re
+    from paged_kv_cache_317_gb300 import binding
+    hdr = open(os.path.join(HEADER_DIR, "pagedkv.h")).read()
+    assert int(re.search(r"#define PAGEDKV_VERSION (\d+)", hdr).group(1)) == binding.ABI_VERSION == 3
     for code in STATUS:
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(999) == b"unknown status"

@@ -39,4 +39,5 @@ def test_c_example_runs(lib, tmp_path):
     m = re.search(r"(\d+)-token partitions, (\d+) work items", r.stdout)
     assert m and int(m.group(1)) <= 64 and int(m.group(2)) > 3   # the split path, work list
     assert "2 records" in r.stdout                  # the shared-partition pass ran
+    assert "prefix records: 1 record" in r.stdout   # prefix record, tail item, device counts
     assert "prefill: fork exact" in r.stdout        # the tensor-core prefill ran
