@@ -176,6 +176,21 @@ def test_merged_partitions_equal_unsplit_attention(part):
                                rtol=0, atol=1e-12)
 
 
+def test_merge_of_uneven_pieces_equals_unsplit_attention():
+    """The split a prefix record makes (a partition's shared first chunks, then
+    each member's own rest, merged as two partials alongside the other
+    partitions) is a regrouping of the same sum: partials over any cut of the
+    tokens into consecutive pieces merge to the unsplit attention."""
+    rng = np.random.default_rng(17)
+    L, H, D = 300, 2, 16
+    q, k, v = rng.standard_normal((H, D)), rng.standard_normal((L, H, D)), rng.standard_normal((L, H, D))
+    for cuts in ([0, 128, 176, 256, 300], [0, 16, 300], [0, 299, 300], [0, 1, 2, 3, 300]):
+        parts = [A.partition_partials(q, k[a:b], v[a:b], 0.7, b - a) for a, b in zip(cuts, cuts[1:])]
+        m, l, acc = (np.concatenate([x[i] for x in parts]) for i in range(3))
+        np.testing.assert_allclose(A.merge_partials(m, l, acc), A.attention(q, k, v, 0.7),
+                                   rtol=0, atol=1e-12)
+
+
 def test_single_partition_partials_normalise_to_attention():
     rng = np.random.default_rng(5)
     q, k, v = rng.standard_normal((2, 8)), rng.standard_normal((30, 2, 8)), rng.standard_normal((30, 2, 8))
