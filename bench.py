@@ -687,7 +687,8 @@ class _Staging:
         """Write the pairs (pad: and -1 pairs up to the capacity) and the counts
         into set step % 2 (its other regions filled through views(step)) and
         enqueue its upload; returns device views (pairs int64 [n, 2], tables,
-        lengths, work list, records, tail starts or None)."""
+        lengths, work list, records, tail starts or None), or None with pad (a
+        captured step reads the capacity views)."""
         import numpy as np
         import torch
         j = step % 2
@@ -702,6 +703,8 @@ class _Staging:
         d = self.dev[j]
         d[:used].copy_(self.host[j][:used], non_blocking=True)
         self.done[j].record(stream)
+        if pad:
+            return None
         return (d[o["pairs"]:o["pairs"] + 4 * n_p].view(torch.int64).view(n_p, 2),
                 d[o["bt"]:o["bt"] + self.n_seqs * self.max_blocks].view(self.n_seqs,
                                                                       self.max_blocks),
@@ -1172,9 +1175,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
             evs = split[s_]
             evs[0].record(stream)
             h1 = time.perf_counter()
-            pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
-                s_, stream, pairs, len(items), len(recs), tails is not None,
-                pad=graphs is not None)
+            staged = staging.upload(s_, stream, pairs, len(items), len(recs), tails is not None,
+                                    pad=graphs is not None)
             stage_s += time.perf_counter() - h1
             evs[1].record(stream)
             h3 = time.perf_counter()
@@ -1183,6 +1185,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
                 graphs[s_ % 2].replay()
                 h4 = h5 = time.perf_counter()
             else:
+                pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staged
                 if len(pairs):
                     B.block_copy([kc], [vc], pairs_d)
                 h4 = time.perf_counter()
