@@ -499,3 +499,37 @@ def test_device_count_above_capacity_is_recorded(B, which):
     assert B.STATUS[code] == "PA_ERR_BAD_SEQ_LEN" and index == -1 - which
     assert value == n[which]
     B.pa_error_clear(fam.rec)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_device_counts_random_capacities(B, seed):
+    """Work lists and records inside larger buffers, junk past their counts: the
+    decode reads exactly the counted entries (prefix plans, fused or not)."""
+    rng = np.random.default_rng(4100 + seed)
+    fused = bool(seed % 2)
+    fam = Families(B, 4200 + seed, prompts=[int(x) for x in rng.integers(100, 1400, 3)],
+                   members=int(rng.integers(2, 10)), tail_max=int(rng.integers(0, 200)), H=4,
+                   D=int(rng.choice([64, 128])), bs=16, dtype="bf16", fused=fused)
+    tables, lens = fam.tables()
+    pt = int(rng.choice([64, 128, 256]))
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, 16, fused_append=fused)
+    RW = B.PA_SHARE_RECORD_WORDS
+    cap_i, cap_r = len(items) + int(rng.integers(0, 300)), len(recs) + int(rng.integers(1, 60))
+    it_d = torch.full((cap_i,), -7, dtype=torch.int32, device="cuda")
+    rc_d = torch.full((cap_r, RW), -7, dtype=torch.int32, device="cuda")
+    it_d[:len(items)] = torch.from_numpy(items)
+    if len(recs):
+        rc_d[:len(recs)] = torch.from_numpy(recs)
+    cnt = torch.tensor([len(items), len(recs)], dtype=torch.int32, device="cuda")
+    bt, sl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+    kw = dict(partition_tokens=pt, error_record=fam.rec, work_items=it_d, shared_records=rc_d,
+              tail_start=torch.from_numpy(tails).cuda(), counts=cnt)
+    if fused:
+        nr = torch.from_numpy(fam.new_rows).cuda()
+        out = B.paged_attn_decode_append(fam.q, fam.store_k[nr], fam.store_v[nr], fam.kc,
+                                         fam.vc, bt, sl, fam.scale, **kw)
+    else:
+        out = B.paged_attn_decode(fam.q, fam.kc, fam.vc, bt, sl, fam.scale, **kw)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    fam.check(out, lens, f"seed {seed}: counts inside capacities {cap_i} / {cap_r}")
