@@ -533,3 +533,30 @@ def test_device_counts_random_capacities(B, seed):
     torch.cuda.synchronize()
     assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
     fam.check(out, lens, f"seed {seed}: counts inside capacities {cap_i} / {cap_r}")
+
+
+def test_prefix_records_with_the_passes_called_apart(B):
+    """phases=1 then phases=2 (partition passes, then the merge, as two calls on the
+    same workspace) gives the single call's bits: tail rows persist between them."""
+    fam = Families(B, 61, prompts=[700, 1000], members=5, tail_max=90, H=4, D=128, bs=16,
+                   dtype="f16", fused=False)
+    tables, lens = fam.tables()
+    pt = 128
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, 16, fused_append=False)
+    assert (recs[:, 1] >> 8).max() > 0
+    N, MB = tables.shape
+    ws = torch.empty(B.paged_attn_workspace_size(N, 4, 128, 16, MB, pt, tails=True),
+                     dtype=torch.uint8, device="cuda")
+    args = (fam.q, fam.kc, fam.vc, torch.from_numpy(tables).cuda(),
+            torch.from_numpy(lens).cuda(), fam.scale)
+    kw = dict(partition_tokens=pt, workspace=ws, work_items=torch.from_numpy(items).cuda(),
+              shared_records=torch.from_numpy(recs).cuda(),
+              tail_start=torch.from_numpy(tails).cuda(), error_record=fam.rec)
+    whole = B.paged_attn_decode(*args, **kw).clone()
+    out = torch.full_like(whole, float("nan"))
+    B.paged_attn_decode(*args, out=out, phases=1, **kw)
+    B.paged_attn_decode(*args, out=out, phases=2, **kw)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(fam.rec) == [0, 0, 0, 0]
+    assert torch.equal(out, whole)
+    fam.check(out, lens, "passes called apart")
