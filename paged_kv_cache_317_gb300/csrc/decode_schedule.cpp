@@ -291,31 +291,33 @@ extern "C" int pa_decode_share_plan_ex(const int32_t* block_tables, const int32_
     for (size_t a = 0; a < keyed.size();) {
       size_t e = a + 1;
       while (e < keyed.size() && key_block(keyed[e]) == key_block(keyed[a])) ++e;
-      // whole records: split the run into groups of identical slices (members
-      // in index order)
+      // whole records: the run's members sorted by their slice of the table
+      // (then by index), so that identical slices are adjacent, each group in
+      // index order; one sort, whatever the number of distinct slices
       run.clear();
       for (size_t k = a; k < e; ++k)
         if (whole_ok(key_seq(keyed[k]))) run.push_back(key_seq(keyed[k]));
-      while (run.size() >= 2) {
-        const int32_t* ref = row(run[0]) + b0;
-        group.clear();
-        size_t keep = 0;
-        for (size_t k = 0; k < run.size(); ++k) {
-          if (k == 0 || std::memcmp(row(run[k]) + b0, ref, n * sizeof(int32_t)) == 0)
-            group.push_back(run[k]);
-          else
-            run[keep++] = run[k];
-        }
-        run.resize(keep);
+      const auto slice_cmp = [&](int32_t x, int32_t y) {
+        return std::memcmp(row(x) + b0, row(y) + b0, n * sizeof(int32_t));
+      };
+      if (run.size() >= 2)
+        std::sort(run.begin(), run.end(), [&](int32_t x, int32_t y) {
+          const int c = slice_cmp(x, y);
+          return c != 0 ? c < 0 : x < y;
+        });
+      for (size_t u = 0; u + 1 < run.size();) {
+        size_t v = u + 1;
+        while (v < run.size() && slice_cmp(run[v], run[u]) == 0) ++v;
         // at most PA_SHARE_MAX_MEMBERS per record; a lone leftover stays private
-        for (size_t at = 0; at + 1 < group.size(); at += PA_SHARE_MAX_MEMBERS) {
-          const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, group.size() - at);
+        for (size_t at = u; at + 1 < v; at += PA_SHARE_MAX_MEMBERS) {
+          const size_t m = std::min<size_t>(PA_SHARE_MAX_MEMBERS, v - at);
           recs.push_back(static_cast<int32_t>(part));
           recs.push_back(static_cast<int32_t>(m));
           for (size_t j = 0; j < PA_SHARE_MAX_MEMBERS; ++j)
-            recs.push_back(j < m ? group[at + j] : -1);
-          for (size_t j = 0; j < m; ++j) covered[first_part[group[at + j]] + part] = 1;
+            recs.push_back(j < m ? run[at + j] : -1);
+          for (size_t j = 0; j < m; ++j) covered[first_part[run[at + j]] + part] = 1;
         }
+        u = v;
       }
       // prefix records over the run's members still in the work list
       group.clear();

@@ -417,3 +417,22 @@ def test_plan_and_tables_fill_caller_buffers_in_place():
         B.share_plan(t, l, pt, bs, out=(it, rc[:, :-1]))
     with pytest.raises(B.PagedKVError):
         B.share_plan(t, l, pt, bs, out=(it[:3], rc))        # too little room
+
+
+def test_share_plan_with_many_distinct_slices_behind_one_first_block():
+    """Many sequences that share only a partition's first block (a short common
+    prompt) and differ after it: no whole records, and the plan takes one sort per
+    partition, not one pass per distinct slice."""
+    import time
+    N, MB, bs, pt = 30000, 64, 16, 512
+    rng = np.random.default_rng(8)
+    tables = rng.permutation(N * MB).astype(np.int32).reshape(N, MB) + 10
+    tables[:, 0] = 3                                   # every table's first block alike
+    lens = np.full(N, MB * bs)
+    t0 = time.perf_counter()
+    items, recs = B.share_plan(tables, lens, pt, bs, fused_append=True)
+    took = time.perf_counter() - t0
+    assert len(recs) == 0 and len(items) == N * (MB * bs // pt)
+    assert took < 0.5, took                        # one pass per slice took seconds
+    items, recs, tails = B.share_plan_prefix(tables, lens, pt, bs, fused_append=True)
+    assert (recs[:, 1] >> 8 == 1).all() and len(recs) == N // 8 and (tails == 16).all()
