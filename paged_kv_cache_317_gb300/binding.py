@@ -181,9 +181,11 @@ def _share_plan(block_tables, seq_lens, partition_tokens, block_size, fused_appe
         recs = np.empty((pairs // 2, PA_SHARE_RECORD_WORDS), dtype=np.int32)
         tails = np.empty(len(lens), dtype=np.int32)
     else:
+        if len(out) not in (2, 3):
+            raise ValueError("out must be (items, records) or (items, records, tail_start)")
         items = _out_buffer(out[0], "items")
         recs = _out_buffer(out[1], "records", (PA_SHARE_RECORD_WORDS,))
-        tails = out[2]
+        tails = out[2] if len(out) == 3 else None
         if tails is None:
             tails = np.empty(len(lens), dtype=np.int32)
         elif _out_buffer(tails, "tail_start").shape[0] != len(lens):
