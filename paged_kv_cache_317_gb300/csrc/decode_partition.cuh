@@ -112,6 +112,16 @@ __device__ __forceinline__ void wait_prerequisite() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// A block's last step.  As the call's first kernel the pass waits for its
+// prerequisite in every block (no block may finish before the kernel before the
+// call has).  Behind the shared-partition pass, whose blocks all waited for the
+// kernel before the call before this pass could start, only the first block waits
+// for that pass, so that this grid (and so the merge after it) completes after
+// both; the other blocks free their slots as soon as their work is done.
+__device__ __forceinline__ void finish(const DecodeParams& p) {
+  if (p.wait_first || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) wait_prerequisite();
+}
+
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int seq, bool report) {
   int L = p.seq_lens[seq];
   const int cap = p.max_blocks * p.block_size;
@@ -161,18 +171,18 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
       if (n < 0 || n > p.num_work_items) {
         if (threadIdx.x == 0 && hg == 0 && blockIdx.y == 0)
           report_error(p.err, PA_ERR_BAD_SEQ_LEN, -1, n);
-        wait_prerequisite();
+        finish(p);
         return;
       }
       if (static_cast<int>(blockIdx.y) >= n) {
-        wait_prerequisite();
+        finish(p);
         return;
       }
     }
     const int item = __ldg(p.work_items + blockIdx.y);
     if (item < 0 || item / p.num_partitions >= p.num_seqs) {
       if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.y, item);
-      wait_prerequisite();
+      finish(p);
       return;
     }
     seq = item / p.num_partitions;
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     if (static_cast<unsigned>(seq) >= static_cast<unsigned>(p.num_seqs)) {
       if (threadIdx.x == 0 && hg == 0 && part == 0)
         report_error(p.err, PA_ERR_BAD_SEQ_LEN, blockIdx.z, seq);
-      wait_prerequisite();
+      finish(p);
       return;
     }
   }
@@ -190,7 +200,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
   const int L = clamp_len(p, seq, threadIdx.x == 0 && hg == 0 && part == 0);
   const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
   if (part >= nparts) {
-    wait_prerequisite();
+    finish(p);
     return;
   }
   int tok_begin = part * p.partition_tokens;
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
     if (ts >= 0 && ts / p.partition_tokens == part) {
       if (ts <= tok_begin || ts >= tok_end || ts % kChunk != 0) {
         if (threadIdx.x == 0 && hg == 0) report_error(p.err, PA_ERR_BAD_SEQ_LEN, seq, ts);
-        wait_prerequisite();
+        finish(p);
         return;
       }
       tok_begin = ts;
@@ -469,7 +479,7 @@ __global__ void __launch_bounds__((kMaxHeadsPerCta + 1) * 32)
       mbar_wait_bounded(&full[s], (last / S) & 1);
     }
   }
-  wait_prerequisite();
+  finish(p);
 }
 
 }  // namespace

@@ -183,9 +183,9 @@ int launch(const DecodeParams& p, int num_seqs, int phases, size_t smem,
     // equal length, and trigger their dependents when they start.  The
     // per-sequence partition pass follows as a programmatic dependent, so its
     // blocks (longest first, then ever shorter) fill the SMs the shared pass's
-    // last wave leaves idle.  The two write disjoint partials; each block of the
-    // second pass waits for the first to complete before it exits, so the merge
-    // after it follows both.
+    // last wave leaves idle.  The two write disjoint partials; the first block of
+    // the second pass waits for the first pass to complete before it exits, so
+    // the merge after it follows both.
     if (shared != nullptr) {
       const int st = launch_shared_partitions(*shared, dtype, D, stream);
       if (st != PA_OK) return st;

@@ -147,8 +147,8 @@ __global__ void __launch_bounds__((kMaxG + 1) * 32, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // The per-sequence partition pass follows as a programmatic dependent (it
   // reads nothing this pass writes): let it start once every block here has
-  // (and so only after the wait above).  Its blocks wait for this pass to
-  // complete before they exit, so the merge after it follows both.
+  // (and so only after the wait above).  Its first block waits for this pass to
+  // complete before it exits, so the merge after it follows both.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = p.heads_per_cta;
