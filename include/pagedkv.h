@@ -225,7 +225,8 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  with lists of other lengths written into the same buffers
  *                  (with the counts).  A count outside [0, capacity] is recorded
  *                  as PA_ERR_BAD_SEQ_LEN (index -1 for the items, -2 for the
- *                  records; value = the count) and that launch computes nothing.
+ *                  records; value = the count), the pass that reads it computes
+ *                  nothing, and `out` is then undefined.
  * With split-K, the partition pass leaves in the workspace, for partition p of
  * sequence i and head h (row = (i * num_heads + h) * P + p, P = ceil(
  * max_blocks_per_seq * block_size / partition_tokens)):
