@@ -216,7 +216,11 @@ int paged_attn_decode(const void* q, const void* k_cache, const void* v_cache,
  *                  the workspace, which the merge adds to the sequence's others.
  *                  The workspace must then hold paged_attn_workspace_size_tails
  *                  bytes.  pa_decode_share_plan_ex builds the records and this
- *                  array together.
+ *                  array together.  An entry t >= 0 that is not a multiple of 16,
+ *                  falls on a partition boundary or lies at or past L is recorded
+ *                  as PA_ERR_BAD_SEQ_LEN (index = sequence, value = t); an entry
+ *                  with no prefix record naming it leaves that sequence's output
+ *                  undefined (its first part is never computed).
  *   counts         NULL, or device int32 [2]: how many of the work_items and of
  *                  the shared_records to run, read by the kernels on the device.
  *                  num_work_items and num_shared are then capacities (the sizes
