@@ -85,6 +85,7 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert call(MB=64) == INV                                 # needs a workspace, none given
     assert call(H=0) == INV
     assert call(scale=float("nan")) == INV
+    assert call(N=65536) == INV                               # more sequences than a call takes
     assert call(N=0) == 0                                     # nothing to do
 
 

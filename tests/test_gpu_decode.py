@@ -315,3 +315,32 @@ def test_bad_block_entry_in_the_second_half_of_a_chunk(B):
     assert r[0] == 4 and r[1] >= 1 and r[2] == 1 and r[3] == b.num_blocks + 7
     assert torch.isfinite(out).all()
     assert_matches_oracle(out[:1], oracle_decode(b, [0]), "unaffected sequence")
+
+
+def test_largest_batch_the_call_takes(B):
+    """65535 sequences (the most one call takes), short ragged lengths with one
+    partition of 16 tokens each, fused append, host schedule (work list): sampled
+    sequences against the oracle, every appended row bit-exact."""
+    rng = np.random.default_rng(65535)
+    lens = rng.integers(1, 41, 65535)
+    b = random_decode_batch(9, lens, 2, 64, 16, dtype="f16", device="cuda", with_append=True,
+                            poison=False)
+    bt, sl = device_tables(b)
+    pt = B.decode_partition_tokens(b.context_lens, 2)
+    items = B.partition_work_items(b.context_lens, pt, b.max_blocks_per_seq, 16)
+    assert len(items) == 65535                   # one item per sequence: the list's limit too
+    rec = B.new_error_record()
+    out = B.paged_attn_decode_append(b.q, b.new_k, b.new_v, b.k_cache, b.v_cache, bt, sl,
+                                     b.scale, out_dtype=torch.float32, partition_tokens=pt,
+                                     work_items=torch.from_numpy(items).cuda(),
+                                     error_record=rec)
+    torch.cuda.synchronize()
+    assert B.pa_error_read(rec) == [0, 0, 0, 0]
+    seqs = sorted(set(rng.choice(65535, 48, replace=False).tolist()) | {0, 65534})
+    assert_matches_oracle(out[seqs], oracle_decode(b, seqs), "65535 sequences")
+    slots = torch.from_numpy(b.slot_mapping).cuda()
+    blk, row = slots // 16, slots % 16
+    assert torch.equal(b.k_cache[blk, :, row], b.new_k) and torch.equal(b.v_cache[blk, :, row], b.new_v)
+    with pytest.raises(B.PagedKVError):                     # one more sequence is refused
+        B.paged_attn_decode(torch.cat([b.q, b.q[:1]]), b.k_cache, b.v_cache,
+                            torch.cat([bt, bt[:1]]), torch.cat([sl, sl[:1]]), b.scale)
