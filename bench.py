@@ -589,7 +589,8 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------- other workloads
 def _time_device(fn, K, W, stream, flush=None):
     """Mean device time of fn() over K calls (after W), in ms.  With `flush`,
-    L2 is flushed before every call and only the calls are timed."""
+    L2 is flushed before every call and only the calls (replayed from a CUDA
+    graph) are timed."""
     import torch
     for _ in range(W):
         fn()
@@ -602,12 +603,25 @@ def _time_device(fn, K, W, stream, flush=None):
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / K
+    # The call is replayed from a CUDA graph between the two events, so that the
+    # host's launch cost (which can exceed a tiny call's device time) cannot leave
+    # the GPU idle inside the timed interval after the flush.
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        fn()
+    torch.cuda.synchronize()
     times = []
     for _ in range(K):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fn()
+        graph.replay()
         b.record(stream)
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
@@ -788,6 +802,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
                             "context_tokens": int(b.context_lens.sum()),
                             "partition_tokens": pt,
                             "schedule": "host-chosen partition length and work list",
+                            "timing": ("each call replayed from a CUDA graph after an L2 flush"
+                                       if flush else "calls back to back between two events"),
                             "l2": "flushed between steps" if flush else "inputs larger than L2"},
                     dtype="f16" if b.dtype == torch.float16 else "bf16")
         tokens = int(b.context_lens.sum())
