@@ -55,6 +55,8 @@ DECODE_SOURCES = ("paged_kv_cache_317_gb300/csrc/decode_partition.cuh",
                   "paged_kv_cache_317_gb300/csrc/decode_config.h",
                   "paged_kv_cache_317_gb300/csrc/common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+# the serving loops' per-step device split is taken on every 4th step
+SPLIT_NOTE = "sampled every 4th step, whose event records add host time"
 
 
 # --------------------------------------------------------------- host logic
@@ -680,6 +682,11 @@ class _Staging:
         self.host = [torch.empty(at, dtype=torch.int32).pin_memory() for _ in range(2)]
         self.host_np = [h.numpy() for h in self.host]
         self.dev = [torch.zeros(at, dtype=torch.int32, device=dev) for _ in range(2)]
+        o = self.off
+        # the regions whose size does not change from step to step, viewed once
+        self.fixed = [(d[o["bt"]:o["bt"] + n_seqs * max_blocks].view(n_seqs, max_blocks),
+                       d[o["sl"]:o["sl"] + n_seqs], d[o["ts"]:o["ts"] + n_seqs])
+                      for d in self.dev]
         for d in self.dev:   # no copy-on-write pairs and no split partitions before an upload
             d[self.off["pairs"]:self.off["pairs"] + self.sizes["pairs"]] = -1
             d[self.off["ts"]:self.off["ts"] + self.sizes["ts"]] = -1
@@ -719,13 +726,11 @@ class _Staging:
         self.done[j].record(stream)
         if pad:
             return None
-        return (d[o["pairs"]:o["pairs"] + 4 * n_p].view(torch.int64).view(n_p, 2),
-                d[o["bt"]:o["bt"] + self.n_seqs * self.max_blocks].view(self.n_seqs,
-                                                                      self.max_blocks),
-                d[o["sl"]:o["sl"] + self.n_seqs],
+        bt, sl, ts = self.fixed[j]
+        return (d[o["pairs"]:o["pairs"] + 4 * n_p].view(torch.int64).view(n_p, 2), bt, sl,
                 d[o["it"]:o["it"] + n_items],
                 d[o["rc"]:o["rc"] + n_recs * self.rw].view(n_recs, self.rw) if n_recs else None,
-                d[o["ts"]:o["ts"] + self.n_seqs] if tails else None)
+                ts if tails else None)
 
     def capacity_views(self, j):
         """Device views of set j over the lists' capacities, for a captured step:
@@ -1012,24 +1017,28 @@ def run_workload(args, rank, world, local_rank, emit=True):
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
             n_prefix += int((recs[:, 1] >> 8 > 0).sum())
-            evs = split[s_]
-            evs[0].record(stream)
+            evs = split[s_] if s_ % 4 == 0 else None   # the split is sampled every 4th step
+            if evs:
+                evs[0].record(stream)
             h1 = time.perf_counter()
             pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
                 s_, stream, pairs, len(items), len(recs), tails is not None)
             stage_s += time.perf_counter() - h1
-            evs[1].record(stream)
+            if evs:
+                evs[1].record(stream)
             h3 = time.perf_counter()
             if len(pairs):
                 B.block_copy([kc], [vc], pairs_d)
             h4 = time.perf_counter()
-            evs[2].record(stream)
+            if evs:
+                evs[2].record(stream)
             h5 = time.perf_counter()
             B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                        partition_tokens=pt, workspace=ws, error_record=rec,
                                        work_items=it_d, shared_records=rc_d, tail_start=ts_d)
             launch_s += time.perf_counter() - h5 + h4 - h3
-            evs[3].record(stream)
+            if evs:
+                evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
@@ -1049,7 +1058,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         torch.cuda.synchronize()
         if not torch.equal(ref_out, out):
             raise RuntimeError("staged and direct inputs gave different outputs")
-        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
+        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split[::4]), 5)
         tokens = lens_seen / plan.steps
         total = tokens * plan.num_heads * plan.head_dim * 4
         value = total / (ms * 1e-3) / 1e9
@@ -1074,7 +1083,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     device_ms_per_step_split={
                         "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
                         "append_and_decode": seg(2, 3),
-                        "note": "the append is fused into the decode launch"},
+                        "note": "the append is fused into the decode launch; " + SPLIT_NOTE},
                     note="value counts K/V bytes only; device time includes copies, H2D "
                          "of tables (staged in pinned memory, two buffer sets) and the decode")
     elif w == "beam":
@@ -1188,13 +1197,15 @@ def run_workload(args, rank, world, local_rank, emit=True):
             plan_s += time.perf_counter() - h2
             n_shared += len(recs)
             n_prefix += int((recs[:, 1] >> 8 > 0).sum())
-            evs = split[s_]
-            evs[0].record(stream)
+            evs = split[s_] if s_ % 4 == 0 else None   # the split is sampled every 4th step
+            if evs:
+                evs[0].record(stream)
             h1 = time.perf_counter()
             staged = staging.upload(s_, stream, pairs, len(items), len(recs), tails is not None,
                                     pad=graphs is not None)
             stage_s += time.perf_counter() - h1
-            evs[1].record(stream)
+            if evs:
+                evs[1].record(stream)
             h3 = time.perf_counter()
             if graphs is not None:
                 qkv.copy_(tok_stack[s_])
@@ -1205,14 +1216,16 @@ def run_workload(args, rank, world, local_rank, emit=True):
                 if len(pairs):
                     B.block_copy([kc], [vc], pairs_d)
                 h4 = time.perf_counter()
-                evs[2].record(stream)
+                if evs:
+                    evs[2].record(stream)
                 h5 = time.perf_counter()
                 B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
                                            partition_tokens=pt, workspace=ws, error_record=rec,
                                            work_items=it_d, shared_records=rc_d,
                                            tail_start=ts_d)
             launch_s += time.perf_counter() - h5 + h4 - h3
-            evs[3].record(stream)
+            if evs:
+                evs[3].record(stream)
         ev1 = torch.cuda.Event(enable_timing=True)
         ev1.record(stream)
         torch.cuda.synchronize()
@@ -1234,7 +1247,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
         torch.cuda.synchronize()
         if not torch.equal(ref_out, out):
             raise RuntimeError("staged and direct inputs gave different outputs")
-        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split), 5)
+        seg = lambda a, c: round(statistics.mean(e[a].elapsed_time(e[c]) for e in split[::4]), 5)
         tokens = lens_seen / plan.steps
         total = tokens * H * D * 4
         value = total / (ms * 1e-3) / 1e9
@@ -1264,11 +1277,12 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     copies_per_step=round(copies / plan.steps, 2),
                     device_ms_per_step_split=(
                         {"table_uploads": seg(0, 1), "copies_append_and_decode": seg(1, 3),
-                         "note": "one graph: copies, then the append fused into the decode"}
+                         "note": "one graph: copies, then the append fused into the decode; "
+                                 + SPLIT_NOTE}
                         if graphs is not None else
                         {"table_uploads": seg(0, 1), "block_copy": seg(1, 2),
                          "append_and_decode": seg(2, 3),
-                         "note": "the append is fused into the decode launch"}),
+                         "note": "the append is fused into the decode launch; " + SPLIT_NOTE}),
                     note="value counts logical K/V bytes (beams share prefix blocks, so part "
                          "of them is served from L2)")
     elif w in ("append", "copy"):
