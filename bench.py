@@ -732,18 +732,16 @@ class _Staging:
                 d[o["rc"]:o["rc"] + n_recs * self.rw].view(n_recs, self.rw) if n_recs else None,
                 ts if tails else None)
 
-    def capacity_views(self, j):
-        """Device views of set j over the lists' capacities, for a captured step:
-        pairs int64 [n_seqs, 2], tables, lengths, work list, records (half the
-        work list's capacity: a record holds at least two pairs), tail starts,
-        counts."""
+    def capacity_views(self, j, n_items_cap, n_recs_cap):
+        """Device views of set j for a captured step: pairs int64 [n_seqs, 2],
+        tables, lengths, the first n_items_cap work-list entries and n_recs_cap
+        records (the launches' sizes), tail starts, counts."""
         import torch
         d, o, n = self.dev[j], self.off, self.n_seqs
-        n_it = self.sizes["it"]
         return (d[o["pairs"]:o["pairs"] + 4 * n].view(torch.int64).view(n, 2),
                 d[o["bt"]:o["bt"] + n * self.max_blocks].view(n, self.max_blocks),
-                d[o["sl"]:o["sl"] + n], d[o["it"]:o["it"] + n_it],
-                d[o["rc"]:o["rc"] + (n_it // 2) * self.rw].view(n_it // 2, self.rw),
+                d[o["sl"]:o["sl"] + n], d[o["it"]:o["it"] + n_items_cap],
+                d[o["rc"]:o["rc"] + n_recs_cap * self.rw].view(n_recs_cap, self.rw),
                 d[o["ts"]:o["ts"] + n], d[o["cnt"]:o["cnt"] + 2])
 
 
@@ -1126,13 +1124,16 @@ def run_workload(args, rank, world, local_rank, emit=True):
         graphs = None
         if not args.no_graph:
             # the device step (copy-on-write copies, fused append + decode) captured
-            # once per staging set over the lists' capacities; each step writes its
-            # lists and their counts into the set and replays the set's graph
+            # once per staging set, its launches sized for 2 N work items and N
+            # records (blocks past the counts exit at once, but each costs a little);
+            # each step writes its lists and their counts into the set and replays the
+            # set's graph, or launches eagerly when its plan does not fit
+            cap_items, cap_recs = 2 * N, N
             qkv = torch.empty((3, N, H, D), dtype=plan.dtype, device=dev)
             tok_stack = torch.stack([torch.stack(t) for t in tokens_all])
             graphs = []
             for j in range(2):
-                pc, btj, slj, itj, rcj, tsj, cj = staging.capacity_views(j)
+                pc, btj, slj, itj, rcj, tsj, cj = staging.capacity_views(j, cap_items, cap_recs)
 
                 def device_step(pc=pc, btj=btj, slj=slj, itj=itj, rcj=rcj, tsj=tsj, cj=cj):
                     B.block_copy([kc], [vc], pc)
@@ -1153,7 +1154,7 @@ def run_workload(args, rank, world, local_rank, emit=True):
                 graphs.append(g)
             torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, copies, n_shared = 0.0, 0.0, 0.0, 0, 0, 0
-        n_prefix, launch_s = 0, 0.0
+        n_prefix, launch_s, n_eager = 0, 0.0, 0
         unique_seen = 0
         split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
                  for _ in range(plan.steps)]
@@ -1201,13 +1202,16 @@ def run_workload(args, rank, world, local_rank, emit=True):
             if evs:
                 evs[0].record(stream)
             h1 = time.perf_counter()
+            captured = (graphs is not None and len(items) <= cap_items
+                        and len(recs) <= cap_recs)
+            n_eager += 0 if captured else 1
             staged = staging.upload(s_, stream, pairs, len(items), len(recs), tails is not None,
-                                    pad=graphs is not None)
+                                    pad=captured)
             stage_s += time.perf_counter() - h1
             if evs:
                 evs[1].record(stream)
             h3 = time.perf_counter()
-            if graphs is not None:
+            if captured:
                 qkv.copy_(tok_stack[s_])
                 graphs[s_ % 2].replay()
                 h4 = h5 = time.perf_counter()
@@ -1263,7 +1267,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
                                          f"records per step, {n_prefix / plan.steps:.1f} "
                                          "of them prefix records) + work list"),
                             "device_step": ("copies + fused append and decode replayed from "
-                                            "a CUDA graph (lists sized by device-side counts)"
+                                            "a CUDA graph (lists sized by device-side counts; "
+                                            f"{n_eager} of {plan.steps} steps launched eagerly "
+                                            "for want of room)"
                                             if graphs is not None else "eager launches"),
                             "l2": "inputs larger than L2"},
                     dtype="bf16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
