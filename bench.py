@@ -968,8 +968,37 @@ def run_workload(args, rank, world, local_rank, emit=True):
         n_items_max = N * int(-(-max_blocks * bs // pt))
         RW = B.PA_SHARE_RECORD_WORDS
         staging = _Staging(N, max_blocks, n_items_max, RW, dev)
+        graphs = None
+        if not args.no_graph:
+            # the device step captured once per staging set, as in the beam loop, its
+            # launches sized for 2N work items and N records
+            cap_items, cap_recs = 2 * N, N
+            qkv = torch.empty((3,) + tuple(out.shape), dtype=plan.dtype, device=dev)
+            tok_stack = torch.stack([torch.stack(t) for t in tokens_all])
+            graphs = []
+            for j in range(2):
+                pc, btj, slj, itj, rcj, tsj, cj = staging.capacity_views(j, cap_items, cap_recs)
+
+                def device_step(pc=pc, btj=btj, slj=slj, itj=itj, rcj=rcj, tsj=tsj, cj=cj):
+                    B.block_copy([kc], [vc], pc)
+                    B.paged_attn_decode_append(qkv[0], qkv[1], qkv[2], kc, vc, btj, slj,
+                                               plan.scale, out=out, partition_tokens=pt,
+                                               workspace=ws, error_record=rec, work_items=itj,
+                                               shared_records=rcj,
+                                               tail_start=tsj if prefix else None, counts=cj)
+                side = torch.cuda.Stream(dev)
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    device_step()                 # counts 0, no pairs: nothing but the merge
+                stream.wait_stream(side)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    device_step()
+                graphs.append(g)
+            torch.cuda.synchronize()
         host_s, stage_s, plan_s, lens_seen, n_shared, n_prefix = 0.0, 0.0, 0.0, 0, 0, 0
-        launch_s = 0.0
+        launch_s, n_eager = 0.0, 0
         unique_seen = 0
         # per step: events before the upload, before the copies, before decode, after
         # (created before the loop: creating events costs host time every step)
@@ -1019,21 +1048,31 @@ def run_workload(args, rank, world, local_rank, emit=True):
             if evs:
                 evs[0].record(stream)
             h1 = time.perf_counter()
-            pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staging.upload(
-                s_, stream, pairs, len(items), len(recs), tails is not None)
+            captured = (graphs is not None and len(items) <= cap_items
+                        and len(recs) <= cap_recs)
+            n_eager += 0 if captured else 1
+            staged = staging.upload(s_, stream, pairs, len(items), len(recs), tails is not None,
+                                    pad=captured)
             stage_s += time.perf_counter() - h1
             if evs:
                 evs[1].record(stream)
             h3 = time.perf_counter()
-            if len(pairs):
-                B.block_copy([kc], [vc], pairs_d)
-            h4 = time.perf_counter()
-            if evs:
-                evs[2].record(stream)
-            h5 = time.perf_counter()
-            B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
-                                       partition_tokens=pt, workspace=ws, error_record=rec,
-                                       work_items=it_d, shared_records=rc_d, tail_start=ts_d)
+            if captured:
+                qkv.copy_(tok_stack[s_])
+                graphs[s_ % 2].replay()
+                h4 = h5 = time.perf_counter()
+            else:
+                pairs_d, bt_d, sl_d, it_d, rc_d, ts_d = staged
+                if len(pairs):
+                    B.block_copy([kc], [vc], pairs_d)
+                h4 = time.perf_counter()
+                if evs:
+                    evs[2].record(stream)
+                h5 = time.perf_counter()
+                B.paged_attn_decode_append(q, k, v, kc, vc, bt_d, sl_d, plan.scale, out=out,
+                                           partition_tokens=pt, workspace=ws, error_record=rec,
+                                           work_items=it_d, shared_records=rc_d,
+                                           tail_start=ts_d)
             launch_s += time.perf_counter() - h5 + h4 - h3
             if evs:
                 evs[3].record(stream)
@@ -1045,6 +1084,8 @@ def run_workload(args, rank, world, local_rank, emit=True):
         # the staged inputs of the last step gave the same output as direct uploads
         # (the fused append rewrites the same rows: idempotent)
         ref_out = torch.empty_like(out)
+        if B.pa_error_read(rec) != [0, 0, 0, 0]:
+            raise RuntimeError(f"device error record {B.pa_error_read(rec)}")
         B.paged_attn_decode_append(q, k, v, kc, vc, torch.from_numpy(tables).to(dev),
                                    torch.from_numpy(lens).to(dev), plan.scale, out=ref_out,
                                    partition_tokens=pt, workspace=ws, error_record=rec,
@@ -1069,6 +1110,11 @@ def run_workload(args, rank, world, local_rank, emit=True):
                                          f"shared partitions ({n_shared / plan.steps:.1f} "
                                          f"records per step, {n_prefix / plan.steps:.1f} "
                                          "of them prefix records) + work list"),
+                            "device_step": ("copies + fused append and decode replayed from "
+                                            "a CUDA graph (lists sized by device-side counts; "
+                                            f"{n_eager} of {plan.steps} steps launched eagerly "
+                                            "for want of room)"
+                                            if graphs is not None else "eager launches"),
                             "l2": "inputs larger than L2"},
                     dtype="f16", host_allocator_ms_per_step=round(1e3 * host_s / plan.steps, 4),
                     host_staging_ms_per_step=round(1e3 * stage_s / plan.steps, 4),
@@ -1078,10 +1124,14 @@ def run_workload(args, rank, world, local_rank, emit=True):
                     unique_kv_gbs=round(unique_kv / (ms * 1e-3) / 1e9, 1),
                     unique_kv_frac_of_peak=round(unique_kv / (ms * 1e-3) / 1e9 / peak, 4),
                     wall_ms_per_step=round(1e3 * wall, 4),
-                    device_ms_per_step_split={
-                        "table_uploads": seg(0, 1), "block_copy": seg(1, 2),
-                        "append_and_decode": seg(2, 3),
-                        "note": "the append is fused into the decode launch; " + SPLIT_NOTE},
+                    device_ms_per_step_split=(
+                        {"table_uploads": seg(0, 1), "copies_append_and_decode": seg(1, 3),
+                         "note": "one graph: copies, then the append fused into the decode; "
+                                 + SPLIT_NOTE}
+                        if graphs is not None else
+                        {"table_uploads": seg(0, 1), "block_copy": seg(1, 2),
+                         "append_and_decode": seg(2, 3),
+                         "note": "the append is fused into the decode launch; " + SPLIT_NOTE}),
                     note="value counts K/V bytes only; device time includes copies, H2D "
                          "of tables (staged in pinned memory, two buffer sets) and the decode")
     elif w == "beam":
@@ -1644,7 +1694,7 @@ def main(argv=None):
                     help="sampling/beam/mixed: read shared partitions once per sequence "
                          "instead of once per group")
     ap.add_argument("--no-graph", action="store_true",
-                    help="beam: launch each step's copies and decode eagerly instead of "
+                    help="beam/mixed: launch each step's copies and decode eagerly instead of "
                          "replaying them from a CUDA graph")
     ap.add_argument("--no-prefix", action="store_true",
                     help="beam/mixed: share whole partitions only, not the shared first "
