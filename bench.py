@@ -794,7 +794,9 @@ def run_workload(args, rank, world, local_rank, emit=True):
             fn = lambda: B.paged_attn_decode(b.q, b.k_cache, b.v_cache, bt, sl, b.scale, **kw)
         flush = None
         if w == "tiny":
-            scratch = torch.empty(2 * 132 * 2 ** 20, dtype=torch.uint8, device=dev)
+            # 1 GiB written between calls: more than L2, and long enough (~0.15 ms)
+            # that the host has enqueued the timed call before the GPU gets to it
+            scratch = torch.empty(2 ** 30, dtype=torch.uint8, device=dev)
             flush = lambda: scratch.fill_(1)
         ms = _time_device(fn, K, W, stream, flush)
         nb = step_bytes(b.context_lens, b.num_heads, b.head_dim, b.block_size,
